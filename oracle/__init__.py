@@ -1,0 +1,23 @@
+"""CPU oracle for the fused attention forward pass -- TEST INFRASTRUCTURE ONLY.
+
+Plain, slow, float64 restatements of what the pages define. Only ``tests/``,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may import
+or execute anything in this package; the library under
+``online_softmax_fwd_gb300/`` never does, and this package never imports it.
+
+Modules
+  attention      one-shot softmax(Q K^T s) V and LSE (the definition), plus the
+                 blockwise online recurrence used only to check the definition
+                 against the identities the pages state.
+  exp2_model     the software exp2 (range reduction + degree-3 Horner) as a
+                 NumPy model, and its accuracy statistics.
+  cmodel         ctypes loader for ``exp2_model.c``: the same software exp2 in
+                 scalar C with a fused multiply-add, for bit-exact comparison.
+  rescale_stats  the lagging-max (tau) rescale simulator and its statistics.
+  mxfp8          the E4M3 / E8M0 32x32 block quantiser and its dequantisation.
+
+Parity pins (tests/test_oracle_*.py, marked "not gpu") tie every function here
+to something other than itself: brute force, closed forms, and the numbers the
+pages print. Degree-4 and degree-5 software exp2 are not built: their
+coefficients are not printed, so they would be parity unpinned.
+"""
