@@ -1,0 +1,360 @@
+"""Benchmark of the fused attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--exp2-emu16 E] [--tau T]
+
+A step is one attention forward (O and LSE) over the whole workload, inputs
+resident in HBM (Q, K, V together exceed the 129 MB L2, so no flush is
+needed). Prints one JSON line on rank 0. Under torchrun each rank runs the
+same workload on its own GPU (weak scaling, no data-path collective); the
+timed region is bracketed by a barrier and a device synchronisation and the
+slowest rank's time is reported.
+
+``--impl reference`` times the float64 CPU oracle instead, on a bounded sample
+of the same workload per step (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import attn_inputs as I  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s on 1xGB300 and fraction of dense BF16/FP8 peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = I.NONCAUSAL_D128.name
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = ["online_softmax_fwd_gb300/csrc/fwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/ptx.cuh",
+                  "online_softmax_fwd_gb300/csrc/exp2_fma.cuh"]
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+def profiled_traffic(workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if it was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"fwd_bf16_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    sha = re.search(r"kernel_sources_sha:\s*([0-9a-f]+)", text)
+    val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not sha or not val or sha.group(1) != kernel_sources_sha():
+        return None
+    return float(val.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples: list[tuple[float, list[str]]] = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        window = "timed_region"
+        if not inside:
+            # the timed region was shorter than one sampling period: use the
+            # samples closest to it
+            near = sorted(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))[:3]
+            inside = [s for _, s in near]
+            window = "nearest_samples"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no_samples"], "window": "none"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in inside if num(s[0]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4) if len(s) > 3 + i and s[3 + i] == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": num(inside[0][1]),
+                "power_w_max": max((num(s[2]) or 0.0) for s in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(w: I.Workload, q, k, v, seconds: float, rows_per_call: int = 512) -> dict:
+    """Time the float64 oracle on consecutive row chunks of the workload's
+    first heads until `seconds` have passed (at least one chunk). Returns the
+    sample description and its rate in the metric's units (useful FLOP of the
+    computed rows, causal rows counting only their allowed keys)."""
+    from oracle.attention import attention_rows
+    t0 = time.perf_counter()
+    flops = 0.0
+    rows_done = 0
+    heads = 0
+    for b in range(w.B):
+        for h in range(w.H):
+            kk, vv = I.as_f64(k[b, h]), I.as_f64(v[b, h])
+            for r0 in range(0, w.N, rows_per_call):
+                r1 = min(w.N, r0 + rows_per_call)
+                idx = np.arange(r0, r1)
+                attention_rows(I.as_f64(q[b, h, r0:r1]), kk, vv, idx, w.causal, w.scale)
+                keys = (idx + 1).sum() if w.causal else (r1 - r0) * w.N
+                flops += 4.0 * keys * w.d
+                rows_done += r1 - r0
+                if time.perf_counter() - t0 >= seconds:
+                    break
+            heads += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "seconds": dt, "rows": rows_done, "heads_touched": heads,
+            "flop": flops}
+
+
+def bench_reference(args, w: I.Workload, world: int, rank: int) -> None:
+    if rank != 0:
+        return
+    q, k, v = I.bf16_qkv(w) if w.dtype == "bf16" else tuple(I.to_bf16(x) for x in I.draw_fp32(
+        w.B, w.H, w.N, w.d, w.qk_std, w.v_std, w.seed))
+    cores = torch.get_num_threads()
+    per_step = max(1.0, args.reference_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(w, q, k, v, per_step)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        s = oracle_sample(w, q, k, v, per_step)
+        vals.append(s["value"])
+        secs.append(s["seconds"])
+    value = float(np.mean(vals))
+    sample = (f"float64 one-shot oracle on the first {s['rows']} query rows (512-row chunks, all {w.N} keys) "
+              f"of the workload per step, ~{per_step:.0f} s per step")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(secs)), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {**w.describe(), "workload": w.name},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
+    import online_softmax_fwd_gb300 as attn
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    attn.lib()
+    q_h, k_h, v_h = I.bf16_qkv(w)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
+
+    def step():
+        st = attn.attn_fwd_raw(*ptrs, w.B, w.H, w.N, w.d, int(w.causal), float(w.scale), sh,
+                               tau=args.tau, exp2_emu16=args.exp2_emu16)
+        if st != 0:
+            raise attn.AttnError(st, "attn_fwd")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.5)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    region0 = torch.cuda.Event(enable_timing=True)
+    region1 = torch.cuda.Event(enable_timing=True)
+    region0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    region1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t_wall1 = time.time()
+    time.sleep(0.3)
+    sampler.stop()
+    st = attn.device_status()
+    if st != attn.Status.OK:
+        raise RuntimeError(f"device status after the timed region: {st!r}")
+    region_ms = region0.elapsed_time(region1)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    region_ms_max = max_over_ranks(region_ms, world, dev)
+    total_flop = w.flops * args.steps * world
+    value = total_flop / (region_ms_max * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, host O and LSE out
+    e2e = None
+    if not args.no_e2e:
+        qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
+        o_host = torch.empty_like(qp).pin_memory()
+        lse_host = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+        ws = {}
+        for _ in range(2):
+            attn.attn_fwd_from_host(qp, kp, vp, w.causal, w.scale, device=dev, o_host=o_host, lse_host=lse_host,
+                                    workspace=ws)
+        n_e2e = max(3, min(args.steps, 10))
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            attn.attn_fwd_from_host(qp, kp, vp, w.causal, w.scale, device=dev, o_host=o_host, lse_host=lse_host,
+                                    workspace=ws)
+        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+        e2e = {"value": w.flops * n_e2e * world / dt / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": 3 * q_h.numel() * 2, "d2h_bytes_per_step": o_host.numel() * 2 + lse_host.numel() * 4,
+               "steps": n_e2e}
+
+    peaks = measured_peaks()
+    peak = peaks.get("bf16_tflops")
+    avg_launch_s = float(np.mean(launch_ms)) * 1e-3
+    achieved = w.flops / avg_launch_s / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": (achieved / peak) if peak else None, "traffic": profiled_traffic(w.name),
+                "peak_source": "measured bf16_tflops (burst, cuBLAS)" if peak else "fallback 1900",
+                "flop_per_launch": w.flops}
+    if not peak:
+        roofline["peak"] = 1900.0
+        roofline["frac"] = achieved / 1900.0
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s = oracle_sample(w, q_h, k_h, v_h, args.cpu_seconds)
+        cpu = {"value": s["value"], "unit": UNIT, "cores": torch.get_num_threads(), "kind": "oracle",
+               "sample": f"float64 one-shot oracle on {s['rows']} query rows of the workload's first "
+                         f"{s['heads_touched']} head(s) against all their keys, {s['seconds']:.1f} s"}
+    clocks = sampler.summary(t_wall0, t_wall1)
+    if rank == 0:
+        out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+               "warmup": args.warmup, "ms_per_step": region_ms_max / args.steps, "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+               "config": {**w.describe(), "parallelism": f"replicas{world}" if world > 1 else "single",
+                          "l2": f"inputs larger than L2 (Q+K+V = {3 * q.numel() * 2 / 2**20:.0f} MiB > 129 MB)",
+                          "tau": args.tau, "exp2_emu16": args.exp2_emu16},
+               "e2e": e2e, "gpu_launches": args.steps, "roofline": roofline, "cpu_baseline": cpu,
+               "clocks": clocks, "kernel_ms": {"mean": float(np.mean(launch_ms)), "min": float(np.min(launch_ms)),
+                                               "max": float(np.max(launch_ms))}}
+        print(json.dumps(out), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--exp2-emu16", type=int, default=0)
+    ap.add_argument("--tau", type=float, default=8.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-seconds", type=float, default=60.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = I.WORKLOADS[args.workload]
+    if w.dtype != "bf16" and args.impl == "ours":
+        ap.error(f"{w.name}: only the bf16 workloads are benchmarked by this build")
+    world, rank, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            bench_reference(args, w, world, rank)
+        else:
+            bench_ours(args, w, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

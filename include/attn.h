@@ -1,0 +1,123 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) fused attention forward library.
+ *
+ * The library computes, for every batch b, head h and query row i,
+ *
+ *     O[b,h,i,:] = sum_j softmax_j( scale * <Q[b,h,i,:], K[b,h,j,:]> ) * V[b,h,j,:]
+ *     LSE[b,h,i] = log sum_j exp( scale * <Q[b,h,i,:], K[b,h,j,:]> )
+ *
+ * over the allowed keys j (all j, or j <= i when causal). This is the
+ * attention of "Flash Attention 4 - the algorithm and the two-MMA problem"
+ * (section "The memory-bound trap") with the per-row log-sum-exp side output
+ * of "Lecture 2 - Online Softmax and Numerical Correctness" (sections "The
+ * classical safe softmax" and "Use it in the real stack"). It is computed
+ * with the online-softmax recurrence over streamed 128-key blocks (same
+ * lecture pages, "Online softmax - three running states" and "Deferred
+ * normalization"), the exp2 fold of the scale ("The exp2 trick"), causal block
+ * skipping with a diagonal -inf mask ("Causal masking just changes which
+ * blocks contribute") and the lagging-max conditional rescale with threshold
+ * tau of "FlashAttention-4's Softmax Tricks" ("Conditional rescaling").
+ *
+ * Conventions shared by every entry point
+ *   - Layout: Q, K, V and O are contiguous row-major [B, H, N, d] (d fastest);
+ *     LSE is contiguous [B, H, N]. Element (b,h,i,c) is at ((b*H + h)*N + i)*d + c.
+ *   - Ownership: the caller allocates and owns every buffer; the attention
+ *     entry points allocate no memory. Pointers are device pointers unless a
+ *     parameter says otherwise.
+ *   - Execution: calls are asynchronous on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and run on the device current to the calling
+ *     thread. Arguments are checked on the host before anything is launched;
+ *     a rejected call launches nothing and changes no buffer.
+ *   - Thread safety: the library keeps no per-call state; concurrent calls on
+ *     different streams are safe if their output buffers do not overlap.
+ *   - Errors: every entry point returns an attn_status_t, never aborts.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null pointer, negative size, non-finite or non-positive scale, ... */
+  ATTN_ERR_UNSUPPORTED = 2, /* a well-formed request this build does not implement (e.g. d = 96) */
+  ATTN_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
+  ATTN_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed (launch, tensor map, ...) */
+  ATTN_ERR_TIMEOUT = 5      /* a kernel gave up waiting on a pipeline barrier (see attn_get_device_status) */
+} attn_status_t;
+
+/*
+ * attn_fwd -- bf16 attention forward with the per-row LSE.
+ *
+ *   q, k, v  const bf16 [B,H,N,d], device, 16-byte aligned.
+ *   o        bf16 [B,H,N,d], device, 16-byte aligned; written, rounded to nearest even.
+ *   lse      float [B,H,N], device, 4-byte aligned; natural-log units of the
+ *            scaled scores: LSE_i = scale * m_i + ln(sum_j exp(scale * (s_ij - m_i))).
+ *   B, H, N  >= 0. Any of them 0: nothing to do, returns ATTN_OK. N <= 2^24.
+ *            N need not be a multiple of 128 (the last key block and the last
+ *            query tile are masked).
+ *   d        64 or 128 (others: ATTN_ERR_UNSUPPORTED).
+ *   causal   0: every key is allowed; 1: key j is allowed for query i iff j <= i.
+ *   scale    finite and > 0 (1/sqrt(d) in the usual use). The running max is
+ *            taken on raw scores, which is the same as on scaled ones only for
+ *            scale > 0.
+ *   stream   cudaStream_t.
+ * Uses tau = 8 (log2 units) and the MUFU exp2 for every element.
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                       int N, int d, int causal, float scale, void* stream);
+
+/*
+ * attn_fwd_ex -- attn_fwd with the two softmax tunables exposed.
+ *
+ *   tau          rescale threshold in log2 units of the scaled score, >= 0
+ *                ("FlashAttention-4's Softmax Tricks", section "Conditional
+ *                rescaling": the running max moves only when it would grow by
+ *                more than tau). 8 for bf16 P; 0 gives the classic rescale on
+ *                every growth. Must be <= 16 so that P <= 2^tau stays far
+ *                below the bf16 range.
+ *   exp2_emu16   how many of every 16 columns of a score row take the software
+ *                exp2 on the FMA pipe instead of the MUFU ex2 (same page,
+ *                section "The emulated exp2"; the page's fractions 6.25%,
+ *                12.5%, 18.75%, 25% are 1, 2, 3, 4 of 16). 0..4 are built;
+ *                others give ATTN_ERR_UNSUPPORTED. Masked key blocks (the
+ *                causal diagonal and a ragged tail) always use the MUFU.
+ * Other arguments as attn_fwd.
+ */
+attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                          int N, int d, int causal, float scale, float tau, int exp2_emu16, void* stream);
+
+/*
+ * attn_exp2_emulated -- y[i] = software exp2 of x[i] for i < n, computed by
+ * the very device function the attention kernels use on the FMA pipe (see
+ * attn_fwd_ex). For checking that function bit for bit against a scalar model.
+ *   x, y   float, device, n elements each (may not overlap unless x == y).
+ *   n      >= 0.
+ */
+attn_status_t attn_exp2_emulated(const float* x, float* y, long long n, void* stream);
+
+/*
+ * attn_get_device_status -- synchronise `stream`, then report and clear the
+ * device-side error word of the current device. Every pipeline wait inside the
+ * kernels has an iteration/time limit (about two seconds); a wait that runs out
+ * records ATTN_ERR_TIMEOUT there and its kernel drains and exits instead of
+ * hanging. Returns ATTN_OK if no kernel recorded an error since the last call.
+ */
+attn_status_t attn_get_device_status(void* stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* attn_status_string(attn_status_t status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

@@ -1,0 +1,11 @@
+"""GB300 (sm_103a) fused attention forward with the online-softmax recurrence.
+
+The computation lives in ``libattn.so`` (CUDA sources under ``csrc/``, C ABI in
+``include/attn.h``); this package only binds it. Build it with
+``python -m online_softmax_fwd_gb300.build``.
+"""
+from ._binding import (AttnError, Status, attn_fwd, attn_fwd_from_host, attn_fwd_raw, device_status,
+                       exp2_emulated, lib, status_string, version)
+
+__all__ = ["AttnError", "Status", "attn_fwd", "attn_fwd_from_host", "attn_fwd_raw", "device_status",
+           "exp2_emulated", "lib", "status_string", "version"]

@@ -1,0 +1,195 @@
+"""ctypes binding of ``libattn.so`` (the C ABI declared in include/attn.h).
+
+Argument marshalling only: torch tensors supply device memory and the current
+CUDA stream; every step of the computation runs in the library's kernels.
+There is no fallback: if the shared library is missing or cannot be loaded,
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn.so")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    INVALID_ARG = 1
+    UNSUPPORTED = 2
+    MISALIGNED = 3
+    CUDA = 4
+    TIMEOUT = 5
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = Status(status) if status in Status._value2member_map_ else status
+        super().__init__(f"{what}: {self.status!r}")
+
+
+_SIGNATURES = {
+    # q, k, v, o, lse, B, H, N, d, causal, scale, stream
+    "attn_fwd": ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_void_p], ctypes.c_int),
+    # ..., scale, tau, exp2_emu16, stream
+    "attn_fwd_ex": ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
+                    + [ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
+    "attn_exp2_emulated": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p], ctypes.c_int),
+    "attn_get_device_status": ([ctypes.c_void_p], ctypes.c_int),
+    "attn_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "attn_version": ([], ctypes.c_int),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load libattn.so once; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with `python -m online_softmax_fwd_gb300.build` "
+                    "(there is no CPU or PyTorch fallback)")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (argtypes, restype) in _SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.argtypes = argtypes
+                fn.restype = restype
+            _lib = handle
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise AttnError(status, what)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _check_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> tuple[int, int, int, int]:
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor [B,H,N,d]")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError(f"q, k, v shapes differ: {tuple(q.shape)} {tuple(k.shape)} {tuple(v.shape)}")
+    B, H, N, d = q.shape
+    return B, H, N, d
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+             scale: float | None = None, o: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+             tau: float = 8.0, exp2_emu16: int = 0, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """O = softmax(scale * Q K^T [causal mask]) V and LSE, through the C ABI.
+
+    q, k, v: contiguous CUDA bf16 [B,H,N,d]. Returns (o bf16 [B,H,N,d],
+    lse float32 [B,H,N]); pass ``o`` / ``lse`` to write into existing buffers.
+    ``tau`` and ``exp2_emu16`` select attn_fwd_ex (defaults = attn_fwd).
+    """
+    B, H, N, d = _check_qkv(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if o.shape != q.shape or o.dtype != torch.bfloat16 or not o.is_contiguous() or o.device != q.device:
+        raise ValueError("o must be a contiguous bf16 tensor shaped like q on q's device")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous() or lse.device != q.device:
+        raise ValueError("lse must be a contiguous float32 tensor [B,H,N] on q's device")
+    h = _stream_handle(stream)
+    with torch.cuda.device(q.device):
+        if tau == 8.0 and exp2_emu16 == 0:
+            st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(bool(causal)),
+                                float(scale), h)
+            _check(st, "attn_fwd")
+        else:
+            st = lib().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                   int(bool(causal)), float(scale), float(tau), int(exp2_emu16), h)
+            _check(st, "attn_fwd_ex")
+    return o, lse
+
+
+def attn_fwd_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int, causal: int,
+                 scale: float, stream: int, tau: float = 8.0, exp2_emu16: int = 0) -> int:
+    """The C entry point with plain integers (device addresses); returns the status."""
+    if tau == 8.0 and exp2_emu16 == 0:
+        return lib().attn_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, stream)
+    return lib().attn_fwd_ex(q, k, v, o, lse, B, H, N, d, causal, scale, tau, exp2_emu16, stream)
+
+
+def attn_fwd_from_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                       scale: float | None = None, device: int | torch.device = 0,
+                       o_host: torch.Tensor | None = None, lse_host: torch.Tensor | None = None,
+                       workspace: dict | None = None, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """End-to-end call with host tensors: copy Q, K, V (pinned CPU bf16) to the
+    device, run attn_fwd, copy O and LSE back into host tensors. ``workspace``
+    (a dict) keeps the device buffers between calls of the same shape."""
+    B, H, N, d = q.shape
+    dev = torch.device("cuda", device) if isinstance(device, int) else device
+    ws = workspace if workspace is not None else {}
+    key = (B, H, N, d, str(dev))
+    if ws.get("key") != key:
+        ws.clear()
+        ws["key"] = key
+        ws["q"] = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+        ws["k"] = torch.empty_like(ws["q"])
+        ws["v"] = torch.empty_like(ws["q"])
+        ws["o"] = torch.empty_like(ws["q"])
+        ws["lse"] = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    ws["q"].copy_(q, non_blocking=True)
+    ws["k"].copy_(k, non_blocking=True)
+    ws["v"].copy_(v, non_blocking=True)
+    attn_fwd(ws["q"], ws["k"], ws["v"], causal, scale, o=ws["o"], lse=ws["lse"], stream=stream)
+    if o_host is None:
+        o_host = torch.empty((B, H, N, d), dtype=torch.bfloat16, pin_memory=True)
+    if lse_host is None:
+        lse_host = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
+    o_host.copy_(ws["o"], non_blocking=True)
+    lse_host.copy_(ws["lse"], non_blocking=True)
+    torch.cuda.current_stream(dev).synchronize()
+    return o_host, lse_host
+
+
+def exp2_emulated(x: torch.Tensor, stream=None) -> torch.Tensor:
+    """The kernels' software exp2 applied elementwise (float32 CUDA tensor)."""
+    if not x.is_cuda or x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA float32 tensor")
+    y = torch.empty_like(x)
+    with torch.cuda.device(x.device):
+        _check(lib().attn_exp2_emulated(_ptr(x), _ptr(y), x.numel(), _stream_handle(stream)),
+               "attn_exp2_emulated")
+    return y
+
+
+def device_status(stream=None) -> Status:
+    """Synchronise and read (and clear) the device error word."""
+    return Status(lib().attn_get_device_status(_stream_handle(stream)))
+
+
+def status_string(status: int) -> str:
+    return lib().attn_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return lib().attn_version()

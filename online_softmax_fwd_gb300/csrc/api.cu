@@ -1,0 +1,179 @@
+// C ABI of the attention forward library: argument checks, TMA tensor maps,
+// dispatch to the kernel instantiations, the device error word and the
+// software-exp2 check kernel. See include/attn.h for the contract.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn.h"
+#include "exp2_fma.cuh"
+#include "fwd_bf16.cuh"
+#include "fwd_dispatch.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr long long kMaxN = 1LL << 24;
+
+// Device error word, one per device (each device holds its own copy).
+__device__ unsigned int g_attn_status;
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Address of g_attn_status on the current device (looked up once per device).
+unsigned int* status_word() {
+  static std::atomic<unsigned int*> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  unsigned int* p = cache[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_attn_status) != cudaSuccess) return nullptr;
+  p = static_cast<unsigned int*>(addr);
+  cache[dev].store(p, std::memory_order_release);
+  return p;
+}
+
+// 3-D map over a contiguous [B*H, N, d] bf16 tensor: d innermost, 64-column
+// boxes (128 bytes, the 128-byte swizzle span) of 128 rows; rows past N of a
+// head read as zero.
+bool make_map(CUtensorMap* m, const void* base, int d, int n, long long bh) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2u, static_cast<cuuint64_t>(d) * 2u * static_cast<cuuint64_t>(n)};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+attn_status_t check_fwd_args(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,
+                             int H, int N, int d, int causal, float scale, float tau, int emu16, bool* empty) {
+  *empty = false;
+  if (B < 0 || H < 0 || N < 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(tau) || tau < 0.f || tau > 16.f) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return (d > 0) ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
+  if (emu16 < 0 || emu16 > 16) return ATTN_ERR_INVALID_ARG;
+  if (emu16 > 4) return ATTN_ERR_UNSUPPORTED;
+  if (N > kMaxN) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || N == 0) {
+    *empty = true;
+    return ATTN_OK;
+  }
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+  return ATTN_OK;
+}
+
+__global__ void exp2_emulated_kernel(const float* __restrict__ x, float* __restrict__ y, long long n) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    y[i] = attn::exp2_fma(x[i]);
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                          int d, int causal, float scale, float tau, int exp2_emu16, void* stream) {
+  bool empty = false;
+  attn_status_t st = check_fwd_args(q, k, v, o, lse, B, H, N, d, causal, scale, tau, exp2_emu16, &empty);
+  if (st != ATTN_OK || empty) return st;
+  const long long bh = static_cast<long long>(B) * H;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, d, N, bh) || !make_map(&mk, k, d, N, bh) || !make_map(&mv, v, d, N, bh))
+    return ATTN_ERR_CUDA;
+  unsigned int* status = status_word();
+  if (!status) return ATTN_ERR_CUDA;
+  attn::FwdArgs a;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.status = status;
+  a.n = N;
+  a.n_kv_blocks = (N + 127) / 128;
+  a.scale = scale;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.tau = tau;
+  const int n_pairs = (N + 255) / 256;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (d == 64)
+    e = causal ? attn::launch_fwd_bf16_d64_c1(exp2_emu16, mq, mk, mv, a, static_cast<int>(bh), n_pairs, s)
+               : attn::launch_fwd_bf16_d64_c0(exp2_emu16, mq, mk, mv, a, static_cast<int>(bh), n_pairs, s);
+  else
+    e = causal ? attn::launch_fwd_bf16_d128_c1(exp2_emu16, mq, mk, mv, a, static_cast<int>(bh), n_pairs, s)
+               : attn::launch_fwd_bf16_d128_c0(exp2_emu16, mq, mk, mv, a, static_cast<int>(bh), n_pairs, s);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                       int causal, float scale, void* stream) {
+  return attn_fwd_ex(q, k, v, o, lse, B, H, N, d, causal, scale, 8.0f, 0, stream);
+}
+
+attn_status_t attn_exp2_emulated(const float* x, float* y, long long n, void* stream) {
+  if (n < 0) return ATTN_ERR_INVALID_ARG;
+  if (n == 0) return ATTN_OK;
+  if (!x || !y) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 3u) || (reinterpret_cast<uintptr_t>(y) & 3u)) return ATTN_ERR_MISALIGNED;
+  const long long want = (n + 255) / 256;
+  const int blocks = static_cast<int>(want < 152 * 16 ? want : 152 * 16);
+  exp2_emulated_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, y, n);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_get_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  unsigned int* p = status_word();
+  if (!p) return ATTN_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, p, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (word == 0) return ATTN_OK;
+  const unsigned int zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+  const unsigned int code = word & 0xffu;
+  return code == ATTN_ERR_TIMEOUT ? ATTN_ERR_TIMEOUT : ATTN_ERR_CUDA;
+}
+
+const char* attn_status_string(attn_status_t status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+  }
+  return "ATTN_ERR_UNKNOWN";
+}
+
+int attn_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,437 @@
+// Fused attention forward, bf16 in / bf16 O + fp32 LSE out, for sm_103a.
+//
+// One CTA owns two 128-row query tiles of one (batch, head) -- the two Q tiles
+// in ping-pong of the FA4 forward pipeline ("Software-Emulated Exponential",
+// KernelWiki; "PyTorch FlashAttention-4 adds MXFP8", section "TMEM allocation")
+// -- and streams the head's keys and values in 128-row blocks:
+//
+//   warp 8      TMA producer: Q0, Q1 once; then K_j, V_j into a ring of
+//               128 x d bf16 shared-memory slots (128-byte swizzle).
+//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T (tcgen05, both operands
+//               in shared memory, fp32 accumulator in TMEM) and O_t += P_t V_j
+//               (A operand P_t read from TMEM, V_j from shared memory).
+//   warps 0-3   softmax for tile 0, warps 4-7 for tile 1; thread = query row.
+//
+// Per key block j, a softmax thread (row i) follows the online recurrence of
+// "Flash Attention 4 - the algorithm and the two-MMA problem" ("Online softmax
+// - three running states", "Deferred normalization", "The exp2 trick"):
+//   load its 128 scores from TMEM; mask keys j > i on the causal diagonal block
+//   and keys >= N in a ragged last block ("Lecture 2 - Online Softmax and
+//   Numerical Correctness", "Causal masking just changes which blocks
+//   contribute"); take the block max of the raw scores; move the running max
+//   only if it would grow by more than tau in log2 units, else keep the stale
+//   max ("FlashAttention-4's Softmax Tricks", "Conditional rescaling": the
+//   SoftmaxSm100.update_row_max rule); if any row of the warp moved, rescale
+//   that warp's O rows in TMEM by 2^((m_old - m_new) s log2 e) (correction done
+//   in place: the MMA thread issues S_t(j) after O_t += P_t V_{j-1}, and tcgen05
+//   operations from one thread complete in order, so when S_t(j) is complete O_t
+//   is quiescent until this warp hands P_t(j) over); p = 2^(s log2e * S -
+//   s log2e * m) with one FFMA and then the MUFU ex2 or, for a compile-time
+//   share of the columns, the software exp2 on the FMA pipe; l += sum p in fp32;
+//   P rounded to bf16 and stored over the S columns it replaces.
+// After the last block: O / l rounded to bf16, and LSE = s m + ln l.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "exp2_fma.cuh"
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr uint32_t kStatusTimeout = 5;  // == ATTN_ERR_TIMEOUT
+
+struct FwdArgs {
+  __nv_bfloat16* o;
+  float* lse;
+  unsigned int* status;  // device error word
+  int n;                 // sequence length N
+  int n_kv_blocks;       // ceil(N / 128)
+  float scale;           // s
+  float scale_log2;      // s * log2(e)
+  float tau;             // rescale threshold, log2 units
+};
+
+template <int D>
+struct FwdCfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kBoxes = D / 64;                     // 64-column (128-byte) swizzle boxes per row
+  static constexpr uint32_t kBoxBytes = 128u * 128u;        // 128 rows x 128 bytes
+  static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;  // one 128 x d bf16 tile
+  static constexpr int kSlots = D == 128 ? 5 : 8;           // K/V ring depth
+  static constexpr uint32_t kRingOff = 2 * kTileBytes;      // after Q0, Q1
+  static constexpr uint32_t kBarOff = kRingOff + kSlots * kTileBytes;
+  // q_full, full[kSlots], empty[kSlots], s_full[2], p_full[2], o_final[2], drain
+  static constexpr int kNumBars = 1 + 2 * kSlots + 7;
+  static constexpr uint32_t kHolderOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kAbortOff = kHolderOff + 4;
+  static constexpr uint32_t kSmemBytes = kAbortOff + 4 + 1024;  // + slack for 1024-byte alignment
+  static constexpr int kThreads = 320;
+  static constexpr uint32_t kTmemCols = 512;
+  // TMEM columns: S_t (fp32, 128 columns; P_t as bf16 pairs over its first 64)
+  // and O_t (fp32, d columns) for the two query tiles.
+  __host__ __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
+  __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + (t ? D : 0); }
+};
+
+// ~2 s at the 2 GHz class SM clock.
+constexpr long long kWaitLimitCycles = 4000000000LL;
+constexpr long long kDrainLimitCycles = 200000000LL;
+
+__device__ __forceinline__ void record_status(unsigned int* status, uint32_t code, uint32_t where) {
+  atomicCAS(status, 0u, code | (where << 8));
+}
+
+// Wait for phase `parity` of an mbarrier, giving up when another role raised
+// the CTA's abort flag or after kWaitLimitCycles (then raising it).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                         unsigned int* status, uint32_t where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      *abort_flag = 1u;
+      record_status(status, kStatusTimeout, where);
+      return false;
+    }
+  }
+}
+
+// Bounded wait used only while draining after an abort.
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kDrainLimitCycles) return;
+  }
+}
+
+template <int EMU, bool MUFU_ONLY>
+__device__ __forceinline__ float exp2_col(int c, float x) {
+  if constexpr (!MUFU_ONLY && EMU > 0) {
+    if ((c & 15) < EMU) return exp2_fma(x);
+  }
+  return ex2_mufu(x);
+}
+
+// p = 2^(S*sl2 + neg_ms) for the 128 scores of a row, rounded to bf16 pairs
+// and stored to TMEM at p_tm; returns the fp32 sum of the unrounded p.
+template <int EMU, bool MUFU_ONLY>
+__device__ __forceinline__ float softmax_p_store(const float (&s)[128], float sl2, float neg_ms,
+                                                 uint32_t p_tm) {
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int chunk = 0; chunk < 4; ++chunk) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c0 = chunk * 32 + 2 * i;
+      const float p0 = exp2_col<EMU, MUFU_ONLY>(c0, __fmaf_rn(s[c0], sl2, neg_ms));
+      const float p1 = exp2_col<EMU, MUFU_ONLY>(c0 + 1, __fmaf_rn(s[c0 + 1], sl2, neg_ms));
+      acc[i & 3] += p0 + p1;
+      pk[i] = pack_bf16x2(p0, p1);
+    }
+    tmem_st16(p_tm + chunk * 16, pk);
+  }
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
+template <int D, bool CAUSAL, int EMU>
+__global__ void __launch_bounds__(320, 1)
+    attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  // 128-byte swizzle atoms need 1024-byte aligned tiles (shared-window address)
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t bar_q = sbase + C::kBarOff;
+  auto bar_full = [&](int i) { return bar_q + 8u * (1 + i); };
+  auto bar_empty = [&](int i) { return bar_q + 8u * (1 + C::kSlots + i); };
+  auto bar_s = [&](int t) { return bar_q + 8u * (1 + 2 * C::kSlots + t); };
+  auto bar_p = [&](int t) { return bar_q + 8u * (3 + 2 * C::kSlots + t); };
+  auto bar_o = [&](int t) { return bar_q + 8u * (5 + 2 * C::kSlots + t); };
+  const uint32_t bar_drain = bar_q + 8u * (7 + 2 * C::kSlots);
+  uint32_t* holder = reinterpret_cast<uint32_t*>(smem + C::kHolderOff);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kAbortOff);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int pair = gridDim.y - 1 - blockIdx.y;  // heaviest causal pairs first
+  const int row0 = pair * 256;
+  const int nkv = args.n_kv_blocks;
+  const int n0 = CAUSAL ? min(2 * pair + 1, nkv) : nkv;  // key blocks of tile 0
+  const int n1 = CAUSAL ? min(2 * pair + 2, nkv) : nkv;  // key blocks of tile 1 (>= n0)
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int i = 0; i < C::kSlots; ++i) {
+      mbar_init(bar_full(i), 1);
+      mbar_init(bar_empty(i), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_s(t), 1);
+      mbar_init(bar_p(t), 128);
+      mbar_init(bar_o(t), 1);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_addr(holder), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *holder;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();
+      mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_3d_hint(sbase + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, bar_q, b * 64, row0 + 128 * t,
+                           bh, pol_q);
+      int seq = 0;
+      bool ok = true;
+      for (int j = 0; ok && j < n1; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const int slot = seq % C::kSlots;
+          const uint32_t ph = (seq / C::kSlots) & 1;
+          if (!wait_bar(bar_empty(slot), ph ^ 1u, abort_flag, args.status, 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar_full(slot), C::kTileBytes);
+          const CUtensorMap* map = kv ? &tm_v : &tm_k;
+#pragma unroll
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d_hint(sbase + C::kRingOff + slot * C::kTileBytes + b * C::kBoxBytes, map, bar_full(slot),
+                             b * 64, j * 128, bh, pol_kv);
+          ++seq;
+        }
+      }
+      if (!ok) {
+        // let the copies already in flight land before the CTA's memory is released
+        drain_bar(bar_q, 0);
+        for (int s = seq - C::kSlots < 0 ? 0 : seq - C::kSlots; s < seq; ++s)
+          drain_bar(bar_full(s % C::kSlots), (s / C::kSlots) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false);
+      constexpr uint32_t kIdO = idesc_bf16_f32(128, D, true);
+      auto k_slot = [&](int j) { return (2 * j) % C::kSlots; };
+      auto k_phase = [&](int j) { return static_cast<uint32_t>(((2 * j) / C::kSlots) & 1); };
+      auto v_slot = [&](int j) { return (2 * j + 1) % C::kSlots; };
+      auto v_phase = [&](int j) { return static_cast<uint32_t>(((2 * j + 1) / C::kSlots) & 1); };
+      auto issue_s = [&](int t, int j) {
+        const uint32_t qa = sbase + t * C::kTileBytes;
+        const uint32_t kb = sbase + C::kRingOff + k_slot(j) * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+          mma_ss(tmem + C::col_s(t), smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
+                 kIdS, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t vb = sbase + C::kRingOff + v_slot(j) * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, smem_desc_sw128(vb + kk * 2048, C::kBoxBytes, 1024),
+                 kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = wait_bar(bar_q, 0, abort_flag, args.status, 2) &&
+                wait_bar(bar_full(k_slot(0)), k_phase(0), abort_flag, args.status, 3);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        tc_commit(bar_s(0));
+        issue_s(1, 0);
+        tc_commit(bar_s(1));
+        tc_commit(bar_empty(k_slot(0)));
+      }
+      for (int j = 0; ok && j < n1; ++j) {
+        if (!wait_bar(bar_full(v_slot(j)), v_phase(j), abort_flag, args.status, 4)) break;
+        bool k_next_ready = false;
+        if (j < n0) {
+          if (!wait_bar(bar_p(0), j & 1, abort_flag, args.status, 5)) break;
+          tc_fence_after();
+          issue_pv(0, j);
+          if (j + 1 < n0) {
+            if (!wait_bar(bar_full(k_slot(j + 1)), k_phase(j + 1), abort_flag, args.status, 6)) break;
+            k_next_ready = true;
+            tc_fence_after();
+            issue_s(0, j + 1);
+            tc_commit(bar_s(0));
+          } else {
+            tc_commit(bar_o(0));
+          }
+        }
+        if (!wait_bar(bar_p(1), j & 1, abort_flag, args.status, 7)) break;
+        tc_fence_after();
+        issue_pv(1, j);
+        tc_commit(bar_empty(v_slot(j)));
+        if (j + 1 < n1) {
+          if (!k_next_ready) {
+            if (!wait_bar(bar_full(k_slot(j + 1)), k_phase(j + 1), abort_flag, args.status, 8)) break;
+            tc_fence_after();
+          }
+          issue_s(1, j + 1);
+          tc_commit(bar_s(1));
+          tc_commit(bar_empty(k_slot(j + 1)));
+        } else {
+          tc_commit(bar_o(1));
+        }
+      }
+      // nothing may still be executing when TMEM is released
+      tc_commit(bar_drain);
+      drain_bar(bar_drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int tile_row0 = row0 + 128 * t;
+    const int grow = tile_row0 + r;
+    const int nt = t ? n1 : n0;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t s_tm = tmem + lane_off + C::col_s(t);
+    const uint32_t o_tm = tmem + lane_off + C::col_o(t);
+    const float sl2 = args.scale_log2;
+    float m = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      ok = wait_bar(bar_s(t), j & 1, abort_flag, args.status, 16 + t);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      float s[128];
+      {
+        uint32_t u[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + 32 * c, u[c]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          reg_fence32(u[c]);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(u[c][i]);
+        }
+      }
+      const int kv0 = j * 128;
+      const bool need_mask = (kv0 + 128 > args.n) || (CAUSAL && kv0 + 127 > tile_row0);
+      if (need_mask) {
+        int lim = args.n - 1 - kv0;
+        if (CAUSAL) lim = min(lim, grow - kv0);
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > lim) s[c] = -INFINITY;
+      }
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+      const float bm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      // keep the stale max unless it would grow by more than tau (log2 units)
+      float m_new = fmaxf(m, bm);
+      const bool fire = !((m_new - m) * sl2 <= args.tau);
+      if (!fire) m_new = m;
+      // 0 while nothing has been accumulated (first block), 1 when the max stays
+      const float corr = fire ? (m == -INFINITY ? 0.f : ex2_mufu((m - m_new) * sl2)) : 1.0f;
+      m = m_new;
+      const float neg_ms = (m == -INFINITY) ? 0.f : -(m * sl2);
+      const float psum = need_mask ? softmax_p_store<EMU, true>(s, sl2, neg_ms, s_tm)
+                                   : softmax_p_store<EMU, false>(s, sl2, neg_ms, s_tm);
+      // correction of O after the scores are dead (lower register pressure);
+      // it still lands before P_t(j) is handed to the MMA thread below
+      if (j > 0 && __any_sync(0xffffffffu, fire)) {
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t ob[32];
+          tmem_ld32(o_tm + c, ob);
+          tmem_ld_wait();
+          reg_fence32(ob);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ob[i] = __float_as_uint(__uint_as_float(ob[i]) * corr);
+          tmem_st32(o_tm + c, ob);
+        }
+      }
+      l = l * corr + psum;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_p(t));
+    }
+    if (ok) {
+      ok = wait_bar(bar_o(t), 0, abort_flag, args.status, 18 + t);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.0f / l;
+      const bool valid = grow < args.n;
+      __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * args.n + (valid ? grow : 0)) * D;
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t ob[32];
+        tmem_ld32(o_tm + c, ob);
+        tmem_ld_wait();
+        reg_fence32(ob);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(ob[2 * i]) * inv_l, __uint_as_float(ob[2 * i + 1]) * inv_l);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+      if (valid) args.lse[static_cast<size_t>(bh) * args.n + grow] = (m * sl2 + lg2_mufu(l)) * 0.69314718055994531f;
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// Launch one instantiation: grid (B*H, ceil(N/256)), 320 threads, one CTA per SM.
+template <int D, bool CAUSAL, int EMU>
+cudaError_t launch_fwd_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                            const FwdArgs& args, int bh, int n_pairs, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kernel = attn_fwd_bf16_kernel<D, CAUSAL, EMU>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(bh, n_pairs);
+  kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, args);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

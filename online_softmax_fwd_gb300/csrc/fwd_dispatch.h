@@ -1,0 +1,20 @@
+// Host-side entry points of the per-(d, causal) kernel instantiation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+struct FwdArgs;
+
+cudaError_t launch_fwd_bf16_d64_c0(int emu16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                   const FwdArgs& a, int bh, int n_pairs, cudaStream_t s);
+cudaError_t launch_fwd_bf16_d64_c1(int emu16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                   const FwdArgs& a, int bh, int n_pairs, cudaStream_t s);
+cudaError_t launch_fwd_bf16_d128_c0(int emu16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                    const FwdArgs& a, int bh, int n_pairs, cudaStream_t s);
+cudaError_t launch_fwd_bf16_d128_c1(int emu16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                    const FwdArgs& a, int bh, int n_pairs, cudaStream_t s);
+
+}  // namespace attn

@@ -1,0 +1,57 @@
+"""Parity helpers shared by the GPU tests.
+
+Tolerances (the kernel's bf16 output against the float64 oracle on the same
+bf16 inputs):
+  * O, elementwise: |O - O_ref| <= max(1e-2, ulp_bf16(|O_ref|)). 1e-2 is the
+    required bound; one bf16 ulp at the reference's magnitude is added because a
+    bf16 output cannot be closer than half an ulp to O_ref and a correct fp32
+    value one rounding step away from O_ref's bf16 neighbour rounds to the other
+    side (|O| >= 2.56 is where half an ulp already exceeds 1e-2 for some values).
+  * O, mean over all compared elements: <= 1e-3.
+  * LSE: |LSE - LSE_ref| <= 1e-3.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+O_MAX_ABS = 1e-2
+O_MEAN_ABS = 1e-3
+LSE_MAX_ABS = 1e-3
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 numbers at |x| (8 significant bits)."""
+    ax = np.maximum(np.abs(x), np.float64(2.0 ** -126))
+    return np.ldexp(1.0, np.floor(np.log2(ax)).astype(np.int64) - 7)
+
+
+def compare(o, lse, o_ref, lse_ref, what: str = "") -> dict:
+    o = np.asarray(o, dtype=np.float64)
+    o_ref = np.asarray(o_ref, dtype=np.float64)
+    err = np.abs(o - o_ref)
+    bound = np.maximum(O_MAX_ABS, bf16_ulp(o_ref))
+    lerr = np.abs(np.asarray(lse, dtype=np.float64) - np.asarray(lse_ref, dtype=np.float64))
+    stats = {
+        "o_max_abs": float(err.max()) if err.size else 0.0,
+        "o_mean_abs": float(err.mean()) if err.size else 0.0,
+        "o_over_1e-2": int((err > O_MAX_ABS).sum()),
+        "o_over_bound": int((err > bound).sum()),
+        "lse_max_abs": float(lerr.max()) if lerr.size else 0.0,
+        "finite": bool(np.isfinite(o).all() and np.isfinite(lse).all()),
+    }
+    assert stats["finite"], f"{what}: non-finite output {stats}"
+    assert stats["o_over_bound"] == 0, f"{what}: O beyond tolerance {stats}"
+    assert stats["o_mean_abs"] <= O_MEAN_ABS, f"{what}: O mean error {stats}"
+    assert stats["lse_max_abs"] <= LSE_MAX_ABS, f"{what}: LSE error {stats}"
+    return stats
+
+
+def sample_rows(N: int, rng: np.random.Generator, n_random: int = 24) -> np.ndarray:
+    """Query rows to check at full size: the first rows, both sides of every
+    128-row tile edge within the first and last 512 rows, the last rows, and
+    random ones."""
+    fixed = [0, 1, 2, 3, 63, 64, 126, 127, 128, 129, 254, 255, 256, 257, 383, 384, 511, 512]
+    fixed += [N - 1, N - 2, N - 127, N - 128, N - 129, N - 255, N - 256, N - 257, N - 512]
+    rnd = rng.integers(0, N, size=n_random).tolist()
+    rows = sorted({r for r in fixed + rnd if 0 <= r < N})
+    return np.array(rows, dtype=np.int64)

@@ -1,0 +1,100 @@
+"""The C ABI library loads, exports every function include/attn.h declares, and
+rejects bad arguments on the host (no GPU needed: rejected calls never reach
+CUDA)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import online_softmax_fwd_gb300 as attn
+    return attn.lib()
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for want in ("attn_fwd", "attn_fwd_ex", "attn_exp2_emulated", "attn_get_device_status",
+                 "attn_status_string", "attn_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_function(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    raw = ctypes.CDLL(lib._name)
+    for name in declared_functions():
+        getattr(raw, name)  # raises AttributeError if the symbol is missing
+
+
+def test_version_and_strings(lib):
+    assert lib.attn_version() >= 100
+    assert lib.attn_status_string(0) == b"ATTN_OK"
+    assert lib.attn_status_string(5) == b"ATTN_ERR_TIMEOUT"
+    assert lib.attn_status_string(99) == b"ATTN_ERR_UNKNOWN"
+
+
+# fake, never dereferenced device addresses
+A = 0x10000
+GOOD = dict(q=A, k=A * 2, v=A * 3, o=A * 4, lse=A * 5, B=1, H=2, N=256, d=64, causal=0, scale=0.125)
+
+
+def call(lib, **over):
+    a = dict(GOOD, **over)
+    return lib.attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["d"],
+                        a["causal"], a["scale"], None)
+
+
+def call_ex(lib, tau=8.0, emu=0, **over):
+    a = dict(GOOD, **over)
+    return lib.attn_fwd_ex(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["d"],
+                           a["causal"], a["scale"], tau, emu, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(d=96), 2), (dict(d=256), 2), (dict(d=0), 1), (dict(d=-64), 1),
+    (dict(B=-1), 1), (dict(H=-3), 1), (dict(N=-1), 1), (dict(N=(1 << 24) + 1), 2),
+    (dict(causal=2), 1), (dict(scale=0.0), 1), (dict(scale=-0.1), 1), (dict(scale=float("inf")), 1),
+    (dict(scale=float("nan")), 1), (dict(q=0), 1), (dict(lse=0), 1),
+    (dict(q=A + 8), 3), (dict(o=A + 2), 3), (dict(lse=A + 2), 3),
+])
+def test_rejects_bad_arguments(lib, over, code):
+    assert call(lib, **over) == code
+
+
+@pytest.mark.parametrize("over", [dict(B=0), dict(H=0), dict(N=0), dict(B=0, q=0, k=0, v=0, o=0, lse=0)])
+def test_empty_problem_is_a_no_op(lib, over):
+    assert call(lib, **over) == 0
+
+
+@pytest.mark.parametrize("tau,emu,code", [(-1.0, 0, 1), (17.0, 0, 1), (float("nan"), 0, 1),
+                                          (8.0, -1, 1), (8.0, 5, 2), (8.0, 16, 2), (8.0, 17, 1)])
+def test_ex_rejects_bad_tunables(lib, tau, emu, code):
+    assert call_ex(lib, tau=tau, emu=emu) == code
+
+
+def test_exp2_entry_rejects_bad_arguments(lib):
+    assert lib.attn_exp2_emulated(A, A, -1, None) == 1
+    assert lib.attn_exp2_emulated(A, A, 0, None) == 0
+    assert lib.attn_exp2_emulated(0, A, 10, None) == 1
+    assert lib.attn_exp2_emulated(A + 2, A, 10, None) == 3
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import online_softmax_fwd_gb300._binding as b
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU or PyTorch fallback"):
+        b.lib()

@@ -1,0 +1,151 @@
+"""Parity of the CUDA path (through the C ABI) against the float64 oracle.
+
+Small shapes are compared element by element: several 128-row tiles, ragged
+tails, N = 1, both head dims, causal and not, every software-exp2 share, tau
+0 and 8, and degenerate inputs. The three bf16 long-sequence workloads run at
+full size in the launch configuration the benchmark times, checked on sampled
+rows that the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import attn_inputs as I
+from oracle.attention import attention_fwd, attention_rows
+from parity import compare, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module")
+def attn():
+    import online_softmax_fwd_gb300 as a
+    a.lib()
+    return a
+
+
+def run(attn, q, k, v, causal, scale, **kw):
+    o, lse = attn.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, scale=scale, **kw)
+    torch.cuda.synchronize()
+    assert attn.device_status() == attn.Status.OK
+    return o.cpu(), lse.cpu()
+
+
+def check_full(attn, q, k, v, causal, scale, what, **kw):
+    o, lse = run(attn, q, k, v, causal, scale, **kw)
+    o_ref, lse_ref = attention_fwd(I.as_f64(q), I.as_f64(k), I.as_f64(v), causal, scale)
+    return compare(I.as_f64(o), lse.double().numpy(), o_ref, lse_ref, what)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_workload(attn, causal):
+    w = I.TINY
+    q, k, v = I.bf16_qkv(w)
+    check_full(attn, q, k, v, causal, w.scale, f"{w.name} causal={causal}")
+
+
+SMALL = [(1, 1, 1, 64), (1, 1, 7, 128), (1, 2, 128, 64), (1, 1, 129, 128), (2, 3, 255, 64), (1, 2, 256, 128),
+         (1, 2, 257, 64), (1, 1, 300, 128), (2, 2, 640, 64), (1, 2, 1000, 128), (1, 1, 1024, 64)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
+def test_small_shapes(attn, shape, causal):
+    B, H, N, d = shape
+    q, k, v = (I.to_bf16(x) for x in I.draw_fp32(B, H, N, d, seed=N + d))
+    check_full(attn, q, k, v, causal, d ** -0.5, f"{shape} causal={causal}")
+
+
+@pytest.mark.parametrize("emu", [1, 2, 3, 4])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_software_exp2_shares(attn, emu, d, causal):
+    q, k, v = (I.to_bf16(x) for x in I.draw_fp32(1, 3, 1000, d, seed=5))
+    check_full(attn, q, k, v, causal, d ** -0.5, f"emu={emu} d={d}", exp2_emu16=emu)
+
+
+@pytest.mark.parametrize("tau", [0.0, 4.0, 8.0, 16.0])
+def test_rescale_thresholds(attn, tau):
+    # Q, K ~ N(0, 2^2): the running max keeps growing along the keys
+    q, k, v = (I.to_bf16(x) for x in I.draw_fp32(1, 2, 1536, 128, qk_std=2.0, seed=9))
+    check_full(attn, q, k, v, True, 128 ** -0.5, f"tau={tau}", tau=tau)
+
+
+def test_scores_rising_along_keys(attn):
+    # a ramp along the key order makes the max grow block after block, so the
+    # correction path fires many times
+    q, k, v = I.draw_fp32(1, 2, 1024, 64, seed=13)
+    q += 1.0
+    k += np.linspace(0.0, 1.5, 1024, dtype=np.float32)[None, None, :, None]
+    q, k, v = I.to_bf16(q), I.to_bf16(k), I.to_bf16(v)
+    for causal in (False, True):
+        check_full(attn, q, k, v, causal, 64 ** -0.5, f"ramp causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_queries_average_values(attn, causal):
+    _, k, v = (I.to_bf16(x) for x in I.draw_fp32(1, 2, 384, 64, seed=3))
+    q = torch.zeros_like(k)
+    o, lse = run(attn, q, k, v, causal, 0.125)
+    vv = I.as_f64(v)
+    n = np.arange(1, 385) if causal else np.full(384, 384)
+    mean = np.cumsum(vv, axis=2) / n[None, None, :, None] if causal else np.broadcast_to(
+        vv.mean(axis=2, keepdims=True), vv.shape)
+    compare(I.as_f64(o), lse.double().numpy(), mean, np.broadcast_to(np.log(n), (1, 2, 384)), "zero q")
+
+
+def test_large_scores(attn):
+    # scaled scores with a standard deviation near 16: P spans the full range
+    q, k, v = (I.to_bf16(x) for x in I.draw_fp32(1, 2, 512, 128, qk_std=4.0, seed=21))
+    for causal in (False, True):
+        check_full(attn, q, k, v, causal, 128 ** -0.5, f"large causal={causal}")
+
+
+def test_non_default_scale(attn):
+    q, k, v = (I.to_bf16(x) for x in I.draw_fp32(1, 2, 384, 64, seed=8))
+    check_full(attn, q, k, v, True, 0.37, "scale 0.37")
+
+
+def test_empty_problems(attn):
+    for shape in ((0, 2, 128, 64), (1, 0, 128, 64), (1, 2, 0, 64)):
+        q = torch.zeros(shape, dtype=torch.bfloat16, device=DEV)
+        o, lse = attn.attn_fwd(q, q, q)
+        assert o.shape == shape and lse.shape == shape[:3]
+    assert attn.device_status() == attn.Status.OK
+
+
+def test_repeat_calls_are_identical(attn):
+    q, k, v = (I.to_bf16(x).to(DEV) for x in I.draw_fp32(2, 2, 777, 128, seed=17))
+    o1, l1 = attn.attn_fwd(q, k, v, causal=True)
+    o2, l2 = attn.attn_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("w", [I.NONCAUSAL_D128, I.CAUSAL_D128_WIDE, I.CAUSAL_D64], ids=lambda w: w.name)
+def test_full_size_workloads_sampled(attn, w):
+    q, k, v = I.bf16_qkv(w)
+    o, lse = run(attn, q, k, v, w.causal, w.scale)
+    assert torch.isfinite(lse).all()
+    rng = np.random.default_rng(1)
+    heads = {(0, 0), (w.B - 1, w.H - 1), (int(rng.integers(w.B)), int(rng.integers(w.H)))}
+    for b, h in sorted(heads):
+        rows = sample_rows(w.N, rng)
+        o_ref, lse_ref = attention_rows(I.as_f64(q[b, h, rows]), I.as_f64(k[b, h]), I.as_f64(v[b, h]), rows,
+                                        w.causal, w.scale)
+        compare(I.as_f64(o[b, h, rows]), lse[b, h, rows].double().numpy(), o_ref, lse_ref,
+                f"{w.name} b={b} h={h}")
+
+
+def test_exp_bound_workload_with_software_share(attn):
+    w = I.CAUSAL_D64
+    q, k, v = I.bf16_qkv(w)
+    o, lse = run(attn, q, k, v, w.causal, w.scale, exp2_emu16=2)
+    rng = np.random.default_rng(2)
+    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
+        rows = sample_rows(w.N, rng)
+        o_ref, lse_ref = attention_rows(I.as_f64(q[b, h, rows]), I.as_f64(k[b, h]), I.as_f64(v[b, h]), rows,
+                                        w.causal, w.scale)
+        compare(I.as_f64(o[b, h, rows]), lse[b, h, rows].double().numpy(), o_ref, lse_ref, "d64 emu2")
