@@ -16,6 +16,7 @@ of the same workload per step (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -74,64 +75,97 @@ def profiled_traffic(workload: str) -> float | None:
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+    """SM clock, power and clock-event reasons sampled DURING the timed region.
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    Reads NVML through ctypes (about every millisecond, so even a short timed
+    region gets samples); falls back to ``nvidia-smi -lms 200`` when NVML
+    cannot be loaded. Only reads; changes no GPU setting."""
 
-    def __init__(self, index: int):
-        self.index = index
-        self.samples: list[tuple[float, list[str]]] = []
-        self.proc = None
-        self.thread = None
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device: torch.device):
+        self.samples: list[tuple[float, float, float, int]] = []  # (t, sm MHz, W, reasons)
+        self.max_mhz = None
+        self.source = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
+        self._nv = None
+        self._h = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            self._uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            self._uuid = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit")
+            h = ctypes.c_void_p()
+            if not self._uuid or nv.nvmlDeviceGetHandleByUUID(self._uuid.encode(), ctypes.byref(h)) != 0:
+                raise OSError("handle")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self._reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self._nv, self._h, self.source = nv, h, "nvml"
+        except (OSError, AttributeError):
+            self.source = "nvidia-smi"
+
+    def _nvml_loop(self):
+        mhz, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            ok = self._nv.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(mhz)) == 0
+            self._nv.nvmlDeviceGetPowerUsage(self._h, ctypes.byref(mw))
+            self._reason_fn(self._h, ctypes.byref(rs))
+            if ok:
+                self.samples.append((time.time(), float(mhz.value), mw.value / 1000.0, int(rs.value)))
+            time.sleep(0.001)
+
+    def _smi_loop(self):
+        fields = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active")
+        target = ["-i", self._uuid] if self._uuid else []
+        try:
+            self._proc = subprocess.Popen(["nvidia-smi", *target, f"--query-gpu={fields}",
+                                           "--format=csv,noheader,nounits", "-lms", "200"],
+                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        for line in self._proc.stdout:
+            f = [x.strip() for x in line.split(",")]
+            try:
+                self.max_mhz = float(f[1])
+                self.samples.append((time.time(), float(f[0]), float(f[2]), int(f[3], 16)))
+            except (ValueError, IndexError):
+                pass
 
     def start(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
-            return
-        self.thread = threading.Thread(target=self._read, daemon=True)
-        self.thread.start()
-
-    def _read(self):
-        for line in self.proc.stdout:
-            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+        loop = self._nvml_loop if self.source == "nvml" else self._smi_loop
+        self._thread = threading.Thread(target=loop, daemon=True)
+        self._thread.start()
 
     def stop(self):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
 
     def summary(self, t0: float, t1: float) -> dict:
-        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
         window = "timed_region"
         if not inside:
-            # the timed region was shorter than one sampling period: use the
-            # samples closest to it
-            near = sorted(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))[:3]
-            inside = [s for _, s in near]
+            inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
             window = "nearest_samples"
         if not inside:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no_samples"], "window": "none"}
-
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-        sm = [num(s[0]) for s in inside if num(s[0]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in inside for i in range(4) if len(s) > 3 + i and s[3 + i] == "Active"})
-        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": num(inside[0][1]),
-                "power_w_max": max((num(s[2]) or 0.0) for s in inside), "reasons": reasons,
-                "samples": len(inside), "window": window}
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no_samples"], "source": self.source}
+        reasons = sorted({name for s in inside for bit, name in self.REASONS.items() if s[3] & bit})
+        return {"sm_mhz": float(np.median([s[1] for s in inside])), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(s[1] for s in inside), "power_w_max": max(s[2] for s in inside),
+                "reasons": reasons, "samples": len(inside), "window": window, "source": self.source}
 
 
 def dist_setup(n_gpus: int):
@@ -244,10 +278,9 @@ def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
     torch.cuda.synchronize(dev)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.5)
+    sampler = ClockSampler(dev)
     barrier(world)
+    sampler.start()
     torch.cuda.synchronize(dev)
     t_wall0 = time.time()
     region0 = torch.cuda.Event(enable_timing=True)
@@ -261,7 +294,6 @@ def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
     torch.cuda.synchronize(dev)
     barrier(world)
     t_wall1 = time.time()
-    time.sleep(0.3)
     sampler.stop()
     st = attn.device_status()
     if st != attn.Status.OK:
@@ -331,6 +363,8 @@ def main() -> None:
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--shape", default=None,
+                    help="B,H,N,d[,causal] instead of a named workload (profiling a smaller case)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--exp2-emu16", type=int, default=0)
     ap.add_argument("--tau", type=float, default=8.0)
@@ -342,6 +376,11 @@ def main() -> None:
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = I.WORKLOADS[args.workload]
+    if args.shape:
+        f = [int(x) for x in args.shape.split(",")]
+        causal = bool(f[4]) if len(f) > 4 else False
+        w = I.Workload(f"custom_b{f[0]}h{f[1]}n{f[2]}d{f[3]}{'_causal' if causal else ''}", f[0], f[1], f[2], f[3],
+                       causal)
     if w.dtype != "bf16" and args.impl == "ours":
         ap.error(f"{w.name}: only the bf16 workloads are benchmarked by this build")
     world, rank, local = dist_setup(args.gpus)

@@ -9,6 +9,14 @@ bf16 inputs):
     side (|O| >= 2.56 is where half an ulp already exceeds 1e-2 for some values).
   * O, mean over all compared elements: <= 1e-3.
   * LSE: |LSE - LSE_ref| <= 1e-3.
+
+Stress inputs outside the five workloads (tau = 16, scaled-score standard
+deviations near 16, very peaked rows) use a bound derived from the arithmetic
+instead of the flat 1e-2: P is rounded to bf16 before P V (relative error
+<= 2^-9 per term), so |dO_ic| <= 2^-9 * A_ic with A_ic = sum_j softmax_ij |V_jc|
+(the oracle's attention of |V|), plus half an output ulp. The bound doubles the
+P term for the fp32 accumulation and adds 1e-3:
+  |O - O_ref| <= max(1e-2, ulp_bf16(|O_ref|), 2^-8 A + ulp_bf16(|O_ref|)/2 + 1e-3).
 """
 from __future__ import annotations
 
@@ -25,11 +33,15 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return np.ldexp(1.0, np.floor(np.log2(ax)).astype(np.int64) - 7)
 
 
-def compare(o, lse, o_ref, lse_ref, what: str = "") -> dict:
+def compare(o, lse, o_ref, lse_ref, what: str = "", abs_v_weight=None) -> dict:
+    """Assert the tolerances; ``abs_v_weight`` (A above) selects the stress bound."""
     o = np.asarray(o, dtype=np.float64)
     o_ref = np.asarray(o_ref, dtype=np.float64)
     err = np.abs(o - o_ref)
-    bound = np.maximum(O_MAX_ABS, bf16_ulp(o_ref))
+    ulp = bf16_ulp(o_ref)
+    bound = np.maximum(O_MAX_ABS, ulp)
+    if abs_v_weight is not None:
+        bound = np.maximum(bound, 2.0 ** -8 * np.asarray(abs_v_weight) + 0.5 * ulp + 1e-3)
     lerr = np.abs(np.asarray(lse, dtype=np.float64) - np.asarray(lse_ref, dtype=np.float64))
     stats = {
         "o_max_abs": float(err.max()) if err.size else 0.0,

@@ -33,10 +33,12 @@ def run(attn, q, k, v, causal, scale, **kw):
     return o.cpu(), lse.cpu()
 
 
-def check_full(attn, q, k, v, causal, scale, what, **kw):
+def check_full(attn, q, k, v, causal, scale, what, stress=False, **kw):
     o, lse = run(attn, q, k, v, causal, scale, **kw)
-    o_ref, lse_ref = attention_fwd(I.as_f64(q), I.as_f64(k), I.as_f64(v), causal, scale)
-    return compare(I.as_f64(o), lse.double().numpy(), o_ref, lse_ref, what)
+    qq, kk, vv = I.as_f64(q), I.as_f64(k), I.as_f64(v)
+    o_ref, lse_ref = attention_fwd(qq, kk, vv, causal, scale)
+    weight = attention_fwd(qq, kk, np.abs(vv), causal, scale)[0] if stress else None
+    return compare(I.as_f64(o), lse.double().numpy(), o_ref, lse_ref, what, abs_v_weight=weight)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -70,7 +72,7 @@ def test_software_exp2_shares(attn, emu, d, causal):
 def test_rescale_thresholds(attn, tau):
     # Q, K ~ N(0, 2^2): the running max keeps growing along the keys
     q, k, v = (I.to_bf16(x) for x in I.draw_fp32(1, 2, 1536, 128, qk_std=2.0, seed=9))
-    check_full(attn, q, k, v, True, 128 ** -0.5, f"tau={tau}", tau=tau)
+    check_full(attn, q, k, v, True, 128 ** -0.5, f"tau={tau}", stress=tau > 8.0, tau=tau)
 
 
 def test_scores_rising_along_keys(attn):
@@ -100,12 +102,12 @@ def test_large_scores(attn):
     # scaled scores with a standard deviation near 16: P spans the full range
     q, k, v = (I.to_bf16(x) for x in I.draw_fp32(1, 2, 512, 128, qk_std=4.0, seed=21))
     for causal in (False, True):
-        check_full(attn, q, k, v, causal, 128 ** -0.5, f"large causal={causal}")
+        check_full(attn, q, k, v, causal, 128 ** -0.5, f"large causal={causal}", stress=True)
 
 
 def test_non_default_scale(attn):
     q, k, v = (I.to_bf16(x) for x in I.draw_fp32(1, 2, 384, 64, seed=8))
-    check_full(attn, q, k, v, True, 0.37, "scale 0.37")
+    check_full(attn, q, k, v, True, 0.37, "scale 0.37", stress=True)
 
 
 def test_empty_problems(attn):
