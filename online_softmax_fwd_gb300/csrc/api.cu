@@ -80,7 +80,7 @@ attn_status_t check_fwd_args(const void* q, const void* k, const void* v, const 
   if (emu16 < 0 || emu16 > 16) return ATTN_ERR_INVALID_ARG;
   if (emu16 > 4) return ATTN_ERR_UNSUPPORTED;
   if (N > kMaxN) return ATTN_ERR_UNSUPPORTED;
-  if (static_cast<long long>(B) * H > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H * ((N + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || N == 0) {
     *empty = true;
     return ATTN_OK;
@@ -122,6 +122,14 @@ attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, 
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.tau = tau;
   const int n_pairs = (N + 255) / 256;
+  a.n_pairs = n_pairs;
+  a.bh = static_cast<int>(bh);
+  // heads whose K and V (2*N*d*2 bytes each) fit together in ~48 MiB of L2
+  const long long kv_head_bytes = 4LL * N * d;
+  long long band = (48LL << 20) / (kv_head_bytes > 0 ? kv_head_bytes : 1);
+  if (band < 1) band = 1;
+  if (band > bh) band = bh;
+  a.band = static_cast<int>(band);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (d == 64)

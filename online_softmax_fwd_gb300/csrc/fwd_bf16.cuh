@@ -50,6 +50,9 @@ struct FwdArgs {
   unsigned int* status;  // device error word
   int n;                 // sequence length N
   int n_kv_blocks;       // ceil(N / 128)
+  int n_pairs;           // ceil(N / 256): Q-tile pairs per head
+  int bh;                // B * H
+  int band;              // heads per scheduling band (their K/V stay in L2 together)
   float scale;           // s
   float scale_log2;      // s * log2(e)
   float tau;             // rescale threshold, log2 units
@@ -69,7 +72,12 @@ struct FwdCfg {
   static constexpr uint32_t kHolderOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kAbortOff = kHolderOff + 4;
   static constexpr uint32_t kSmemBytes = kAbortOff + 4 + 1024;  // + slack for 1024-byte alignment
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 384;  // 8 softmax warps, TMA warp, MMA warp, 2 spare
+  // setmaxnreg split: softmax warpgroups grow, the producer warpgroup shrinks.
+  // 2*128*216 + 128*64 = 63488 <= 384 threads x 168 registers at launch.
+  static constexpr uint32_t kRegsSoftmax = 216;
+  static constexpr uint32_t kRegsOther = 64;
+  static constexpr int kLaunchRegs = 168;
   static constexpr uint32_t kTmemCols = 512;
   // TMEM columns: S_t (fp32, 128 columns; P_t as bf16 pairs over its first 64)
   // and O_t (fp32, d columns) for the two query tiles.
@@ -119,29 +127,35 @@ __device__ __forceinline__ float exp2_col(int c, float x) {
 }
 
 // p = 2^(S*sl2 + neg_ms) for the 128 scores of a row, rounded to bf16 pairs
-// and stored to TMEM at p_tm; returns the fp32 sum of the unrounded p.
+// and stored to TMEM at p_tm; returns the fp32 sum of the unrounded p. The
+// scale-and-shift and the running sums work on fp32 pairs (f32x2).
 template <int EMU, bool MUFU_ONLY>
-__device__ __forceinline__ float softmax_p_store(const float (&s)[128], float sl2, float neg_ms,
+__device__ __forceinline__ float softmax_p_store(const float (&s)[128], uint64_t sl2_2, uint64_t neg_ms_2,
                                                  uint32_t p_tm) {
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  uint64_t acc[2] = {0ull, 0ull};
 #pragma unroll
   for (int chunk = 0; chunk < 4; ++chunk) {
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int c0 = chunk * 32 + 2 * i;
-      const float p0 = exp2_col<EMU, MUFU_ONLY>(c0, __fmaf_rn(s[c0], sl2, neg_ms));
-      const float p1 = exp2_col<EMU, MUFU_ONLY>(c0 + 1, __fmaf_rn(s[c0 + 1], sl2, neg_ms));
-      acc[i & 3] += p0 + p1;
+      float x0, x1;
+      f2_unpack(f2_fma(f2_pack(s[c0], s[c0 + 1]), sl2_2, neg_ms_2), x0, x1);
+      const float p0 = exp2_col<EMU, MUFU_ONLY>(c0, x0);
+      const float p1 = exp2_col<EMU, MUFU_ONLY>(c0 + 1, x1);
+      acc[i & 1] = f2_add(acc[i & 1], f2_pack(p0, p1));
       pk[i] = pack_bf16x2(p0, p1);
     }
     tmem_st16(p_tm + chunk * 16, pk);
   }
-  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  float a0, a1, b0, b1;
+  f2_unpack(acc[0], a0, a1);
+  f2_unpack(acc[1], b0, b1);
+  return (a0 + a1) + (b0 + b1);
 }
 
 template <int D, bool CAUSAL, int EMU>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
   using C = FwdCfg<D>;
@@ -161,8 +175,18 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int pair = gridDim.y - 1 - blockIdx.y;  // heaviest causal pairs first
+  // 1-D grid in bands of `band` heads: inside a band the Q-tile pairs of its
+  // heads come heaviest first (causal), so co-resident CTAs share the band's
+  // K/V in L2 and the long causal tiles start early.
+  int bh, pair;
+  {
+    const int per_band = args.band * args.n_pairs;
+    const int band_id = blockIdx.x / per_band;
+    const int r = blockIdx.x - band_id * per_band;
+    const int heads = min(args.band, args.bh - band_id * args.band);
+    pair = args.n_pairs - 1 - r / heads;
+    bh = band_id * args.band + r % heads;
+  }
   const int row0 = pair * 256;
   const int nkv = args.n_kv_blocks;
   const int n0 = CAUSAL ? min(2 * pair + 1, nkv) : nkv;  // key blocks of tile 0
@@ -192,6 +216,9 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *holder;
 
+  if (warp >= 8) {
+  // ============================================================ producer warpgroup
+  regs_decrease<C::kRegsOther>();
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -306,8 +333,10 @@ __global__ void __launch_bounds__(320, 1)
       drain_bar(bar_drain, 0);
     }
     __syncwarp();
+  }
   } else {
-    // ------------------------------------------------------------ softmax
+    // ============================================================ softmax warpgroups
+    regs_increase<C::kRegsSoftmax>();
     const int t = warp >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
@@ -318,6 +347,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t s_tm = tmem + lane_off + C::col_s(t);
     const uint32_t o_tm = tmem + lane_off + C::col_o(t);
     const float sl2 = args.scale_log2;
+    const uint64_t sl2_2 = f2_pack(sl2, sl2);
     float m = -INFINITY;
     float l = 0.f;
     bool ok = true;
@@ -350,11 +380,14 @@ __global__ void __launch_bounds__(320, 1)
       }
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+      for (int i = 0; i < 8; ++i) mx[i] = fmax3(s[i], s[8 + i], s[16 + i]);
 #pragma unroll
-      for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-      const float bm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int c = 24; c < 120; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + i], s[c + 8 + i]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[120 + i]);
+      const float bm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       // keep the stale max unless it would grow by more than tau (log2 units)
       float m_new = fmaxf(m, bm);
       const bool fire = !((m_new - m) * sl2 <= args.tau);
@@ -363,8 +396,9 @@ __global__ void __launch_bounds__(320, 1)
       const float corr = fire ? (m == -INFINITY ? 0.f : ex2_mufu((m - m_new) * sl2)) : 1.0f;
       m = m_new;
       const float neg_ms = (m == -INFINITY) ? 0.f : -(m * sl2);
-      const float psum = need_mask ? softmax_p_store<EMU, true>(s, sl2, neg_ms, s_tm)
-                                   : softmax_p_store<EMU, false>(s, sl2, neg_ms, s_tm);
+      const uint64_t neg_ms_2 = f2_pack(neg_ms, neg_ms);
+      const float psum = need_mask ? softmax_p_store<EMU, true>(s, sl2_2, neg_ms_2, s_tm)
+                                   : softmax_p_store<EMU, false>(s, sl2_2, neg_ms_2, s_tm);
       // correction of O after the scores are dead (lower register pressure);
       // it still lands before P_t(j) is handed to the MMA thread below
       if (j > 0 && __any_sync(0xffffffffu, fire)) {
@@ -374,8 +408,14 @@ __global__ void __launch_bounds__(320, 1)
           tmem_ld32(o_tm + c, ob);
           tmem_ld_wait();
           reg_fence32(ob);
+          const uint64_t corr_2 = f2_pack(corr, corr);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ob[i] = __float_as_uint(__uint_as_float(ob[i]) * corr);
+          for (int i = 0; i < 32; i += 2) {
+            float a, b;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(ob[i]), __uint_as_float(ob[i + 1])), corr_2), a, b);
+            ob[i] = __float_as_uint(a);
+            ob[i + 1] = __float_as_uint(b);
+          }
           tmem_st32(o_tm + c, ob);
         }
       }
@@ -400,9 +440,13 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld_wait();
         reg_fence32(ob);
         uint32_t pk[16];
+        const uint64_t inv_l_2 = f2_pack(inv_l, inv_l);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(ob[2 * i]) * inv_l, __uint_as_float(ob[2 * i + 1]) * inv_l);
+        for (int i = 0; i < 16; ++i) {
+          float a, b;
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(ob[2 * i]), __uint_as_float(ob[2 * i + 1])), inv_l_2), a, b);
+          pk[i] = pack_bf16x2(a, b);
+        }
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
@@ -421,7 +465,7 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-// Launch one instantiation: grid (B*H, ceil(N/256)), 320 threads, one CTA per SM.
+// Launch one instantiation: B*H*ceil(N/256) CTAs of 384 threads, one CTA per SM.
 template <int D, bool CAUSAL, int EMU>
 cudaError_t launch_fwd_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                             const FwdArgs& args, int bh, int n_pairs, cudaStream_t stream) {
@@ -429,8 +473,17 @@ cudaError_t launch_fwd_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, co
   auto kernel = attn_fwd_bf16_kernel<D, CAUSAL, EMU>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(bh, n_pairs);
-  kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, args);
+  // The setmaxnreg split redistributes the registers the CTA is launched
+  // with; it must not ask for more than that, or the increase would wait for
+  // ever. Refuse to launch if the compiled register count differs.
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs < C::kLaunchRegs) return cudaErrorInvalidConfiguration;
+  (void)bh;
+  (void)n_pairs;
+  const long long ctas = static_cast<long long>(args.bh) * args.n_pairs;
+  kernel<<<static_cast<unsigned>(ctas), C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, args);
   return cudaGetLastError();
 }
 
