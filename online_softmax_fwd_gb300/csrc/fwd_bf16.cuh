@@ -74,9 +74,9 @@ struct FwdCfg {
   static constexpr uint32_t kSmemBytes = kAbortOff + 4 + 1024;  // + slack for 1024-byte alignment
   static constexpr int kThreads = 384;  // 8 softmax warps, TMA warp, MMA warp, 2 spare
   // setmaxnreg split: softmax warpgroups grow, the producer warpgroup shrinks.
-  // 2*128*216 + 128*64 = 63488 <= 384 threads x 168 registers at launch.
-  static constexpr uint32_t kRegsSoftmax = 216;
-  static constexpr uint32_t kRegsOther = 64;
+  // 2*128*208 + 128*88 = 64512 = 384 threads x 168 registers at launch.
+  static constexpr uint32_t kRegsSoftmax = 208;
+  static constexpr uint32_t kRegsOther = 88;
   static constexpr int kLaunchRegs = 168;
   static constexpr uint32_t kTmemCols = 512;
   // TMEM columns: S_t (fp32, 128 columns; P_t as bf16 pairs over its first 64)
@@ -126,32 +126,29 @@ __device__ __forceinline__ float exp2_col(int c, float x) {
   return ex2_mufu(x);
 }
 
-// p = 2^(S*sl2 + neg_ms) for the 128 scores of a row, rounded to bf16 pairs
-// and stored to TMEM at p_tm; returns the fp32 sum of the unrounded p. The
-// scale-and-shift and the running sums work on fp32 pairs (f32x2).
+// p = 2^(S*sl2 + neg_ms) for the 128 scores of a row (as 64 pairs), rounded
+// to bf16 pairs and stored to TMEM at p_tm; returns the fp32 sum of the
+// unrounded p. The scale-and-shift and the running sums use the packed fp32
+// pair instructions (one issue for two lanes of work).
 template <int EMU, bool MUFU_ONLY>
-__device__ __forceinline__ float softmax_p_store(const float (&s)[128], uint64_t sl2_2, uint64_t neg_ms_2,
+__device__ __forceinline__ float softmax_p_store(const float2 (&s)[64], float2 sl2_2, float2 neg_ms_2,
                                                  uint32_t p_tm) {
-  uint64_t acc[2] = {0ull, 0ull};
+  float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
   for (int chunk = 0; chunk < 4; ++chunk) {
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const int c0 = chunk * 32 + 2 * i;
-      float x0, x1;
-      f2_unpack(f2_fma(f2_pack(s[c0], s[c0 + 1]), sl2_2, neg_ms_2), x0, x1);
-      const float p0 = exp2_col<EMU, MUFU_ONLY>(c0, x0);
-      const float p1 = exp2_col<EMU, MUFU_ONLY>(c0 + 1, x1);
-      acc[i & 1] = f2_add(acc[i & 1], f2_pack(p0, p1));
-      pk[i] = pack_bf16x2(p0, p1);
+      const int c = chunk * 16 + i;  // pair index
+      const float2 x = __ffma2_rn(s[c], sl2_2, neg_ms_2);
+      const float2 p = make_float2(exp2_col<EMU, MUFU_ONLY>(2 * c, x.x), exp2_col<EMU, MUFU_ONLY>(2 * c + 1, x.y));
+      acc[i & 1] = __fadd2_rn(acc[i & 1], p);
+      pk[i] = pack_bf16x2(p.x, p.y);
     }
     tmem_st16(p_tm + chunk * 16, pk);
   }
-  float a0, a1, b0, b1;
-  f2_unpack(acc[0], a0, a1);
-  f2_unpack(acc[1], b0, b1);
-  return (a0 + a1) + (b0 + b1);
+  const float2 t = __fadd2_rn(acc[0], acc[1]);
+  return t.x + t.y;
 }
 
 template <int D, bool CAUSAL, int EMU>
@@ -263,50 +260,68 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t kIdO = idesc_bf16_f32(128, D, true);
-      auto k_slot = [&](int j) { return (2 * j) % C::kSlots; };
-      auto k_phase = [&](int j) { return static_cast<uint32_t>(((2 * j) / C::kSlots) & 1); };
-      auto v_slot = [&](int j) { return (2 * j + 1) % C::kSlots; };
-      auto v_phase = [&](int j) { return static_cast<uint32_t>(((2 * j + 1) / C::kSlots) & 1); };
-      auto issue_s = [&](int t, int j) {
-        const uint32_t qa = sbase + t * C::kTileBytes;
-        const uint32_t kb = sbase + C::kRingOff + k_slot(j) * C::kTileBytes;
+      constexpr uint64_t kSlotStep = C::kTileBytes >> 4;  // descriptor units between ring slots
+      // Descriptors are built once and advanced with constant adds (the start
+      // address is their low field; every operand stays below 256 KiB).
+      // Q and K are K-major: 8-row groups 1024 bytes apart; the next K=16 slice
+      // is 32 bytes further inside a 128-byte swizzle row, the 5th starts the
+      // next 64-column box.
+      const uint64_t q_desc[2] = {smem_desc_sw128(sbase, 16, 1024),
+                                  smem_desc_sw128(sbase + C::kTileBytes, 16, 1024)};
+      const uint64_t k_ring = smem_desc_sw128(sbase + C::kRingOff, 16, 1024);
+      // V is MN-major: 64-column halves kBoxBytes apart, 8-key groups 1024 bytes
+      // apart; the next 16 keys are 2048 bytes further.
+      const uint64_t v_ring = smem_desc_sw128(sbase + C::kRingOff, C::kBoxBytes, 1024);
+      auto kmajor_step = [](int kk) -> uint64_t {
+        return static_cast<uint64_t>(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
+      };
+      auto issue_s = [&](int t, uint32_t slot) {
+        const uint64_t a = q_desc[t];
+        const uint64_t b = k_ring + slot * kSlotStep;
+        const uint32_t d = tmem + C::col_s(t);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::col_s(t), smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
-                 kIdS, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(d, a + kmajor_step(kk), b + kmajor_step(kk), kIdS, kk > 0 ? 1u : 0u);
+      };
+      auto issue_pv = [&](int t, uint32_t slot, bool first) {
+        const uint64_t b = v_ring + slot * kSlotStep;
+        const uint32_t d = tmem + C::col_o(t);
+        const uint32_t a = tmem + C::col_s(t);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ts(d, a + kk * 8, b + kk * 128, kIdO, (!first || kk > 0) ? 1u : 0u);
+      };
+      // ring positions: K_j is the (2j)-th load, V_j the (2j+1)-th
+      auto advance2 = [](uint32_t& slot, uint32_t& phase) {
+        slot += 2;
+        if (slot >= static_cast<uint32_t>(C::kSlots)) {
+          slot -= C::kSlots;
+          phase ^= 1u;
         }
       };
-      auto issue_pv = [&](int t, int j) {
-        const uint32_t vb = sbase + C::kRingOff + v_slot(j) * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, smem_desc_sw128(vb + kk * 2048, C::kBoxBytes, 1024),
-                 kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-      };
-      bool ok = wait_bar(bar_q, 0, abort_flag, args.status, 2) &&
-                wait_bar(bar_full(k_slot(0)), k_phase(0), abort_flag, args.status, 3);
+      uint32_t ks = 0, kph = 0;  // K_j
+      uint32_t vs = 1, vph = 0;  // V_j
+      bool ok = wait_bar(bar_q, 0, abort_flag, args.status, 2) && wait_bar(bar_full(ks), kph, abort_flag, args.status, 3);
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
+        issue_s(0, ks);
         tc_commit(bar_s(0));
-        issue_s(1, 0);
+        issue_s(1, ks);
         tc_commit(bar_s(1));
-        tc_commit(bar_empty(k_slot(0)));
+        tc_commit(bar_empty(ks));
       }
       for (int j = 0; ok && j < n1; ++j) {
-        if (!wait_bar(bar_full(v_slot(j)), v_phase(j), abort_flag, args.status, 4)) break;
+        if (!wait_bar(bar_full(vs), vph, abort_flag, args.status, 4)) break;
+        uint32_t ks_next = ks, kph_next = kph;
+        advance2(ks_next, kph_next);
         bool k_next_ready = false;
         if (j < n0) {
           if (!wait_bar(bar_p(0), j & 1, abort_flag, args.status, 5)) break;
           tc_fence_after();
-          issue_pv(0, j);
+          issue_pv(0, vs, j == 0);
           if (j + 1 < n0) {
-            if (!wait_bar(bar_full(k_slot(j + 1)), k_phase(j + 1), abort_flag, args.status, 6)) break;
+            if (!wait_bar(bar_full(ks_next), kph_next, abort_flag, args.status, 6)) break;
             k_next_ready = true;
             tc_fence_after();
-            issue_s(0, j + 1);
+            issue_s(0, ks_next);
             tc_commit(bar_s(0));
           } else {
             tc_commit(bar_o(0));
@@ -314,19 +329,22 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (!wait_bar(bar_p(1), j & 1, abort_flag, args.status, 7)) break;
         tc_fence_after();
-        issue_pv(1, j);
-        tc_commit(bar_empty(v_slot(j)));
+        issue_pv(1, vs, j == 0);
+        tc_commit(bar_empty(vs));
         if (j + 1 < n1) {
           if (!k_next_ready) {
-            if (!wait_bar(bar_full(k_slot(j + 1)), k_phase(j + 1), abort_flag, args.status, 8)) break;
+            if (!wait_bar(bar_full(ks_next), kph_next, abort_flag, args.status, 8)) break;
             tc_fence_after();
           }
-          issue_s(1, j + 1);
+          issue_s(1, ks_next);
           tc_commit(bar_s(1));
-          tc_commit(bar_empty(k_slot(j + 1)));
+          tc_commit(bar_empty(ks_next));
         } else {
           tc_commit(bar_o(1));
         }
+        ks = ks_next;
+        kph = kph_next;
+        advance2(vs, vph);
       }
       // nothing may still be executing when TMEM is released
       tc_commit(bar_drain);
@@ -347,7 +365,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t s_tm = tmem + lane_off + C::col_s(t);
     const uint32_t o_tm = tmem + lane_off + C::col_o(t);
     const float sl2 = args.scale_log2;
-    const uint64_t sl2_2 = f2_pack(sl2, sl2);
+    const float2 sl2_2 = make_float2(sl2, sl2);
     float m = -INFINITY;
     float l = 0.f;
     bool ok = true;
@@ -356,7 +374,7 @@ __global__ void __launch_bounds__(384, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      float s[128];
+      float2 s[64];  // the row's 128 scores as (even, odd) column pairs
       {
         uint32_t u[4][32];
 #pragma unroll
@@ -366,7 +384,8 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < 4; ++c) {
           reg_fence32(u[c]);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(u[c][i]);
+          for (int i = 0; i < 16; ++i)
+            s[16 * c + i] = make_float2(__uint_as_float(u[c][2 * i]), __uint_as_float(u[c][2 * i + 1]));
         }
       }
       const int kv0 = j * 128;
@@ -375,18 +394,22 @@ __global__ void __launch_bounds__(384, 1)
         int lim = args.n - 1 - kv0;
         if (CAUSAL) lim = min(lim, grow - kv0);
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c > lim) s[c] = -INFINITY;
+        for (int c = 0; c < 64; ++c) {
+          if (2 * c > lim) s[c].x = -INFINITY;
+          if (2 * c + 1 > lim) s[c].y = -INFINITY;
+        }
       }
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmax3(s[i], s[8 + i], s[16 + i]);
+      for (int i = 0; i < 8; ++i) mx[i] = fmax3(s[i].x, s[i].y, s[8 + i].x);
 #pragma unroll
-      for (int c = 24; c < 120; c += 16)
+      for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[8 + i].y, s[16 + i].x);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + i], s[c + 8 + i]);
+      for (int c = 16; c < 56; c += 8)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[120 + i]);
+        for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[c + i].y, s[c + 8 + i].x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[56 + i].y, -INFINITY);
       const float bm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       // keep the stale max unless it would grow by more than tau (log2 units)
       float m_new = fmaxf(m, bm);
@@ -396,7 +419,7 @@ __global__ void __launch_bounds__(384, 1)
       const float corr = fire ? (m == -INFINITY ? 0.f : ex2_mufu((m - m_new) * sl2)) : 1.0f;
       m = m_new;
       const float neg_ms = (m == -INFINITY) ? 0.f : -(m * sl2);
-      const uint64_t neg_ms_2 = f2_pack(neg_ms, neg_ms);
+      const float2 neg_ms_2 = make_float2(neg_ms, neg_ms);
       const float psum = need_mask ? softmax_p_store<EMU, true>(s, sl2_2, neg_ms_2, s_tm)
                                    : softmax_p_store<EMU, false>(s, sl2_2, neg_ms_2, s_tm);
       // correction of O after the scores are dead (lower register pressure);
@@ -408,13 +431,12 @@ __global__ void __launch_bounds__(384, 1)
           tmem_ld32(o_tm + c, ob);
           tmem_ld_wait();
           reg_fence32(ob);
-          const uint64_t corr_2 = f2_pack(corr, corr);
+          const float2 corr_2 = make_float2(corr, corr);
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            float a, b;
-            f2_unpack(f2_mul(f2_pack(__uint_as_float(ob[i]), __uint_as_float(ob[i + 1])), corr_2), a, b);
-            ob[i] = __float_as_uint(a);
-            ob[i + 1] = __float_as_uint(b);
+            const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(ob[i]), __uint_as_float(ob[i + 1])), corr_2);
+            ob[i] = __float_as_uint(o2.x);
+            ob[i + 1] = __float_as_uint(o2.y);
           }
           tmem_st32(o_tm + c, ob);
         }
@@ -440,12 +462,11 @@ __global__ void __launch_bounds__(384, 1)
         tmem_ld_wait();
         reg_fence32(ob);
         uint32_t pk[16];
-        const uint64_t inv_l_2 = f2_pack(inv_l, inv_l);
+        const float2 inv_l_2 = make_float2(inv_l, inv_l);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          float a, b;
-          f2_unpack(f2_mul(f2_pack(__uint_as_float(ob[2 * i]), __uint_as_float(ob[2 * i + 1])), inv_l_2), a, b);
-          pk[i] = pack_bf16x2(a, b);
+          const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(ob[2 * i]), __uint_as_float(ob[2 * i + 1])), inv_l_2);
+          pk[i] = pack_bf16x2(o2.x, o2.y);
         }
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c);
