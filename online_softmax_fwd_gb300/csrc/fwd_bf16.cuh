@@ -218,46 +218,62 @@ __global__ void __launch_bounds__(384, 1)
   regs_decrease<C::kRegsOther>();
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t pol_q = policy_evict_first();
-      const uint64_t pol_kv = policy_evict_last();
+    // The whole warp runs the loop (warp-uniform values); one elected lane
+    // issues the copies.
+    const uint32_t leader = elect_one();
+    const uint64_t pol_q = policy_evict_first();
+    const uint64_t pol_kv = policy_evict_last();
+    if (leader) {
       mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
 #pragma unroll
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d_hint(sbase + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, bar_q, b * 64, row0 + 128 * t,
-                           bh, pol_q);
-      int seq = 0;
-      bool ok = true;
-      for (int j = 0; ok && j < n1; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
-          const int slot = seq % C::kSlots;
-          const uint32_t ph = (seq / C::kSlots) & 1;
-          if (!wait_bar(bar_empty(slot), ph ^ 1u, abort_flag, args.status, 1)) {
-            ok = false;
-            break;
-          }
+          tma_load_3d_hint(sbase + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, bar_q, b * 64, row0 + 128 * t, bh,
+                           pol_q);
+    }
+    int seq = 0;
+    uint32_t slot = 0, ph = 0;
+    bool ok = true;
+    for (int j = 0; ok && j < n1; ++j) {
+      for (int kv = 0; kv < 2; ++kv) {
+        ok = __all_sync(0xffffffffu, wait_bar(bar_empty(slot), ph ^ 1u, abort_flag, args.status, 1));
+        if (!ok) break;
+        if (leader) {
           mbar_arrive_expect_tx(bar_full(slot), C::kTileBytes);
           const CUtensorMap* map = kv ? &tm_v : &tm_k;
 #pragma unroll
           for (int b = 0; b < C::kBoxes; ++b)
             tma_load_3d_hint(sbase + C::kRingOff + slot * C::kTileBytes + b * C::kBoxBytes, map, bar_full(slot),
                              b * 64, j * 128, bh, pol_kv);
-          ++seq;
+        }
+        ++seq;
+        if (++slot == static_cast<uint32_t>(C::kSlots)) {
+          slot = 0;
+          ph ^= 1u;
         }
       }
-      if (!ok) {
-        // let the copies already in flight land before the CTA's memory is released
-        drain_bar(bar_q, 0);
-        for (int s = seq - C::kSlots < 0 ? 0 : seq - C::kSlots; s < seq; ++s)
-          drain_bar(bar_full(s % C::kSlots), (s / C::kSlots) & 1);
-      }
+    }
+    if (!ok) {
+      // let the copies already in flight land before the CTA's memory is released
+      drain_bar(bar_q, 0);
+      for (int s = seq - C::kSlots < 0 ? 0 : seq - C::kSlots; s < seq; ++s)
+        drain_bar(bar_full(s % C::kSlots), (s / C::kSlots) & 1);
     }
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop so descriptors and ring positions stay
+    // warp-uniform; one elected lane issues the MMAs and commits (a commit
+    // tracks the MMAs of the thread that issues it, always the same lane).
+    {
+      const uint32_t leader = elect_one();
+      auto commit = [&](uint32_t bar) {
+        if (leader) tc_commit(bar);
+      };
+      auto wait = [&](uint32_t bar, uint32_t parity, uint32_t where) {
+        return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, args.status, where));
+      };
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t kIdO = idesc_bf16_f32(128, D, true);
       constexpr uint64_t kSlotStep = C::kTileBytes >> 4;  // descriptor units between ring slots
@@ -279,15 +295,20 @@ __global__ void __launch_bounds__(384, 1)
         const uint64_t a = q_desc[t];
         const uint64_t b = k_ring + slot * kSlotStep;
         const uint32_t d = tmem + C::col_s(t);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) mma_ss(d, a + kmajor_step(kk), b + kmajor_step(kk), kIdS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(d, a + kmajor_step(kk), b + kmajor_step(kk), kIdS, kk > 0 ? 1u : 0u);
+        }
       };
       auto issue_pv = [&](int t, uint32_t slot, bool first) {
         const uint64_t b = v_ring + slot * kSlotStep;
         const uint32_t d = tmem + C::col_o(t);
         const uint32_t a = tmem + C::col_s(t);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ts(d, a + kk * 8, b + kk * 128, kIdO, (!first || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) mma_ts(d, a + kk * 8, b + kk * 128, kIdO, (!first || kk > 0) ? 1u : 0u);
+        }
       };
       // ring positions: K_j is the (2j)-th load, V_j the (2j+1)-th
       auto advance2 = [](uint32_t& slot, uint32_t& phase) {
@@ -299,55 +320,55 @@ __global__ void __launch_bounds__(384, 1)
       };
       uint32_t ks = 0, kph = 0;  // K_j
       uint32_t vs = 1, vph = 0;  // V_j
-      bool ok = wait_bar(bar_q, 0, abort_flag, args.status, 2) && wait_bar(bar_full(ks), kph, abort_flag, args.status, 3);
+      bool ok = wait(bar_q, 0, 2) && wait(bar_full(ks), kph, 3);
       if (ok) {
         tc_fence_after();
         issue_s(0, ks);
-        tc_commit(bar_s(0));
+        commit(bar_s(0));
         issue_s(1, ks);
-        tc_commit(bar_s(1));
-        tc_commit(bar_empty(ks));
+        commit(bar_s(1));
+        commit(bar_empty(ks));
       }
       for (int j = 0; ok && j < n1; ++j) {
-        if (!wait_bar(bar_full(vs), vph, abort_flag, args.status, 4)) break;
+        if (!wait(bar_full(vs), vph, 4)) break;
         uint32_t ks_next = ks, kph_next = kph;
         advance2(ks_next, kph_next);
         bool k_next_ready = false;
         if (j < n0) {
-          if (!wait_bar(bar_p(0), j & 1, abort_flag, args.status, 5)) break;
+          if (!wait(bar_p(0), j & 1, 5)) break;
           tc_fence_after();
           issue_pv(0, vs, j == 0);
           if (j + 1 < n0) {
-            if (!wait_bar(bar_full(ks_next), kph_next, abort_flag, args.status, 6)) break;
+            if (!wait(bar_full(ks_next), kph_next, 6)) break;
             k_next_ready = true;
             tc_fence_after();
             issue_s(0, ks_next);
-            tc_commit(bar_s(0));
+            commit(bar_s(0));
           } else {
-            tc_commit(bar_o(0));
+            commit(bar_o(0));
           }
         }
-        if (!wait_bar(bar_p(1), j & 1, abort_flag, args.status, 7)) break;
+        if (!wait(bar_p(1), j & 1, 7)) break;
         tc_fence_after();
         issue_pv(1, vs, j == 0);
-        tc_commit(bar_empty(vs));
+        commit(bar_empty(vs));
         if (j + 1 < n1) {
           if (!k_next_ready) {
-            if (!wait_bar(bar_full(ks_next), kph_next, abort_flag, args.status, 8)) break;
+            if (!wait(bar_full(ks_next), kph_next, 8)) break;
             tc_fence_after();
           }
           issue_s(1, ks_next);
-          tc_commit(bar_s(1));
-          tc_commit(bar_empty(ks_next));
+          commit(bar_s(1));
+          commit(bar_empty(ks_next));
         } else {
-          tc_commit(bar_o(1));
+          commit(bar_o(1));
         }
         ks = ks_next;
         kph = kph_next;
         advance2(vs, vph);
       }
       // nothing may still be executing when TMEM is released
-      tc_commit(bar_drain);
+      commit(bar_drain);
       drain_bar(bar_drain, 0);
     }
     __syncwarp();

@@ -208,6 +208,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 namespace attn {
 
+// 1 in exactly one lane of a converged warp (the same lane every time), 0 in
+// the others: warp-wide code stays warp-uniform and only that lane issues.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred;
+}
+
 // max of three fp32 values in one instruction
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
