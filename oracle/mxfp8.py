@@ -1,0 +1,91 @@
+"""MXFP8 (E4M3 payload, E8M0 block scales) quantiser -- TEST INFRASTRUCTURE ONLY.
+
+"PyTorch FlashAttention-4 adds MXFP8 block-scaled forward and backward for
+Blackwell", section "Quantization along both axes and jagged tensors": Q and K
+are quantised along the embedding dimension and V along the sequence, with
+square 32 x 32 blocks, each block sharing one E8M0 (power of two) scale.
+
+The pages do not state the scale rule. The reading taken here: a block's scale
+is the smallest power of two 2^e with amax / 2^e <= 448 (the largest finite
+E4M3 value), so the block's largest element lands in the top binade of E4M3
+without saturating; an all-zero block takes e = 0. Elements are divided by 2^e
+(exact) and rounded to E4M3, nearest with ties to even, saturating at +-448.
+
+E4M3 (the OCP "E4M3FN" encoding): 1 sign bit, 4 exponent bits with bias 7,
+3 mantissa bits; exponent field 0 encodes subnormals m * 2^-9; the code
+S.1111.111 is NaN and there are no infinities, so the largest finite value is
+1.75 * 2^8 = 448 and the smallest subnormal 2^-9.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+E4M3_MAX = 448.0
+BLOCK = 32
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values (float64) of E4M3 byte codes; NaN for the NaN codes."""
+    c = np.asarray(codes, dtype=np.int64) & 0xFF
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def _all_finite_values() -> tuple[np.ndarray, np.ndarray]:
+    codes = np.arange(0, 0x7F)  # non-negative finite codes 0x00 .. 0x7E, ascending values
+    return codes, e4m3_decode(codes)
+
+
+_POS_CODES, _POS_VALUES = _all_finite_values()
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Round float values to E4M3 codes: nearest, ties to the even code
+    (even mantissa), magnitudes above 448 saturate to 448. NaN is not expected."""
+    x = np.asarray(x, dtype=np.float64)
+    mag = np.minimum(np.abs(x), E4M3_MAX)
+    # index of the largest representable value <= mag
+    lo = np.clip(np.searchsorted(_POS_VALUES, mag, side="right") - 1, 0, len(_POS_VALUES) - 1)
+    hi = np.minimum(lo + 1, len(_POS_VALUES) - 1)
+    vlo, vhi = _POS_VALUES[lo], _POS_VALUES[hi]
+    dlo, dhi = mag - vlo, vhi - mag
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi != lo) & ((_POS_CODES[lo] & 1) == 1))
+    code = np.where(pick_hi, _POS_CODES[hi], _POS_CODES[lo])
+    # the sign is kept, also when the magnitude rounds to zero (IEEE style)
+    return np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
+
+
+def e8m0_exponent(amax) -> np.ndarray:
+    """Smallest integer e with amax <= 448 * 2^e (0 for amax == 0)."""
+    # amax = m * 2^E with m in [0.5, 1) and 448 = 0.875 * 2^9, so
+    # amax <= 448 * 2^e  <=>  e >= E - 9 when m <= 0.875, else e >= E - 8.
+    a = np.asarray(amax, dtype=np.float64)
+    m, E = np.frexp(a)
+    e = np.where(m <= 0.875, E - 9, E - 8)
+    return np.where(a > 0, e, 0).astype(np.int64)
+
+
+def quantize_blocks(x: np.ndarray) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Quantise [..., R, C] with one scale per 32 x 32 block (R, C padded up to
+    multiples of 32 with zeros for the amax only).
+
+    Returns (codes uint8 [..., R, C], e int64 [..., ceil(R/32), ceil(C/32)],
+    dequantised float64 [..., R, C] = e4m3_decode(codes) * 2^e)."""
+    x = np.asarray(x, dtype=np.float64)
+    *lead, R, C = x.shape
+    rb, cb = -(-R // BLOCK), -(-C // BLOCK)
+    pad = np.zeros((*lead, rb * BLOCK, cb * BLOCK))
+    pad[..., :R, :C] = x
+    blocks = pad.reshape(*lead, rb, BLOCK, cb, BLOCK)
+    amax = np.abs(blocks).max(axis=(-3, -1))                     # [..., rb, cb]
+    e = e8m0_exponent(amax)
+    scale_full = np.repeat(np.repeat(np.exp2(e.astype(np.float64)), BLOCK, axis=-2), BLOCK, axis=-1)
+    scaled = pad / scale_full
+    codes_full = e4m3_encode(scaled)
+    codes = codes_full[..., :R, :C]
+    deq = e4m3_decode(codes) * scale_full[..., :R, :C]
+    return codes, e, deq

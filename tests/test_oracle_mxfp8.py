@@ -1,0 +1,74 @@
+"""Pins for the MXFP8 quantiser of the oracle (CPU only): the E4M3 format's
+closed forms, PyTorch's float8_e4m3fn conversion as a library cross-check, the
+E8M0 scale rule as a property, and the 32 x 32 block structure."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import mxfp8 as M
+
+
+def test_e4m3_known_codes():
+    table = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x30: 0.5, 0x38: 1.0,
+             0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0}
+    for code, val in table.items():
+        assert M.e4m3_decode(code) == val
+    assert np.isnan(M.e4m3_decode(0x7F)) and np.isnan(M.e4m3_decode(0xFF))
+
+
+def test_round_trip_every_finite_code():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)])
+    assert np.array_equal(M.e4m3_encode(M.e4m3_decode(codes)), codes)
+
+
+def test_ties_go_to_even_and_saturation():
+    assert M.e4m3_encode(1.0625) == 0x38      # between 1.0 (0x38) and 1.125 (0x39)
+    assert M.e4m3_encode(1.1875) == 0x3A      # between 1.125 (0x39) and 1.25 (0x3A)
+    assert M.e4m3_encode(1.9375) == 0x40      # between 1.875 (0x3F) and 2.0 (0x40)
+    assert M.e4m3_encode(2.0 ** -10) == 0x00  # half the smallest subnormal -> 0 (even)
+    assert M.e4m3_encode(3 * 2.0 ** -10) == 0x02
+    for big, code in ((448.0, 0x7E), (460.0, 0x7E), (500.0, 0x7E), (1e9, 0x7E), (-1e9, 0xFE)):
+        assert M.e4m3_encode(big) == code
+
+
+def test_agrees_with_torch_float8_in_range():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.uniform(-448, 448, 200000), rng.standard_normal(200000) * 3,
+                        rng.standard_normal(100000) * 1e-2]).astype(np.float32)
+    ours = M.e4m3_encode(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_scale_rule_is_the_smallest_power_of_two():
+    rng = np.random.default_rng(1)
+    amax = np.concatenate([np.exp(rng.uniform(-20, 20, 10000)), 448.0 * np.exp2(np.arange(-10, 10.0)),
+                           [1.0, 1.75, 448.0, 449.0]])
+    e = M.e8m0_exponent(amax)
+    assert np.all(amax <= 448.0 * np.exp2(e))
+    assert np.all(amax > 448.0 * np.exp2(e - 1))
+    assert list(M.e8m0_exponent([448.0, 449.0, 1.0, 1.75, 1.76, 0.0])) == [0, 1, -8, -8, -7, 0]
+
+
+def test_block_structure_and_error_bound():
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((2, 3, 96, 128))
+    x[0, 0, 32:64, 64:96] *= 1000.0            # one loud block must not change its neighbours
+    codes, e, deq = M.quantize_blocks(x)
+    assert codes.shape == x.shape and e.shape == (2, 3, 3, 4)
+    amax = np.abs(x.reshape(2, 3, 3, 32, 4, 32)).max(axis=(3, 5))
+    assert np.array_equal(e, M.e8m0_exponent(amax))
+    assert e[0, 0, 1, 2] > e[0, 0, 1, 1] + 8
+    # every block's largest element reaches at least the top half of E4M3's range
+    assert np.all(amax / np.exp2(e) > 224.0)
+    # 3 mantissa bits: relative error <= 2^-4 for elements in E4M3's normal range
+    normal = np.abs(x) / np.repeat(np.repeat(np.exp2(e.astype(float)), 32, -2), 32, -1) >= 2.0 ** -6
+    rel = np.abs(deq - x)[normal] / np.abs(x)[normal]
+    assert rel.max() <= 2.0 ** -4 + 1e-12
+
+
+def test_ragged_rows_are_padded_for_amax_only():
+    x = np.ones((1, 1, 40, 64))
+    codes, e, deq = M.quantize_blocks(x)
+    assert codes.shape == (1, 1, 40, 64) and e.shape == (1, 1, 2, 2)
+    assert np.array_equal(deq, x)
