@@ -40,7 +40,8 @@ UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = I.NONCAUSAL_D128.name
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = ["online_softmax_fwd_gb300/csrc/fwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/ptx.cuh",
-                  "online_softmax_fwd_gb300/csrc/exp2_fma.cuh"]
+                  "online_softmax_fwd_gb300/csrc/exp2_fma.cuh", "online_softmax_fwd_gb300/csrc/fwd_mxfp8.cuh",
+                  "online_softmax_fwd_gb300/csrc/mxfp8_common.cuh"]
 
 
 def kernel_sources_sha() -> str:
@@ -62,11 +63,11 @@ def measured_peaks() -> dict:
 def profiled_traffic(workload: str) -> float | None:
     """DRAM bytes per launch from the committed ncu summary of this workload,
     if it was taken on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"fwd_bf16_{workload}.md")
-    try:
-        text = open(path).read()
-    except OSError:
+    prof = os.path.join(ROOT, "profiles")
+    names = [f for f in (os.listdir(prof) if os.path.isdir(prof) else []) if f.endswith(f"_{workload}.md")]
+    if not names:
         return None
+    text = open(os.path.join(prof, sorted(names)[0])).read()
     sha = re.search(r"kernel_sources_sha:\s*([0-9a-f]+)", text)
     val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     if not sha or not val or sha.group(1) != kernel_sources_sha():
@@ -202,17 +203,23 @@ def oracle_sample(w: I.Workload, q, k, v, seconds: float, rows_per_call: int = 5
     sample description and its rate in the metric's units (useful FLOP of the
     computed rows, causal rows counting only their allowed keys)."""
     from oracle.attention import attention_rows
+    if w.dtype == "mxfp8":
+        from oracle.mxfp8 import quantize_blocks
+        prep = lambda t: quantize_blocks(I.as_f64(t))[2]
+    else:
+        prep = I.as_f64
     t0 = time.perf_counter()
     flops = 0.0
     rows_done = 0
     heads = 0
     for b in range(w.B):
         for h in range(w.H):
-            kk, vv = I.as_f64(k[b, h]), I.as_f64(v[b, h])
+            kk, vv = prep(k[b, h]), prep(v[b, h])
+            qq = prep(q[b, h])
             for r0 in range(0, w.N, rows_per_call):
                 r1 = min(w.N, r0 + rows_per_call)
                 idx = np.arange(r0, r1)
-                attention_rows(I.as_f64(q[b, h, r0:r1]), kk, vv, idx, w.causal, w.scale)
+                attention_rows(qq[r0:r1], kk, vv, idx, w.causal, w.scale)
                 keys = (idx + 1).sum() if w.causal else (r1 - r0) * w.N
                 flops += 4.0 * keys * w.d
                 rows_done += r1 - r0
@@ -231,7 +238,7 @@ def oracle_sample(w: I.Workload, q, k, v, seconds: float, rows_per_call: int = 5
 def bench_reference(args, w: I.Workload, world: int, rank: int) -> None:
     if rank != 0:
         return
-    q, k, v = I.bf16_qkv(w) if w.dtype == "bf16" else tuple(I.to_bf16(x) for x in I.draw_fp32(
+    q, k, v = I.bf16_qkv(w) if w.dtype == "bf16" else tuple(torch.from_numpy(x) for x in I.draw_fp32(
         w.B, w.H, w.N, w.d, w.qk_std, w.v_std, w.seed))
     cores = torch.get_num_threads()
     per_step = max(1.0, args.reference_seconds / max(1, args.steps + args.warmup))
@@ -254,30 +261,130 @@ def bench_reference(args, w: I.Workload, world: int, rank: int) -> None:
     print(json.dumps(out), flush=True)
 
 
+class Bf16Step:
+    """One pass of the bf16 path: attn_fwd over the resident inputs."""
+
+    launches = 1
+
+    def __init__(self, attn, w, dev, args):
+        self.attn, self.w, self.args = attn, w, args
+        self.q_h, self.k_h, self.v_h = I.bf16_qkv(w)
+        self.q, self.k, self.v = (t.to(dev) for t in (self.q_h, self.k_h, self.v_h))
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+        self.ptrs = tuple(t.data_ptr() for t in (self.q, self.k, self.v, self.o, self.lse))
+
+    def run(self, sh, ev=None):
+        w = self.w
+        if ev:
+            ev[0].record()
+        st = self.attn.attn_fwd_raw(*self.ptrs, w.B, w.H, w.N, w.d, int(w.causal), float(w.scale), sh,
+                                    tau=self.args.tau, exp2_emu16=self.args.exp2_emu16)
+        if ev:
+            ev[1].record()
+        if st != 0:
+            raise self.attn.AttnError(st, "attn_fwd")
+
+    def input_bytes(self):
+        return 3 * self.q.numel() * 2
+
+    def e2e(self, dev, n_steps, world):
+        w = self.w
+        qp, kp, vp = (t.pin_memory() for t in (self.q_h, self.k_h, self.v_h))
+        o_host = torch.empty_like(qp).pin_memory()
+        lse_host = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+        ws = {}
+        call = lambda: self.attn.attn_fwd_from_host(qp, kp, vp, w.causal, w.scale, device=dev, o_host=o_host,
+                                                    lse_host=lse_host, workspace=ws)
+        for _ in range(2):
+            call()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(n_steps):
+            call()
+        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+        return {"value": w.flops * n_steps * world / dt / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": 3 * qp.numel() * 2, "d2h_bytes_per_step": o_host.numel() * 2 + lse_host.numel() * 4,
+                "steps": n_steps}
+
+
+class Mxfp8Step:
+    """One pass of the MXFP8 path: quantise Q, K, V (fp32 resident in HBM) to
+    E4M3 + E8M0 and run the block-scaled attention."""
+
+    launches = 4
+
+    def __init__(self, attn, w, dev, args):
+        self.attn, self.w, self.args = attn, w, args
+        self.xq_h, self.xk_h, self.xv_h = (torch.from_numpy(x) for x in I.draw_fp32(
+            w.B, w.H, w.N, w.d, w.qk_std, w.v_std, w.seed))
+        self.x = [t.to(dev) for t in (self.xq_h, self.xk_h, self.xv_h)]
+        nsf = attn.mxfp8_scale_bytes(w.B, w.H, w.N, w.d)
+        self.codes = [torch.empty(t.shape, dtype=torch.uint8, device=dev) for t in self.x]
+        self.sf = [torch.empty(nsf, dtype=torch.uint8, device=dev) for _ in self.x]
+        self.o = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+        self.tau = 0.0 if args.tau_given is None else args.tau
+
+    def run(self, sh, ev=None):
+        w, L = self.w, self.attn.lib()
+        for i, role in enumerate((0, 0, 1)):
+            st = L.attn_mxfp8_quantize(self.x[i].data_ptr(), self.codes[i].data_ptr(), self.sf[i].data_ptr(),
+                                       w.B, w.H, w.N, w.d, role, sh)
+            if st != 0:
+                raise self.attn.AttnError(st, "attn_mxfp8_quantize")
+        if ev:
+            ev[0].record()
+        st = L.attn_fwd_mxfp8_ex(self.codes[0].data_ptr(), self.sf[0].data_ptr(), self.codes[1].data_ptr(),
+                                 self.sf[1].data_ptr(), self.codes[2].data_ptr(), self.sf[2].data_ptr(),
+                                 self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N, w.d, int(w.causal),
+                                 float(w.scale), float(self.tau), int(self.args.exp2_emu16), sh)
+        if ev:
+            ev[1].record()
+        if st != 0:
+            raise self.attn.AttnError(st, "attn_fwd_mxfp8")
+
+    def input_bytes(self):
+        return 3 * self.x[0].numel() * 4
+
+    def e2e(self, dev, n_steps, world):
+        w = self.w
+        hp = [t.pin_memory() for t in (self.xq_h, self.xk_h, self.xv_h)]
+        o_host = torch.empty(self.o.shape, dtype=torch.bfloat16).pin_memory()
+        lse_host = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+        sh = torch.cuda.current_stream(dev).cuda_stream
+
+        def call():
+            for d_, h_ in zip(self.x, hp):
+                d_.copy_(h_, non_blocking=True)
+            self.run(sh)
+            o_host.copy_(self.o, non_blocking=True)
+            lse_host.copy_(self.lse, non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+        for _ in range(2):
+            call()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(n_steps):
+            call()
+        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+        return {"value": w.flops * n_steps * world / dt / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": sum(h.numel() * 4 for h in hp),
+                "d2h_bytes_per_step": o_host.numel() * 2 + lse_host.numel() * 4, "steps": n_steps}
+
+
 def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
     import online_softmax_fwd_gb300 as attn
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     attn.lib()
-    q_h, k_h, v_h = I.bf16_qkv(w)
-    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
-    o = torch.empty_like(q)
-    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    step = (Mxfp8Step if w.dtype == "mxfp8" else Bf16Step)(attn, w, dev, args)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
-
-    def step():
-        st = attn.attn_fwd_raw(*ptrs, w.B, w.H, w.N, w.d, int(w.causal), float(w.scale), sh,
-                               tau=args.tau, exp2_emu16=args.exp2_emu16)
-        if st != 0:
-            raise attn.AttnError(st, "attn_fwd")
-
     for _ in range(args.warmup):
-        step()
+        step.run(sh)
     torch.cuda.synchronize(dev)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     sampler = ClockSampler(dev)
     barrier(world)
     sampler.start()
@@ -287,9 +394,7 @@ def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
     region1 = torch.cuda.Event(enable_timing=True)
     region0.record(stream)
     for i in range(args.steps):
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
+        step.run(sh, evs[i])
     region1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -299,62 +404,56 @@ def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
     if st != attn.Status.OK:
         raise RuntimeError(f"device status after the timed region: {st!r}")
     region_ms = region0.elapsed_time(region1)
-    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    launch_ms = [a.elapsed_time(b) for a, b in evs]
     region_ms_max = max_over_ranks(region_ms, world, dev)
-    total_flop = w.flops * args.steps * world
-    value = total_flop / (region_ms_max * 1e-3) / 1e12
+    value = w.flops * args.steps * world / (region_ms_max * 1e-3) / 1e12
 
-    # end to end through the public API: pinned host inputs in, host O and LSE out
-    e2e = None
-    if not args.no_e2e:
-        qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
-        o_host = torch.empty_like(qp).pin_memory()
-        lse_host = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
-        ws = {}
-        for _ in range(2):
-            attn.attn_fwd_from_host(qp, kp, vp, w.causal, w.scale, device=dev, o_host=o_host, lse_host=lse_host,
-                                    workspace=ws)
-        n_e2e = max(3, min(args.steps, 10))
-        barrier(world)
-        t0 = time.perf_counter()
-        for _ in range(n_e2e):
-            attn.attn_fwd_from_host(qp, kp, vp, w.causal, w.scale, device=dev, o_host=o_host, lse_host=lse_host,
-                                    workspace=ws)
-        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
-        e2e = {"value": w.flops * n_e2e * world / dt / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": 3 * q_h.numel() * 2, "d2h_bytes_per_step": o_host.numel() * 2 + lse_host.numel() * 4,
-               "steps": n_e2e}
+    e2e = None if args.no_e2e else step.e2e(dev, max(3, min(args.steps, 10)), world)
 
     peaks = measured_peaks()
-    peak = peaks.get("bf16_tflops")
+    bf16_peak = peaks.get("bf16_tflops")
+    src = "measured bf16_tflops (burst, cuBLAS)" if bf16_peak else "fallback 1900 bf16"
+    if not bf16_peak:
+        bf16_peak = 1900.0
+    if w.dtype == "mxfp8":
+        peak = 2.0 * bf16_peak   # FP8 dense = 2 x bf16 dense (4.5 / 2.25 PFLOP/s nominal)
+        src += " x 2 (nominal FP8/bf16 ratio)"
+    else:
+        peak = bf16_peak
     avg_launch_s = float(np.mean(launch_ms)) * 1e-3
     achieved = w.flops / avg_launch_s / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": (achieved / peak) if peak else None, "traffic": profiled_traffic(w.name),
-                "peak_source": "measured bf16_tflops (burst, cuBLAS)" if peak else "fallback 1900",
-                "flop_per_launch": w.flops}
-    if not peak:
-        roofline["peak"] = 1900.0
-        roofline["frac"] = achieved / 1900.0
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": profiled_traffic(w.name), "peak_source": src, "flop_per_launch": w.flops,
+                "kernel": "attn_fwd_mxfp8_kernel" if w.dtype == "mxfp8" else "attn_fwd_bf16_kernel"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        s = oracle_sample(w, q_h, k_h, v_h, args.cpu_seconds)
+        s = oracle_sample(w, *cpu_inputs(step, w), args.cpu_seconds)
         cpu = {"value": s["value"], "unit": UNIT, "cores": torch.get_num_threads(), "kind": "oracle",
                "sample": f"float64 one-shot oracle on {s['rows']} query rows of the workload's first "
-                         f"{s['heads_touched']} head(s) against all their keys, {s['seconds']:.1f} s"}
+                         f"{s['heads_touched']} head(s) against all their keys, {s['seconds']:.1f} s"
+                         + (" (inputs: the oracle's own MXFP8 quantisation, dequantised)" if w.dtype == "mxfp8" else "")}
     clocks = sampler.summary(t_wall0, t_wall1)
     if rank == 0:
         out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                "warmup": args.warmup, "ms_per_step": region_ms_max / args.steps, "higher_is_better": True,
-               "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+               "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8" if w.dtype == "mxfp8" else "bf16",
+               "data": "synthetic",
                "config": {**w.describe(), "parallelism": f"replicas{world}" if world > 1 else "single",
-                          "l2": f"inputs larger than L2 (Q+K+V = {3 * q.numel() * 2 / 2**20:.0f} MiB > 129 MB)",
-                          "tau": args.tau, "exp2_emu16": args.exp2_emu16},
-               "e2e": e2e, "gpu_launches": args.steps, "roofline": roofline, "cpu_baseline": cpu,
+                          "l2": f"inputs larger than L2 ({step.input_bytes() / 2**20:.0f} MiB > 129 MB)",
+                          "tau": step.tau if w.dtype == "mxfp8" else args.tau, "exp2_emu16": args.exp2_emu16},
+               "e2e": e2e, "gpu_launches": args.steps * step.launches, "roofline": roofline, "cpu_baseline": cpu,
                "clocks": clocks, "kernel_ms": {"mean": float(np.mean(launch_ms)), "min": float(np.min(launch_ms)),
                                                "max": float(np.max(launch_ms))}}
         print(json.dumps(out), flush=True)
+
+
+def cpu_inputs(step, w):
+    """Inputs for the oracle sample: the bf16 tensors, or for MXFP8 the oracle's
+    own dequantisation of the fp32 draws (per head, inside oracle_sample)."""
+    if w.dtype == "mxfp8":
+        return step.xq_h, step.xk_h, step.xv_h
+    return step.q_h, step.k_h, step.v_h
 
 
 def main() -> None:
@@ -364,10 +463,11 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
     ap.add_argument("--shape", default=None,
-                    help="B,H,N,d[,causal] instead of a named workload (profiling a smaller case)")
+                    help="B,H,N,d[,causal[,mxfp8]] instead of a named workload (profiling a smaller case)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--exp2-emu16", type=int, default=0)
-    ap.add_argument("--tau", type=float, default=8.0)
+    ap.add_argument("--tau", type=float, default=None,
+                    help="rescale threshold (default 8 for bf16 P, 0 for FP8 P)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -376,13 +476,15 @@ def main() -> None:
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = I.WORKLOADS[args.workload]
+    args.tau_given = args.tau
+    if args.tau is None:
+        args.tau = 8.0
     if args.shape:
         f = [int(x) for x in args.shape.split(",")]
         causal = bool(f[4]) if len(f) > 4 else False
-        w = I.Workload(f"custom_b{f[0]}h{f[1]}n{f[2]}d{f[3]}{'_causal' if causal else ''}", f[0], f[1], f[2], f[3],
-                       causal)
-    if w.dtype != "bf16" and args.impl == "ours":
-        ap.error(f"{w.name}: only the bf16 workloads are benchmarked by this build")
+        dt = "mxfp8" if len(f) > 5 and f[5] else "bf16"
+        w = I.Workload(f"custom_b{f[0]}h{f[1]}n{f[2]}d{f[3]}{'_causal' if causal else ''}{'_mxfp8' if dt == 'mxfp8' else ''}",
+                       f[0], f[1], f[2], f[3], causal, dtype=dt)
     world, rank, local = dist_setup(args.gpus)
     try:
         if args.impl == "reference":

@@ -93,6 +93,62 @@ attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, 
                           int N, int d, int causal, float scale, float tau, int exp2_emu16, void* stream);
 
 /*
+ * MXFP8 variant ("PyTorch FlashAttention-4 adds MXFP8 block-scaled forward and
+ * backward for Blackwell"): Q, K, V in E4M3 with one E8M0 (power-of-two) scale
+ * per 32 x 32 block -- Q and K blocked along d for S = Q K^T, V along the
+ * sequence for O = P V (section "Quantization along both axes and jagged
+ * tensors") -- and P converted to MXFP8 online per 32 keys inside the kernel
+ * (section "Softmax conversion and unroll-KV"). Only d = 128.
+ *
+ * Scale arrays ("atoms"): for each (b, h) and each 128-row tile t of the
+ * sequence, 512 bytes at offset ((b*H + h) * ceil(N/128) + t) * 512 holding the
+ * E8M0 scales of 128 rows x 4 blocks of 32 along the GEMM's K dimension; row r,
+ * block kb at byte (r % 32) * 16 + (r / 32) * 4 + kb. For Q and K (role 0) the
+ * row is the sequence position in the tile and kb = d / 32; for V (role 1) the
+ * row is the d column and kb the 32-key block of the tile. This is the layout
+ * the block-scaled tensor-core MMA reads after tcgen05.cp.
+ */
+
+/* Bytes of one tensor's scale array: B*H*ceil(N/128)*512; 0 if any size is
+ * <= 0 or d != 128. The caller allocates it (device, 16-byte aligned). */
+size_t attn_mxfp8_scale_bytes(int B, int H, int N, int d);
+
+/*
+ * attn_mxfp8_quantize -- fp32 [B,H,N,d] (device, 16-byte aligned) to E4M3
+ * codes [B,H,N,d] (x_e4m3, one byte each) and the scale array (x_scales).
+ * Each 32 x 32 block (rows past N count as zero) takes the smallest power of
+ * two 2^e with amax / 2^e <= 448; elements are multiplied by 2^-e and rounded
+ * to E4M3, nearest even, saturating at +-448. role 0: Q or K; role 1: V.
+ * d must be 128 (else ATTN_ERR_UNSUPPORTED); B*H <= 65535. Asynchronous on
+ * stream; allocates nothing.
+ */
+attn_status_t attn_mxfp8_quantize(const float* x, void* x_e4m3, void* x_scales, int B, int H, int N, int d,
+                                  int role, void* stream);
+
+/*
+ * attn_fwd_mxfp8 -- attention forward from MXFP8 inputs (the outputs of
+ * attn_mxfp8_quantize: q8/q_sf and k8/k_sf with role 0, v8/v_sf with role 1),
+ * block-scaled tensor-core MMAs with fp32 accumulation, P converted to
+ * E4M3 with one E8M0 scale per 32 keys (the block's amax from its score max),
+ * the row sum taken from fp32 P. o, lse, B, H, N, causal, scale as attn_fwd;
+ * d must be 128. All pointers device, 16-byte aligned (lse: 4).
+ * tau = 0: the threshold is dtype-aware ("FlashAttention-4's Softmax Tricks",
+ * section "Where exact breaks: P in FP8": 8 for 16-bit P, 0 for FP8). With a
+ * stale max a row's largest P is 2^delta, not exactly 1, and E4M3's 3-bit
+ * mantissa rounds it by up to 2^-4, which on peaked rows moves O by several
+ * 1e-2; with tau = 0 it is exactly 1 and exact in E4M3 after its scale.
+ */
+attn_status_t attn_fwd_mxfp8(const void* q8, const void* q_sf, const void* k8, const void* k_sf, const void* v8,
+                             const void* v_sf, void* o, float* lse, int B, int H, int N, int d, int causal,
+                             float scale, void* stream);
+
+/* attn_fwd_mxfp8 with tau in [0, 16] and a software-exp2 share of 0, 2 or 4
+ * of every 16 score columns (others: ATTN_ERR_UNSUPPORTED). */
+attn_status_t attn_fwd_mxfp8_ex(const void* q8, const void* q_sf, const void* k8, const void* k_sf, const void* v8,
+                                const void* v_sf, void* o, float* lse, int B, int H, int N, int d, int causal,
+                                float scale, float tau, int exp2_emu16, void* stream);
+
+/*
  * attn_exp2_emulated -- y[i] = software exp2 of x[i] for i < n, computed by
  * the very device function the attention kernels use on the FMA pipe (see
  * attn_fwd_ex). For checking that function bit for bit against a scalar model.

@@ -43,6 +43,13 @@ _SIGNATURES = {
     # ..., scale, tau, exp2_emu16, stream
     "attn_fwd_ex": ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
                     + [ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
+    "attn_mxfp8_scale_bytes": ([ctypes.c_int] * 4, ctypes.c_size_t),
+    # x, x_e4m3, x_scales, B, H, N, d, role, stream
+    "attn_mxfp8_quantize": ([ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [ctypes.c_void_p], ctypes.c_int),
+    # q8, q_sf, k8, k_sf, v8, v_sf, o, lse, B, H, N, d, causal, scale, stream
+    "attn_fwd_mxfp8": ([ctypes.c_void_p] * 8 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_void_p], ctypes.c_int),
+    "attn_fwd_mxfp8_ex": ([ctypes.c_void_p] * 8 + [ctypes.c_int] * 5
+                          + [ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
     "attn_exp2_emulated": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p], ctypes.c_int),
     "attn_get_device_status": ([ctypes.c_void_p], ctypes.c_int),
     "attn_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -169,6 +176,56 @@ def attn_fwd_from_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal
     lse_host.copy_(ws["lse"], non_blocking=True)
     torch.cuda.current_stream(dev).synchronize()
     return o_host, lse_host
+
+
+def mxfp8_scale_bytes(B: int, H: int, N: int, d: int) -> int:
+    return lib().attn_mxfp8_scale_bytes(B, H, N, d)
+
+
+def mxfp8_quantize(x: torch.Tensor, role: int, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """fp32 CUDA [B,H,N,128] -> (E4M3 codes uint8 [B,H,N,128], scale atoms uint8
+    [B*H*ceil(N/128)*512]). role 0: Q or K; role 1: V."""
+    if not x.is_cuda or x.dtype != torch.float32 or x.dim() != 4 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA float32 tensor [B,H,N,d]")
+    B, H, N, d = x.shape
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(max(1, mxfp8_scale_bytes(B, H, N, d)), dtype=torch.uint8, device=x.device)
+    with torch.cuda.device(x.device):
+        _check(lib().attn_mxfp8_quantize(_ptr(x), _ptr(codes), _ptr(scales), B, H, N, d, int(role),
+                                         _stream_handle(stream)), "attn_mxfp8_quantize")
+    return codes, scales
+
+
+def attn_fwd_mxfp8(q8: torch.Tensor, q_sf: torch.Tensor, k8: torch.Tensor, k_sf: torch.Tensor, v8: torch.Tensor,
+                   v_sf: torch.Tensor, causal: bool = False, scale: float | None = None, o: torch.Tensor | None = None,
+                   lse: torch.Tensor | None = None, tau: float = 0.0, exp2_emu16: int = 0,
+                   stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Attention forward from MXFP8 inputs (outputs of mxfp8_quantize); tau
+    defaults to 0, the FP8 setting (attn_fwd_mxfp8)."""
+    for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
+        if not t.is_cuda or t.dtype != torch.uint8 or t.dim() != 4 or not t.is_contiguous() or t.shape != q8.shape:
+            raise ValueError(f"{name} must be contiguous CUDA uint8 (E4M3 codes) shaped like q8")
+    B, H, N, d = q8.shape
+    need = mxfp8_scale_bytes(B, H, N, d)
+    for name, t in (("q_sf", q_sf), ("k_sf", k_sf), ("v_sf", v_sf)):
+        if not t.is_cuda or t.dtype != torch.uint8 or t.numel() < need:
+            raise ValueError(f"{name} must be a CUDA uint8 scale array of >= {need} bytes")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    h = _stream_handle(stream)
+    ptrs = [_ptr(t) for t in (q8, q_sf, k8, k_sf, v8, v_sf, o, lse)]
+    with torch.cuda.device(q8.device):
+        if tau == 0.0 and exp2_emu16 == 0:
+            st = lib().attn_fwd_mxfp8(*ptrs, B, H, N, d, int(bool(causal)), float(scale), h)
+        else:
+            st = lib().attn_fwd_mxfp8_ex(*ptrs, B, H, N, d, int(bool(causal)), float(scale), float(tau),
+                                         int(exp2_emu16), h)
+    _check(st, "attn_fwd_mxfp8")
+    return o, lse
 
 
 def exp2_emulated(x: torch.Tensor, stream=None) -> torch.Tensor:

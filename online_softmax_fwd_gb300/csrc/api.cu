@@ -14,6 +14,7 @@
 #include "exp2_fma.cuh"
 #include "fwd_bf16.cuh"
 #include "fwd_dispatch.h"
+#include "fwd_mxfp8.cuh"
 
 namespace {
 
@@ -67,7 +68,30 @@ bool make_map(CUtensorMap* m, const void* base, int d, int n, long long bh) {
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over a contiguous [B*H, N, 128] E4M3 tensor: one 128-byte swizzle
+// row per sequence row, boxes of 128 rows.
+bool make_map_e4m3(CUtensorMap* m, const void* base, int n, long long bh) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {128u, 128u * static_cast<cuuint64_t>(n)};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+long long band_for(long long kv_head_bytes, long long bh) {
+  // heads whose K and V fit together in ~48 MiB of L2
+  long long band = (48LL << 20) / (kv_head_bytes > 0 ? kv_head_bytes : 1);
+  if (band < 1) band = 1;
+  if (band > bh) band = bh;
+  return band;
+}
 
 attn_status_t check_fwd_args(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,
                              int H, int N, int d, int causal, float scale, float tau, int emu16, bool* empty) {
@@ -124,12 +148,7 @@ attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, 
   const int n_pairs = (N + 255) / 256;
   a.n_pairs = n_pairs;
   a.bh = static_cast<int>(bh);
-  // heads whose K and V (2*N*d*2 bytes each) fit together in ~48 MiB of L2
-  const long long kv_head_bytes = 4LL * N * d;
-  long long band = (48LL << 20) / (kv_head_bytes > 0 ? kv_head_bytes : 1);
-  if (band < 1) band = 1;
-  if (band > bh) band = bh;
-  a.band = static_cast<int>(band);
+  a.band = static_cast<int>(band_for(4LL * N * d, bh));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (d == 64)
@@ -144,6 +163,72 @@ attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                        int causal, float scale, void* stream) {
   return attn_fwd_ex(q, k, v, o, lse, B, H, N, d, causal, scale, 8.0f, 0, stream);
+}
+
+size_t attn_mxfp8_scale_bytes(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0 || d != 128) return 0;
+  return static_cast<size_t>(B) * H * ((N + 127) / 128) * 512u;
+}
+
+attn_status_t attn_mxfp8_quantize(const float* x, void* x_e4m3, void* x_scales, int B, int H, int N, int d, int role,
+                                  void* stream) {
+  if (B < 0 || H < 0 || N < 0 || (role != 0 && role != 1)) return ATTN_ERR_INVALID_ARG;
+  if (d != 128) return d > 0 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
+  if (N > kMaxN || static_cast<long long>(B) * H > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (!x || !x_e4m3 || !x_scales) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_e4m3) || !aligned16(x_scales)) return ATTN_ERR_MISALIGNED;
+  cudaError_t e = attn::launch_mxfp8_quantize(x, static_cast<uint8_t*>(x_e4m3), static_cast<uint8_t*>(x_scales),
+                                              static_cast<long long>(B) * H, N, role, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_fwd_mxfp8_ex(const void* q8, const void* q_sf, const void* k8, const void* k_sf, const void* v8,
+                                const void* v_sf, void* o, float* lse, int B, int H, int N, int d, int causal,
+                                float scale, float tau, int exp2_emu16, void* stream) {
+  if (B < 0 || H < 0 || N < 0 || (causal != 0 && causal != 1)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(tau) || tau < 0.f || tau > 16.f) return ATTN_ERR_INVALID_ARG;
+  if (d != 128) return d > 0 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
+  if (exp2_emu16 < 0 || exp2_emu16 > 16) return ATTN_ERR_INVALID_ARG;
+  if (exp2_emu16 != 0 && exp2_emu16 != 2 && exp2_emu16 != 4) return ATTN_ERR_UNSUPPORTED;
+  if (N > kMaxN || static_cast<long long>(B) * H * ((N + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (!q8 || !q_sf || !k8 || !k_sf || !v8 || !v_sf || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(q_sf) || !aligned16(k_sf) ||
+      !aligned16(v_sf) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  const long long bh = static_cast<long long>(B) * H;
+  CUtensorMap mq, mk, mv;
+  if (!make_map_e4m3(&mq, q8, N, bh) || !make_map_e4m3(&mk, k8, N, bh) || !make_map_e4m3(&mv, v8, N, bh))
+    return ATTN_ERR_CUDA;
+  unsigned int* status = status_word();
+  if (!status) return ATTN_ERR_CUDA;
+  attn::FwdMxArgs a;
+  a.q_sf = static_cast<const uint8_t*>(q_sf);
+  a.k_sf = static_cast<const uint8_t*>(k_sf);
+  a.v_sf = static_cast<const uint8_t*>(v_sf);
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.status = status;
+  a.n = N;
+  a.n_tiles = (N + 127) / 128;
+  a.bh = static_cast<int>(bh);
+  a.band = static_cast<int>(band_for(2LL * N * 128, bh));
+  a.scale = scale;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.tau = tau;
+  cudaError_t e = attn::launch_fwd_mxfp8_d128(causal, exp2_emu16, mq, mk, mv, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_fwd_mxfp8(const void* q8, const void* q_sf, const void* k8, const void* k_sf, const void* v8,
+                             const void* v_sf, void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
+                             void* stream) {
+  // tau = 0 for FP8 P: with a stale max a row's largest P is 2^delta instead of
+  // exactly 1 and E4M3 rounds it by up to 2^-4 (FlashAttention-4's Softmax
+  // Tricks, "Where exact breaks: P in FP8": tau 8 for 16-bit P, 0 for FP8)
+  return attn_fwd_mxfp8_ex(q8, q_sf, k8, k_sf, v8, v_sf, o, lse, B, H, N, d, causal, scale, 0.0f, 0, stream);
 }
 
 attn_status_t attn_exp2_emulated(const float* x, float* y, long long n, void* stream) {

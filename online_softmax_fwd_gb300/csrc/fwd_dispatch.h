@@ -4,9 +4,12 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstdint>
+
 namespace attn {
 
 struct FwdArgs;
+struct FwdMxArgs;
 
 cudaError_t launch_fwd_bf16_d64_c0(int emu16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                    const FwdArgs& a, int bh, int n_pairs, cudaStream_t s);
@@ -16,5 +19,10 @@ cudaError_t launch_fwd_bf16_d128_c0(int emu16, const CUtensorMap& q, const CUten
                                     const FwdArgs& a, int bh, int n_pairs, cudaStream_t s);
 cudaError_t launch_fwd_bf16_d128_c1(int emu16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                     const FwdArgs& a, int bh, int n_pairs, cudaStream_t s);
+
+cudaError_t launch_fwd_mxfp8_d128(int causal, int emu16, const CUtensorMap& q, const CUtensorMap& k,
+                                  const CUtensorMap& v, const FwdMxArgs& a, cudaStream_t s);
+cudaError_t launch_mxfp8_quantize(const float* x, uint8_t* q, uint8_t* atoms, long long bh, int n, int role,
+                                  cudaStream_t stream);
 
 }  // namespace attn

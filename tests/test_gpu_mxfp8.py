@@ -1,0 +1,146 @@
+"""MXFP8 path on the GPU, through the C ABI.
+
+The quantiser must equal the oracle's bit for bit (E4M3 codes and E8M0 scales,
+the latter expanded into the documented 512-byte atom layout). The attention
+output is compared with the float64 oracle run on the dequantised inputs, with
+the MXFP8 bound of 6e-2 on O (P is quantised to E4M3 inside the kernel) and
+1e-3 on LSE (computed from fp32 P).
+"""
+import numpy as np
+import pytest
+import torch
+
+import attn_inputs as I
+from oracle import mxfp8 as M
+from oracle.attention import attention_fwd, attention_rows
+from parity import sample_rows
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+O_MAX_ABS_MXFP8 = 6e-2
+LSE_MAX_ABS = 1e-3
+
+
+@pytest.fixture(scope="module")
+def attn():
+    import online_softmax_fwd_gb300 as a
+    a.lib()
+    return a
+
+
+def atoms_from_oracle(e: np.ndarray, role: int) -> np.ndarray:
+    """Expand oracle block exponents e [BH, N/32, 4] into the atom layout:
+    per 128-row tile, byte (r%32)*16 + (r/32)*4 + kb."""
+    bh, nb, db = e.shape
+    tiles = -(-nb // 4)
+    out = np.zeros((bh, tiles, 512), np.uint8)
+    r = np.arange(128)[:, None]
+    kb = np.arange(4)[None, :]
+    idx = (r % 32) * 16 + (r // 32) * 4 + kb
+    for t in range(tiles):
+        for h in range(bh):
+            if role == 0:   # row = sequence row, kb = d block
+                rb = np.minimum(4 * t + r // 32, nb - 1)
+                val = e[h, rb, kb] + 127
+                valid = (4 * t + r // 32) < nb
+            else:           # row = d column, kb = key block of the tile
+                kbb = 4 * t + kb
+                val = e[h, np.minimum(kbb, nb - 1), r // 32] + 127
+                valid = kbb < nb
+            tile_atom = out[h, t]
+            tile_atom[idx[np.broadcast_to(valid, idx.shape)]] = val[np.broadcast_to(valid, idx.shape)]
+    return out
+
+
+def quantize_gpu(attn, x32: np.ndarray, role: int):
+    codes, sf = attn.mxfp8_quantize(torch.from_numpy(x32).to(DEV), role)
+    torch.cuda.synchronize()
+    return codes, sf
+
+
+@pytest.mark.parametrize("N", [128, 256, 300, 1000])
+@pytest.mark.parametrize("role", [0, 1])
+def test_quantizer_bit_exact(attn, N, role):
+    x, _, _ = I.draw_fp32(2, 3, N, 128, seed=N + role)
+    x[0, 1, :min(N, 64), :32] *= 300.0      # blocks with very different scales
+    x[1, 2, :min(N, 32), 96:] = 0.0         # an all-zero block when N allows
+    codes, sf = quantize_gpu(attn, x, role)
+    o_codes, o_e, _ = M.quantize_blocks(x.reshape(6, N, 128))
+    assert np.array_equal(codes.cpu().numpy().reshape(6, N, 128), o_codes)
+    got = sf.cpu().numpy().reshape(6, -1, 512)
+    want = atoms_from_oracle(o_e, role)
+    if N % 128 == 0:
+        assert np.array_equal(got, want)
+    else:  # bytes of rows (role 0) / key blocks (role 1) past N are free
+        mask = atoms_from_oracle(np.zeros_like(o_e) + 1, role) > 0
+        assert np.array_equal(got[mask], want[mask])
+
+
+def run_mxfp8(attn, w_causal, x_q, x_k, x_v, scale, **kw):
+    q8, q_sf = quantize_gpu(attn, x_q, 0)
+    k8, k_sf = quantize_gpu(attn, x_k, 0)
+    v8, v_sf = quantize_gpu(attn, x_v, 1)
+    o, lse = attn.attn_fwd_mxfp8(q8, q_sf, k8, k_sf, v8, v_sf, causal=w_causal, scale=scale, **kw)
+    torch.cuda.synchronize()
+    assert attn.device_status() == attn.Status.OK
+    return o.cpu(), lse.cpu()
+
+
+def check(o, lse, o_ref, lse_ref, what):
+    err = np.abs(I.as_f64(o) - o_ref)
+    lerr = np.abs(lse.double().numpy() - lse_ref)
+    assert np.isfinite(err).all() and np.isfinite(lerr).all(), what
+    assert err.max() <= O_MAX_ABS_MXFP8, f"{what}: O max abs {err.max():.4g} mean {err.mean():.3g}"
+    assert lerr.max() <= LSE_MAX_ABS, f"{what}: LSE max abs {lerr.max():.3g}"
+    return err.max(), err.mean()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(1, 1, 128), (1, 2, 256), (2, 1, 300), (1, 2, 1000), (1, 1, 1024)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_small_shapes(attn, shape, causal):
+    B, H, N = shape
+    xq, xk, xv = I.draw_fp32(B, H, N, 128, seed=N + 7)
+    o, lse = run_mxfp8(attn, causal, xq, xk, xv, 128 ** -0.5)
+    deq = [M.quantize_blocks(x.reshape(B * H, N, 128))[2].reshape(B, H, N, 128) for x in (xq, xk, xv)]
+    o_ref, lse_ref = attention_fwd(*deq, causal, 128 ** -0.5)
+    check(o, lse, o_ref, lse_ref, f"{shape} causal={causal}")
+
+
+def peaked_case():
+    # Q, K ~ N(0, 2^2): peaked rows whose largest P dominates the output
+    xq, xk, xv = I.draw_fp32(1, 2, 768, 128, qk_std=2.0, seed=31)
+    deq = [M.quantize_blocks(x.reshape(2, 768, 128))[2].reshape(1, 2, 768, 128) for x in (xq, xk, xv)]
+    return (xq, xk, xv), attention_fwd(*deq, True, 128 ** -0.5)
+
+
+@pytest.mark.parametrize("emu", [0, 2, 4])
+def test_software_exp2_shares_on_peaked_rows(attn, emu):
+    (xq, xk, xv), (o_ref, lse_ref) = peaked_case()
+    o, lse = run_mxfp8(attn, True, xq, xk, xv, 128 ** -0.5, exp2_emu16=emu)
+    check(o, lse, o_ref, lse_ref, f"emu={emu}")
+
+
+def test_lagging_max_costs_accuracy_with_fp8_p(attn):
+    # the reason for tau = 0 with FP8 P: with tau = 8 the dominant P is 2^delta
+    # and E4M3 rounds it by up to 2^-4; with tau = 0 it is exactly 1
+    (xq, xk, xv), (o_ref, lse_ref) = peaked_case()
+    o0, _ = run_mxfp8(attn, True, xq, xk, xv, 128 ** -0.5, tau=0.0)
+    o8, lse8 = run_mxfp8(attn, True, xq, xk, xv, 128 ** -0.5, tau=8.0)
+    e0 = np.abs(I.as_f64(o0) - o_ref).max()
+    e8 = np.abs(I.as_f64(o8) - o_ref).max()
+    assert e8 > 1.5 * e0
+    assert np.abs(lse8.double().numpy() - lse_ref).max() <= LSE_MAX_ABS  # LSE comes from fp32 P either way
+
+
+def test_full_size_workload_sampled(attn):
+    w = I.MXFP8_CAUSAL
+    xq, xk, xv = I.draw_fp32(w.B, w.H, w.N, w.d, w.qk_std, w.v_std, w.seed)
+    o, lse = run_mxfp8(attn, w.causal, xq, xk, xv, w.scale)
+    assert torch.isfinite(lse).all()
+    rng = np.random.default_rng(3)
+    for b, h in ((0, 0), (w.B - 1, w.H - 1), (int(rng.integers(w.B)), int(rng.integers(w.H)))):
+        dq, dk, dv = (M.quantize_blocks(x[b, h])[2] for x in (xq, xk, xv))
+        rows = sample_rows(w.N, rng)
+        o_ref, lse_ref = attention_rows(dq[rows], dk, dv, rows, w.causal, w.scale)
+        check(o[b, h, rows], lse[b, h, rows], o_ref, lse_ref, f"{w.name} b={b} h={h}")
