@@ -39,14 +39,20 @@ METRIC = "attention fwd TFLOP/s on 1xGB300 and fraction of dense BF16/FP8 peak"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = I.NONCAUSAL_D128.name
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_SOURCES = ["online_softmax_fwd_gb300/csrc/fwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/ptx.cuh",
-                  "online_softmax_fwd_gb300/csrc/exp2_fma.cuh", "online_softmax_fwd_gb300/csrc/fwd_mxfp8.cuh",
-                  "online_softmax_fwd_gb300/csrc/mxfp8_common.cuh"]
+# sources each kernel is compiled from (a profile's traffic figure is only
+# reported while these are unchanged)
+KERNEL_SOURCES = {
+    "bf16": ["online_softmax_fwd_gb300/csrc/fwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/ptx.cuh",
+             "online_softmax_fwd_gb300/csrc/exp2_fma.cuh"],
+    "mxfp8": ["online_softmax_fwd_gb300/csrc/fwd_mxfp8.cuh", "online_softmax_fwd_gb300/csrc/mxfp8_common.cuh",
+              "online_softmax_fwd_gb300/csrc/fwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/ptx.cuh",
+              "online_softmax_fwd_gb300/csrc/exp2_fma.cuh"],
+}
 
 
-def kernel_sources_sha() -> str:
+def kernel_sources_sha(kind: str = "bf16") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -69,8 +75,11 @@ def profiled_traffic(workload: str) -> float | None:
         return None
     text = open(os.path.join(prof, sorted(names)[0])).read()
     sha = re.search(r"kernel_sources_sha:\s*([0-9a-f]+)", text)
+    kind = re.search(r"kernel_kind:\s*(\w+)", text)
     val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not sha or not val or sha.group(1) != kernel_sources_sha():
+    if not sha or not val or not kind or kind.group(1) not in KERNEL_SOURCES:
+        return None
+    if sha.group(1) != kernel_sources_sha(kind.group(1)):
         return None
     return float(val.group(1))
 

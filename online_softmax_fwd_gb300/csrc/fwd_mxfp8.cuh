@@ -364,21 +364,26 @@ __global__ void __launch_bounds__(384, 1)
       const float corr = fire ? (m == -INFINITY ? 0.f : ex2_mufu((m - m_new) * sl2)) : 1.0f;
       m = m_new;
       const float neg_ms = (m == -INFINITY) ? 0.f : -(m * sl2);
-      const float2 neg_ms_2 = make_float2(neg_ms, neg_ms);
       // E8M0 scale of each of this half's 32-key blocks of P: the block amax is
       // one exp of the block's score max
       const uint32_t sf_mine0 = e8m0_for_amax(ex2_mufu(__fmaf_rn(bmx[0], sl2, neg_ms)));
       const uint32_t sf_mine1 = e8m0_for_amax(ex2_mufu(__fmaf_rn(bmx[1], sl2, neg_ms)));
-      float2 acc = make_float2(0.f, 0.f);
+      // P / 2^e of a block is 2^(x - e): the block's scale goes into the exp's
+      // shift, so the conversion needs no multiply; the fp32 row sum takes the
+      // scaled block sums times 2^e.
+      float lsum = 0.f;
       uint32_t pk[16];
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
-        const float inv = e8m0_inverse(g ? sf_mine1 : sf_mine0);
+        const uint32_t sfb = g ? sf_mine1 : sf_mine0;
+        const float shift = neg_ms - static_cast<float>(static_cast<int>(sfb) - 127);
+        const float2 shift_2 = make_float2(shift, shift);
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
           const int c = 16 * g + i;
-          const float2 x0 = __ffma2_rn(s[c], sl2_2, neg_ms_2);
-          const float2 x1 = __ffma2_rn(s[c + 1], sl2_2, neg_ms_2);
+          const float2 x0 = __ffma2_rn(s[c], sl2_2, shift_2);
+          const float2 x1 = __ffma2_rn(s[c + 1], sl2_2, shift_2);
           float2 p0, p1;
           if (need_mask) {
             p0 = make_float2(ex2_mufu(x0.x), ex2_mufu(x0.y));
@@ -388,8 +393,9 @@ __global__ void __launch_bounds__(384, 1)
             p1 = make_float2(exp2_col<EMU, false>(2 * c + 2, x1.x), exp2_col<EMU, false>(2 * c + 3, x1.y));
           }
           acc = __fadd2_rn(acc, __fadd2_rn(p0, p1));
-          pk[8 * g + i / 2] = pack_e4m3x4(p0.x * inv, p0.y * inv, p1.x * inv, p1.y * inv);
+          pk[8 * g + i / 2] = pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
         }
+        lsum = __fmaf_rn(acc.x + acc.y, __uint_as_float(sfb << 23), lsum);  // * 2^(sfb - 127)
       }
       tmem_st16(tmem + lane_off + C::col_s(b) + 16 * half, pk);
       // the row's four P scales, one byte per key block, written by half 0
@@ -418,7 +424,7 @@ __global__ void __launch_bounds__(384, 1)
           tmem_st32(o_tm, ob);
         }
       }
-      l = l * corr + (acc.x + acc.y);
+      l = l * corr + lsum;
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_p(b));

@@ -44,11 +44,16 @@ def test_traffic_gated_by_kernel_fingerprint(tmp_path, monkeypatch):
     import bench
     prof = tmp_path / "profiles"
     prof.mkdir()
-    (prof / "fwd_bf16_w.md").write_text(f"kernel_sources_sha: {bench.kernel_sources_sha()}\n"
+    sha = bench.kernel_sources_sha("bf16")
+    assert sha != bench.kernel_sources_sha("mxfp8")
+    (prof / "fwd_bf16_w.md").write_text(f"kernel_kind: bf16\nkernel_sources_sha: {sha}\n"
                                         "dram_bytes_per_launch: 1.5e8\n")
+    monkeypatch.setattr(bench, "kernel_sources_sha", lambda kind="bf16": sha)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "kernel_sources_sha", lambda: "abc")
+    assert bench.profiled_traffic("w") == 1.5e8
+    monkeypatch.setattr(bench, "kernel_sources_sha", lambda kind="bf16": "abc")
     assert bench.profiled_traffic("w") is None  # taken on other kernel sources
+
 
 
 def test_reference_arm_json_line():
