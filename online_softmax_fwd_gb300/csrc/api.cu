@@ -192,7 +192,7 @@ attn_status_t attn_fwd_mxfp8_ex(const void* q8, const void* q_sf, const void* k8
   if (d != 128) return d > 0 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
   if (exp2_emu16 < 0 || exp2_emu16 > 16) return ATTN_ERR_INVALID_ARG;
   if (exp2_emu16 != 0 && exp2_emu16 != 2 && exp2_emu16 != 4) return ATTN_ERR_UNSUPPORTED;
-  if (N > kMaxN || static_cast<long long>(B) * H * ((N + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (N > kMaxN || static_cast<long long>(B) * H * ((N + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
   if (!q8 || !q_sf || !k8 || !k_sf || !v8 || !v_sf || !o || !lse) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(q_sf) || !aligned16(k_sf) ||
@@ -213,6 +213,7 @@ attn_status_t attn_fwd_mxfp8_ex(const void* q8, const void* q_sf, const void* k8
   a.status = status;
   a.n = N;
   a.n_tiles = (N + 127) / 128;
+  a.n_pairs = (N + 255) / 256;
   a.bh = static_cast<int>(bh);
   a.band = static_cast<int>(band_for(2LL * N * 128, bh));
   a.scale = scale;

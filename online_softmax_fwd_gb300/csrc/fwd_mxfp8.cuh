@@ -4,24 +4,24 @@
 // quant_mxfp8.cu); P is converted to MXFP8 online, per 32 keys ("PyTorch
 // FlashAttention-4 adds MXFP8 block-scaled forward and backward for Blackwell",
 // section "Softmax conversion and unroll-KV": the block amax of P comes from
-// one extra exp of the block's score max, the scale from its exponent and
-// mantissa bits). The online-softmax recurrence, tau rescale and epilogue are
-// those of the bf16 kernel.
+// one extra exp of the block's score max, the E8M0 scale from its exponent and
+// mantissa bits). The online-softmax recurrence, lagging-max rescale and
+// epilogue are those of the bf16 kernel (fwd_bf16.cuh).
 //
-// One CTA owns one 128-row Q tile of one (batch, head). The lower-precision
-// MMAs are twice as fast, so softmax is the bound; S is double-buffered in
-// TMEM so S(j+1) is computed while the softmax works on S(j):
-//   TMEM cols   0-127  S buffer 0 (P(j) as E4M3 over its first 32 columns)
-//             128-255  S buffer 1
-//             256-383  O (fp32)
-//             384..411 scale factors, 4 columns each: Q (A of S), K[2] (B of S),
-//                      P[2] (A of O), V[2] (B of O)
-//   warps 0-7  softmax: warp w owns TMEM lane quadrant w % 4 and the key
-//              columns [64 (w / 4), 64 (w / 4) + 64) of each block; the two
-//              halves of a row swap their 32-key block maxima through shared
-//              memory (published with per-thread sequence numbers)
-//   warp 8     TMA: Q tile + its scale atom; then K_0, K_1, V_0, K_2, V_1, ...
-//   warp 9     MMA (elected lane): S(j) into buffer j % 2; O += P(j) V_j.
+// Structure: the bf16 kernel's two 128-row Q tiles in ping-pong, one CTA per
+// (tile pair, head), warps 0-7 softmax (thread = row), warp 8 TMA, warp 9 MMA.
+// The 512 TMEM columns hold S0, S1, O0, O1 (128 each) as in the bf16 kernel,
+// so the scale factors go where the same page's section "TMEM allocation and
+// scale factor placement" puts them:
+//   * the two first S GEMMs read their Q and K scales from the O regions,
+//     which no MMA has written yet;
+//   * an O GEMM of tile t reads P's scales (written by the softmax) and V's
+//     scales from free columns of S_t: P as E4M3 takes columns 0-31, so
+//     32-35 (P) and 36-39 (V) are free once the softmax has read S_t;
+//   * S_t(j+1) reads its Q and K scales from columns 40-47 of the OTHER tile's
+//     S region, copied there only after that tile's softmax has loaded its
+//     scores (one extra MMA <- softmax barrier per tile, "s_loaded").
+// All scale regions are 4-column aligned.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -44,7 +44,8 @@ struct FwdMxArgs {
   float* lse;
   unsigned int* status;
   int n;
-  int n_tiles;           // ceil(N / 128): Q tiles and key blocks per head
+  int n_tiles;           // ceil(N / 128)
+  int n_pairs;           // ceil(N / 256)
   int bh;
   int band;
   float scale;
@@ -53,49 +54,29 @@ struct FwdMxArgs {
 };
 
 struct MxCfg {
-  static constexpr uint32_t kTileBytes = 128u * 128u;   // 128 x 128 E4M3
+  static constexpr uint32_t kTileBytes = 128u * 128u;  // 128 x 128 E4M3
   static constexpr uint32_t kAtomBytes = 512u;
   static constexpr int kSlots = 8;
-  static constexpr uint32_t kQOff = 0;
-  static constexpr uint32_t kRingOff = kTileBytes;                       // 1024-aligned payloads
-  static constexpr uint32_t kQAtomOff = kRingOff + kSlots * kTileBytes;
-  static constexpr uint32_t kAtomOff = kQAtomOff + kAtomBytes;           // one atom per ring slot
-  static constexpr uint32_t kXchOff = kAtomOff + kSlots * kAtomBytes;    // [2 parity][4 quad][2 half][32][2] floats
-  static constexpr uint32_t kXchBytes = 2 * 4 * 2 * 32 * 2 * 4;
-  static constexpr uint32_t kLOff = kXchOff + kXchBytes;                 // [2 half][128] floats
-  static constexpr uint32_t kSeqOff = kLOff + 2 * 128 * 4;              // [2 half][128] ints
-  static constexpr uint32_t kBarOff = kSeqOff + 2 * 128 * 4;
-  // q_full, full[kSlots], empty[kSlots], s_full[2], p_full[2], o_done, drain
-  static constexpr int kNumBars = 1 + 2 * kSlots + 6;
+  static constexpr uint32_t kRingOff = 2 * kTileBytes;                   // after Q0, Q1
+  static constexpr uint32_t kQAtomOff = kRingOff + kSlots * kTileBytes;  // Q0, Q1 atoms
+  static constexpr uint32_t kAtomOff = kQAtomOff + 2 * kAtomBytes;       // one atom per ring slot
+  static constexpr uint32_t kBarOff = kAtomOff + kSlots * kAtomBytes;
+  // q_full, full[kSlots], empty[kSlots], s_full[2], p_full[2], o_final[2], s_loaded[2], drain
+  static constexpr int kNumBars = 1 + 2 * kSlots + 9;
   static constexpr uint32_t kHolderOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kAbortOff = kHolderOff + 4;
   static constexpr uint32_t kSmemBytes = kAbortOff + 4 + 1024;
   static constexpr int kThreads = 384;
+  static constexpr uint32_t kRegsSoftmax = 208;
+  static constexpr uint32_t kRegsOther = 88;
+  static constexpr int kLaunchRegs = 168;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColO = 256;
-  static constexpr uint32_t kColSfQ = 384;
-  __host__ __device__ static constexpr uint32_t col_s(int b) { return b ? 128u : 0u; }
-  __host__ __device__ static constexpr uint32_t col_sf_k(int b) { return 388u + 4u * b; }
-  __host__ __device__ static constexpr uint32_t col_sf_p(int b) { return 396u + 4u * b; }
-  __host__ __device__ static constexpr uint32_t col_sf_v(int b) { return 404u + 4u * b; }
+  __host__ __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
+  __host__ __device__ static constexpr uint32_t col_o(int t) { return t ? 384u : 256u; }
+  // inside S_t: P (E4M3) 0-31, P scales 32-35, V scales 36-39; scales of the
+  // other tile's next S GEMM: Q 40-43, K 44-47
+  static constexpr uint32_t kPScale = 32, kVScale = 36, kQScale = 40, kKScale = 44;
 };
-
-// Bounded wait until *seq >= want (a partner thread's publication), giving up
-// on the CTA's abort flag or after kWaitLimitCycles.
-__device__ __forceinline__ bool wait_seq(const volatile int* seq, int want, volatile uint32_t* abort_flag,
-                                         unsigned int* status, uint32_t where) {
-  if (*seq >= want) return true;
-  const long long t0 = clock64();
-  while (*seq < want) {
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
-      *abort_flag = 1u;
-      record_status(status, kStatusTimeout, where);
-      return false;
-    }
-  }
-  return true;
-}
 
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
@@ -112,26 +93,29 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t bar_q = sbase + C::kBarOff;
   auto bar_full = [&](int i) { return bar_q + 8u * (1 + i); };
   auto bar_empty = [&](int i) { return bar_q + 8u * (1 + C::kSlots + i); };
-  auto bar_s = [&](int b) { return bar_q + 8u * (1 + 2 * C::kSlots + b); };
-  auto bar_p = [&](int b) { return bar_q + 8u * (3 + 2 * C::kSlots + b); };
-  const uint32_t bar_o = bar_q + 8u * (5 + 2 * C::kSlots);
-  const uint32_t bar_drain = bar_q + 8u * (6 + 2 * C::kSlots);
+  auto bar_s = [&](int t) { return bar_q + 8u * (1 + 2 * C::kSlots + t); };
+  auto bar_p = [&](int t) { return bar_q + 8u * (3 + 2 * C::kSlots + t); };
+  auto bar_o = [&](int t) { return bar_q + 8u * (5 + 2 * C::kSlots + t); };
+  auto bar_ld = [&](int t) { return bar_q + 8u * (7 + 2 * C::kSlots + t); };
+  const uint32_t bar_drain = bar_q + 8u * (9 + 2 * C::kSlots);
   uint32_t* holder = reinterpret_cast<uint32_t*>(smem + C::kHolderOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kAbortOff);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int bh, tile;
+  int bh, pair;
   {
-    const int per_band = args.band * args.n_tiles;
+    const int per_band = args.band * args.n_pairs;
     const int band_id = blockIdx.x / per_band;
     const int r = blockIdx.x - band_id * per_band;
     const int heads = min(args.band, args.bh - band_id * args.band);
-    tile = args.n_tiles - 1 - r / heads;  // heaviest causal tiles first
+    pair = args.n_pairs - 1 - r / heads;  // heaviest causal pairs first
     bh = band_id * args.band + r % heads;
   }
-  const int row0 = tile * 128;
-  const int nblk = CAUSAL ? min(tile + 1, args.n_tiles) : args.n_tiles;
+  const int row0 = pair * 256;
+  const int nkv = args.n_tiles;
+  const int n0 = CAUSAL ? min(2 * pair + 1, nkv) : nkv;
+  const int n1 = CAUSAL ? min(2 * pair + 2, nkv) : nkv;
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -139,16 +123,16 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar_full(i), 1);
       mbar_init(bar_empty(i), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_s(b), 1);
-      mbar_init(bar_p(b), 256);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_s(t), 1);
+      mbar_init(bar_p(t), 128);
+      mbar_init(bar_o(t), 1);
+      mbar_init(bar_ld(t), 128);
     }
-    mbar_init(bar_o, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0u;
     fence_barrier_init();
   }
-  if (warp < 8) reinterpret_cast<int*>(smem + C::kSeqOff)[threadIdx.x] = 0;
   if (warp == 9) {
     tmem_alloc(smem_addr(holder), C::kTmemCols);
     tmem_relinquish();
@@ -158,181 +142,208 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *holder;
 
-  // load order shared by the producer and the MMA warp: K_0, K_1, then V_j, K_{j+2}
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    const uint32_t leader = elect_one();
-    const uint64_t pol_q = policy_evict_first();
-    const uint64_t pol_kv = policy_evict_last();
-    const size_t head_atoms = static_cast<size_t>(bh) * args.n_tiles;
-    if (leader) {
-      mbar_arrive_expect_tx(bar_q, C::kTileBytes + C::kAtomBytes);
-      tma_load_3d_hint(sbase + C::kQOff, &tm_q, bar_q, 0, row0, bh, pol_q);
-      bulk_load(sbase + C::kQAtomOff, args.q_sf + (head_atoms + tile) * C::kAtomBytes, C::kAtomBytes, bar_q);
-    }
-    uint32_t slot = 0, ph = 0;
-    int seq = 0;
-    bool ok = true;
-    auto load = [&](bool is_v, int blk) {
-      ok = __all_sync(0xffffffffu, wait_bar(bar_empty(slot), ph ^ 1u, abort_flag, args.status, 1));
-      if (!ok) return;
+  if (warp >= 8) {
+    // ============================================================ producer warpgroup
+    regs_decrease<C::kRegsOther>();
+    if (warp == 8) {
+      // ---------------------------------------------------------- TMA: Q0, Q1 (+ atoms), then K_j, V_j
+      const uint32_t leader = elect_one();
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();
+      const size_t head_atoms = static_cast<size_t>(bh) * nkv;
       if (leader) {
-        mbar_arrive_expect_tx(bar_full(slot), C::kTileBytes + C::kAtomBytes);
-        tma_load_3d_hint(sbase + C::kRingOff + slot * C::kTileBytes, is_v ? &tm_v : &tm_k, bar_full(slot), 0,
-                         blk * 128, bh, pol_kv);
-        bulk_load(sbase + C::kAtomOff + slot * C::kAtomBytes,
-                  (is_v ? args.v_sf : args.k_sf) + (head_atoms + blk) * C::kAtomBytes, C::kAtomBytes, bar_full(slot));
-      }
-      ++seq;
-      if (++slot == static_cast<uint32_t>(C::kSlots)) {
-        slot = 0;
-        ph ^= 1u;
-      }
-    };
-    load(false, 0);
-    if (ok && nblk > 1) load(false, 1);
-    for (int j = 0; ok && j < nblk; ++j) {
-      load(true, j);
-      if (ok && j + 2 < nblk) load(false, j + 2);
-    }
-    if (!ok) {
-      drain_bar(bar_q, 0);
-      for (int s = seq - C::kSlots < 0 ? 0 : seq - C::kSlots; s < seq; ++s)
-        drain_bar(bar_full(s % C::kSlots), (s / C::kSlots) & 1);
-    }
-    __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    const uint32_t leader = elect_one();
-    auto commit = [&](uint32_t bar) {
-      if (leader) tc_commit(bar);
-    };
-    auto wait = [&](uint32_t bar, uint32_t parity, uint32_t where) {
-      return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, args.status, where));
-    };
-    // E4M3 tiles: one 128-byte swizzle row per matrix row; K-major Q and K
-    // advance 32 bytes per K=32 step, MN-major V advances 32 rows (4096 bytes)
-    const uint64_t q_desc = smem_desc_sw128(sbase + C::kQOff, 16, 1024);
-    const uint64_t ring_k = smem_desc_sw128(sbase + C::kRingOff, 16, 1024);
-    const uint64_t ring_v = smem_desc_sw128(sbase + C::kRingOff, C::kTileBytes, 1024);
-    constexpr uint64_t kSlotStep = C::kTileBytes >> 4;
-    uint32_t slot = 0, ph = 0;
-    auto next = [&]() {
-      if (++slot == static_cast<uint32_t>(C::kSlots)) {
-        slot = 0;
-        ph ^= 1u;
-      }
-    };
-    auto issue_s = [&](int b, uint32_t kslot) {
-      // K's scales into the buffer's B-scale columns, then 4 MMAs of K = 32
-      const uint32_t sfk = tmem + C::col_sf_k(b);
-      if (leader) {
-        sf_copy_to_tmem(sfk, sbase + C::kAtomOff + kslot * C::kAtomBytes);
+        mbar_arrive_expect_tx(bar_q, 2 * (C::kTileBytes + C::kAtomBytes));
 #pragma unroll
-        for (uint32_t kk = 0; kk < 4; ++kk)
-          mma_mxf8_ss(tmem + C::col_s(b), q_desc + 2 * kk, ring_k + kslot * kSlotStep + 2 * kk,
-                      idesc_mxf8(128, 128, false, kk, kk), kk > 0 ? 1u : 0u, tmem + C::kColSfQ, sfk);
+        for (int t = 0; t < 2; ++t) {
+          tma_load_3d_hint(sbase + t * C::kTileBytes, &tm_q, bar_q, 0, row0 + 128 * t, bh, pol_q);
+          // a tile past N reads zeros through the map; its scales may be any valid atom
+          const int qt = min(2 * pair + t, nkv - 1);
+          bulk_load(sbase + C::kQAtomOff + t * C::kAtomBytes, args.q_sf + (head_atoms + qt) * C::kAtomBytes,
+                    C::kAtomBytes, bar_q);
+        }
       }
-    };
-    auto issue_pv = [&](int b, uint32_t vslot, bool first) {
-      const uint32_t sfv = tmem + C::col_sf_v(b);
-      if (leader) {
-        sf_copy_to_tmem(sfv, sbase + C::kAtomOff + vslot * C::kAtomBytes);
+      int seq = 0;
+      uint32_t slot = 0, ph = 0;
+      bool ok = true;
+      for (int j = 0; ok && j < n1; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          ok = __all_sync(0xffffffffu, wait_bar(bar_empty(slot), ph ^ 1u, abort_flag, args.status, 1));
+          if (!ok) break;
+          if (leader) {
+            mbar_arrive_expect_tx(bar_full(slot), C::kTileBytes + C::kAtomBytes);
+            tma_load_3d_hint(sbase + C::kRingOff + slot * C::kTileBytes, kv ? &tm_v : &tm_k, bar_full(slot), 0,
+                             j * 128, bh, pol_kv);
+            bulk_load(sbase + C::kAtomOff + slot * C::kAtomBytes,
+                      (kv ? args.v_sf : args.k_sf) + (head_atoms + j) * C::kAtomBytes, C::kAtomBytes,
+                      bar_full(slot));
+          }
+          ++seq;
+          if (++slot == static_cast<uint32_t>(C::kSlots)) {
+            slot = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        drain_bar(bar_q, 0);
+        for (int s = seq - C::kSlots < 0 ? 0 : seq - C::kSlots; s < seq; ++s)
+          drain_bar(bar_full(s % C::kSlots), (s / C::kSlots) & 1);
+      }
+      __syncwarp();
+    } else if (warp == 9) {
+      // ---------------------------------------------------------- MMA issuer (elected lane)
+      const uint32_t leader = elect_one();
+      auto commit = [&](uint32_t bar) {
+        if (leader) tc_commit(bar);
+      };
+      auto wait = [&](uint32_t bar, uint32_t parity, uint32_t where) {
+        return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, args.status, where));
+      };
+      constexpr uint64_t kSlotStep = C::kTileBytes >> 4;
+      const uint64_t q_desc[2] = {smem_desc_sw128(sbase, 16, 1024), smem_desc_sw128(sbase + C::kTileBytes, 16, 1024)};
+      const uint64_t ring_k = smem_desc_sw128(sbase + C::kRingOff, 16, 1024);
+      const uint64_t ring_v = smem_desc_sw128(sbase + C::kRingOff, C::kTileBytes, 1024);
+      auto slot_atom = [&](uint32_t slot) { return sbase + C::kAtomOff + slot * C::kAtomBytes; };
+      // S_t = Q_t K^T from ring slot kslot; scales copied to TMEM columns sf_cols (Q) and sf_cols + 4 (K)
+      auto issue_s = [&](int t, uint32_t kslot, uint32_t sf_cols) {
+        if (leader) {
+          sf_copy_to_tmem(tmem + sf_cols, sbase + C::kQAtomOff + t * C::kAtomBytes);
+          sf_copy_to_tmem(tmem + sf_cols + 4, slot_atom(kslot));
 #pragma unroll
-        for (uint32_t kk = 0; kk < 4; ++kk)
-          mma_mxf8_ts(tmem + C::kColO, tmem + C::col_s(b) + 8 * kk, ring_v + vslot * kSlotStep + 256 * kk,
-                      idesc_mxf8(128, 128, true, kk, kk), (!first || kk > 0) ? 1u : 0u, tmem + C::col_sf_p(b),
-                      sfv);
-      }
-    };
-    bool ok = wait(bar_q, 0, 2);
-    if (ok) {
-      tc_fence_after();
-      if (leader) sf_copy_to_tmem(tmem + C::kColSfQ, sbase + C::kQAtomOff);
-    }
-    for (int b = 0; ok && b < 2 && b < nblk; ++b) {
-      ok = wait(bar_full(slot), ph, 3);
-      if (!ok) break;
-      tc_fence_after();
-      issue_s(b, slot);
-      commit(bar_s(b));
-      commit(bar_empty(slot));
-      next();
-    }
-    for (int j = 0; ok && j < nblk; ++j) {
-      const int b = j & 1;
-      if (!wait(bar_full(slot), ph, 4)) break;  // V_j
-      if (!wait(bar_p(b), (j >> 1) & 1, 5)) break;
-      tc_fence_after();
-      issue_pv(b, slot, j == 0);
-      commit(bar_empty(slot));
-      next();
-      if (j + 2 < nblk) {
-        if (!wait(bar_full(slot), ph, 6)) break;  // K_{j+2}
+          for (uint32_t kk = 0; kk < 4; ++kk)
+            mma_mxf8_ss(tmem + C::col_s(t), q_desc[t] + 2 * kk, ring_k + kslot * kSlotStep + 2 * kk,
+                        idesc_mxf8(128, 128, false, kk, kk), kk > 0 ? 1u : 0u, tmem + sf_cols, tmem + sf_cols + 4);
+        }
+      };
+      // O_t += P_t V from ring slot vslot; P_t and its scales in S_t, V's scales copied beside them
+      auto issue_pv = [&](int t, uint32_t vslot, bool first) {
+        if (leader) {
+          const uint32_t s_cols = tmem + C::col_s(t);
+          sf_copy_to_tmem(s_cols + C::kVScale, slot_atom(vslot));
+#pragma unroll
+          for (uint32_t kk = 0; kk < 4; ++kk)
+            mma_mxf8_ts(tmem + C::col_o(t), s_cols + 8 * kk, ring_v + vslot * kSlotStep + 256 * kk,
+                        idesc_mxf8(128, 128, true, kk, kk), (!first || kk > 0) ? 1u : 0u, s_cols + C::kPScale,
+                        s_cols + C::kVScale);
+        }
+      };
+      auto advance2 = [](uint32_t& slot, uint32_t& phase) {
+        slot += 2;
+        if (slot >= static_cast<uint32_t>(C::kSlots)) {
+          slot -= C::kSlots;
+          phase ^= 1u;
+        }
+      };
+      uint32_t ks = 0, kph = 0;  // K_j
+      uint32_t vs = 1, vph = 0;  // V_j
+      bool ok = wait(bar_q, 0, 2) && wait(bar_full(ks), kph, 3);
+      if (ok) {
         tc_fence_after();
-        issue_s(b, slot);
-        commit(bar_s(b));
-        commit(bar_empty(slot));
-        next();
-      } else if (j == nblk - 1) {
-        commit(bar_o);
+        // first S GEMMs: scales in the O regions, which no MMA has written yet
+        issue_s(0, ks, C::col_o(0));
+        commit(bar_s(0));
+        issue_s(1, ks, C::col_o(1));
+        commit(bar_s(1));
+        commit(bar_empty(ks));
       }
+      for (int j = 0; ok && j < n1; ++j) {
+        if (!wait(bar_full(vs), vph, 4)) break;
+        uint32_t ks_next = ks, kph_next = kph;
+        advance2(ks_next, kph_next);
+        bool k_next_ready = false;
+        if (j < n0) {
+          if (!wait(bar_p(0), j & 1, 5)) break;
+          tc_fence_after();
+          issue_pv(0, vs, j == 0);
+          if (j + 1 < n0) {
+            // S0(j+1)'s scales go into S1's columns 40-47: S1(j) must be loaded
+            if (!wait(bar_full(ks_next), kph_next, 6) || !wait(bar_ld(1), j & 1, 9)) break;
+            k_next_ready = true;
+            tc_fence_after();
+            issue_s(0, ks_next, C::col_s(1) + C::kQScale);
+            commit(bar_s(0));
+          } else {
+            commit(bar_o(0));
+          }
+        }
+        if (!wait(bar_p(1), j & 1, 7)) break;
+        tc_fence_after();
+        issue_pv(1, vs, j == 0);
+        commit(bar_empty(vs));
+        if (j + 1 < n1) {
+          if (!k_next_ready && !wait(bar_full(ks_next), kph_next, 8)) break;
+          // S1(j+1)'s scales go into S0's columns 40-47: if tile 0 has block
+          // j+1, its scores there must have been loaded first
+          if (j + 1 < n0 && !wait(bar_ld(0), (j + 1) & 1, 10)) break;
+          tc_fence_after();
+          issue_s(1, ks_next, C::col_s(0) + C::kQScale);
+          commit(bar_s(1));
+          commit(bar_empty(ks_next));
+        } else {
+          commit(bar_o(1));
+        }
+        ks = ks_next;
+        kph = kph_next;
+        advance2(vs, vph);
+      }
+      commit(bar_drain);
+      drain_bar(bar_drain, 0);
+      __syncwarp();
     }
-    commit(bar_drain);
-    drain_bar(bar_drain, 0);
-    __syncwarp();
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ softmax
+  } else {
+    // ============================================================ softmax warpgroups
+    regs_increase<C::kRegsSoftmax>();
+    const int t = warp >> 2;
     const int quad = warp & 3;
-    const int half = warp >> 2;
     const int r = quad * 32 + lane;
-    const int grow = row0 + r;
+    const int tile_row0 = row0 + 128 * t;
+    const int grow = tile_row0 + r;
+    const int nt = t ? n1 : n0;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    float* xch = reinterpret_cast<float*>(smem + C::kXchOff);  // [parity][quad][half][lane][2]
-    volatile float* lx = reinterpret_cast<volatile float*>(smem + C::kLOff);  // [half][128]
-    volatile int* seqs = reinterpret_cast<volatile int*>(smem + C::kSeqOff);  // [half][128]
-    volatile int* my_seq = seqs + half * 128 + r;
-    const volatile int* their_seq = seqs + (half ^ 1) * 128 + r;
+    const uint32_t s_tm = tmem + lane_off + C::col_s(t);
+    const uint32_t o_tm = tmem + lane_off + C::col_o(t);
     const float sl2 = args.scale_log2;
     const float2 sl2_2 = make_float2(sl2, sl2);
     float m = -INFINITY;
-    float l = 0.f;  // this half's share of the row sum
+    float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nblk; ++j) {
-      const int b = j & 1;
-      ok = __all_sync(0xffffffffu, wait_bar(bar_s(b), (j >> 1) & 1, abort_flag, args.status, 16 + half));
+    for (int j = 0; j < nt; ++j) {
+      ok = __all_sync(0xffffffffu, wait_bar(bar_s(t), j & 1, abort_flag, args.status, 16 + t));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t s_tm = tmem + lane_off + C::col_s(b) + 64 * half;
-      float2 s[32];
+      float2 s[64];
       {
-        uint32_t u[2][32];
-        tmem_ld32(s_tm, u[0]);
-        tmem_ld32(s_tm + 32, u[1]);
+        uint32_t u[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + 32 * c, u[c]);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < 4; ++c) {
           reg_fence32(u[c]);
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             s[16 * c + i] = make_float2(__uint_as_float(u[c][2 * i]), __uint_as_float(u[c][2 * i + 1]));
         }
       }
-      const int kv0 = j * 128 + 64 * half;
-      const bool need_mask = (j * 128 + 128 > args.n) || (CAUSAL && j == tile);
+      // the scores are in registers: the other tile's next S GEMM may now put
+      // its scale factors into this region
+      tc_fence_before();
+      mbar_arrive(bar_ld(t));
+      const int kv0 = j * 128;
+      const bool need_mask = (kv0 + 128 > args.n) || (CAUSAL && kv0 + 127 > tile_row0);
       if (need_mask) {
         int lim = args.n - 1 - kv0;
         if (CAUSAL) lim = min(lim, grow - kv0);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
+        for (int c = 0; c < 64; ++c) {
           if (2 * c > lim) s[c].x = -INFINITY;
           if (2 * c + 1 > lim) s[c].y = -INFINITY;
         }
       }
-      // maxima of this half's two 32-key blocks (two interleaved chains each)
-      float bmx[2];
+      // maxima of the four 32-key blocks (two interleaved chains each)
+      float bmx[4];
 #pragma unroll
-      for (int g = 0; g < 2; ++g) {
+      for (int g = 0; g < 4; ++g) {
         float a = fmaxf(s[16 * g].x, s[16 * g].y);
         float c = fmaxf(s[16 * g + 1].x, s[16 * g + 1].y);
 #pragma unroll
@@ -342,40 +353,23 @@ __global__ void __launch_bounds__(384, 1)
         }
         bmx[g] = fmaxf(a, c);
       }
-      // swap with the other half of the row (values double-buffered by block
-      // parity; a per-thread sequence number publishes them)
-      volatile float* mine = xch + ((((b * 4 + quad) * 2 + half) * 32 + lane) * 2);
-      const volatile float* theirs = xch + ((((b * 4 + quad) * 2 + (half ^ 1)) * 32 + lane) * 2);
-      mine[0] = bmx[0];
-      mine[1] = bmx[1];
-      __threadfence_block();
-      my_seq[0] = j + 1;
-      ok = __all_sync(0xffffffffu, wait_seq(their_seq, j + 1, abort_flag, args.status, 20));
-      if (!ok) break;
-      __threadfence_block();
-      // the four 32-key block maxima of the row, in key order
-      const float t0 = theirs[0], t1 = theirs[1];
-      const float blk0 = half ? t0 : bmx[0], blk1 = half ? t1 : bmx[1];
-      const float blk2 = half ? bmx[0] : t0, blk3 = half ? bmx[1] : t1;
-      const float bm = fmaxf(fmaxf(blk0, blk1), fmaxf(blk2, blk3));
+      const float bm = fmaxf(fmaxf(bmx[0], bmx[1]), fmaxf(bmx[2], bmx[3]));
       float m_new = fmaxf(m, bm);
       const bool fire = !((m_new - m) * sl2 <= args.tau);
       if (!fire) m_new = m;
       const float corr = fire ? (m == -INFINITY ? 0.f : ex2_mufu((m - m_new) * sl2)) : 1.0f;
       m = m_new;
       const float neg_ms = (m == -INFINITY) ? 0.f : -(m * sl2);
-      // E8M0 scale of each of this half's 32-key blocks of P: the block amax is
-      // one exp of the block's score max
-      const uint32_t sf_mine0 = e8m0_for_amax(ex2_mufu(__fmaf_rn(bmx[0], sl2, neg_ms)));
-      const uint32_t sf_mine1 = e8m0_for_amax(ex2_mufu(__fmaf_rn(bmx[1], sl2, neg_ms)));
-      // P / 2^e of a block is 2^(x - e): the block's scale goes into the exp's
-      // shift, so the conversion needs no multiply; the fp32 row sum takes the
-      // scaled block sums times 2^e.
+      // P per 32-key block: E8M0 scale from one exp of the block max; P / 2^e
+      // = 2^(x - e), so the scale rides in the exp's shift; the fp32 row sum
+      // takes each block's sum times 2^e
       float lsum = 0.f;
-      uint32_t pk[16];
+      uint32_t pk[32];
+      uint32_t sfw = 0;
 #pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        const uint32_t sfb = g ? sf_mine1 : sf_mine0;
+      for (int g = 0; g < 4; ++g) {
+        const uint32_t sfb = e8m0_for_amax(ex2_mufu(__fmaf_rn(bmx[g], sl2, neg_ms)));
+        sfw |= sfb << (8 * g);
         const float shift = neg_ms - static_cast<float>(static_cast<int>(sfb) - 127);
         const float2 shift_2 = make_float2(shift, shift);
         float2 acc = make_float2(0.f, 0.f);
@@ -397,22 +391,15 @@ __global__ void __launch_bounds__(384, 1)
         }
         lsum = __fmaf_rn(acc.x + acc.y, __uint_as_float(sfb << 23), lsum);  // * 2^(sfb - 127)
       }
-      tmem_st16(tmem + lane_off + C::col_s(b) + 16 * half, pk);
-      // the row's four P scales, one byte per key block, written by half 0
-      // (half 1's two are recomputed from the swapped maxima)
-      if (half == 0) {
-        const uint32_t sf2 = e8m0_for_amax(ex2_mufu(__fmaf_rn(blk2, sl2, neg_ms)));
-        const uint32_t sf3 = e8m0_for_amax(ex2_mufu(__fmaf_rn(blk3, sl2, neg_ms)));
-        tmem_st1(tmem + lane_off + C::col_sf_p(b) + quad, sf_mine0 | (sf_mine1 << 8) | (sf2 << 16) | (sf3 << 24));
-      }
-      // correction of this half's O columns once the scores are dead
+      tmem_st32(s_tm, pk);                      // P, 4 keys per column
+      tmem_st1(s_tm + C::kPScale + quad, sfw);  // row r's scales at column r / 32
+      // correction of O once the scores are dead; lands before P is handed over
       if (j > 0 && __any_sync(0xffffffffu, fire)) {
         const float2 corr_2 = make_float2(corr, corr);
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) {
+        for (int c = 0; c < 128; c += 32) {
           uint32_t ob[32];
-          const uint32_t o_tm = tmem + lane_off + C::kColO + 64 * half + c;
-          tmem_ld32(o_tm, ob);
+          tmem_ld32(o_tm + c, ob);
           tmem_ld_wait();
           reg_fence32(ob);
 #pragma unroll
@@ -421,34 +408,25 @@ __global__ void __launch_bounds__(384, 1)
             ob[i] = __float_as_uint(o2.x);
             ob[i + 1] = __float_as_uint(o2.y);
           }
-          tmem_st32(o_tm, ob);
+          tmem_st32(o_tm + c, ob);
         }
       }
       l = l * corr + lsum;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar_p(b));
+      mbar_arrive(bar_p(t));
     }
-    if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar_o, 0, abort_flag, args.status, 18));
-    // the row's sum is the two halves' sums
-    if (ok) {
-      lx[half * 128 + r] = l;
-      __threadfence_block();
-      my_seq[0] = nblk + 1;
-      ok = __all_sync(0xffffffffu, wait_seq(their_seq, nblk + 1, abort_flag, args.status, 21));
-      __threadfence_block();
-    }
+    if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar_o(t), 0, abort_flag, args.status, 18 + t));
     if (ok) {
       tc_fence_after();
-      const float l_row = lx[r] + lx[128 + r];
-      const float inv_l = 1.0f / l_row;
+      const float inv_l = 1.0f / l;
       const bool valid = grow < args.n;
-      __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * args.n + (valid ? grow : 0)) * 128 + 64 * half;
+      __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * args.n + (valid ? grow : 0)) * 128;
       const float2 inv_l_2 = make_float2(inv_l, inv_l);
 #pragma unroll
-      for (int c = 0; c < 64; c += 32) {
+      for (int c = 0; c < 128; c += 32) {
         uint32_t ob[32];
-        tmem_ld32(tmem + lane_off + C::kColO + 64 * half + c, ob);
+        tmem_ld32(o_tm + c, ob);
         tmem_ld_wait();
         reg_fence32(ob);
         uint32_t w[16];
@@ -463,8 +441,7 @@ __global__ void __launch_bounds__(384, 1)
           for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
         }
       }
-      if (valid && half == 0)
-        args.lse[static_cast<size_t>(bh) * args.n + grow] = (m * sl2 + lg2_mufu(l_row)) * 0.69314718055994531f;
+      if (valid) args.lse[static_cast<size_t>(bh) * args.n + grow] = (m * sl2 + lg2_mufu(l)) * 0.69314718055994531f;
     }
     tc_fence_before();
   }
@@ -482,7 +459,12 @@ cudaError_t launch_fwd_mxfp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, c
   auto kernel = attn_fwd_mxfp8_kernel<CAUSAL, EMU>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MxCfg::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const long long ctas = static_cast<long long>(args.bh) * args.n_tiles;
+  // the setmaxnreg split must fit the registers the CTA is launched with
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs < MxCfg::kLaunchRegs) return cudaErrorInvalidConfiguration;
+  const long long ctas = static_cast<long long>(args.bh) * args.n_pairs;
   kernel<<<static_cast<unsigned>(ctas), MxCfg::kThreads, MxCfg::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, args);
   return cudaGetLastError();
 }
