@@ -28,7 +28,9 @@
 //   is quiescent until this warp hands P_t(j) over); p = 2^(s log2e * S -
 //   s log2e * m) with one FFMA and then the MUFU ex2 or, for a compile-time
 //   share of the columns, the software exp2 on the FMA pipe; l += sum p in fp32;
-//   P rounded to bf16 and stored over the S columns it replaces.
+//   P rounded to bf16 and stored over the S columns it replaces, handed over in
+//   two halves of 64 keys so the O MMA of the first half overlaps the softmax
+//   of the second.
 // After the last block: O / l rounded to bf16, and LSE = s m + ln l.
 #pragma once
 
@@ -67,8 +69,8 @@ struct FwdCfg {
   static constexpr int kSlots = D == 128 ? 5 : 8;           // K/V ring depth
   static constexpr uint32_t kRingOff = 2 * kTileBytes;      // after Q0, Q1
   static constexpr uint32_t kBarOff = kRingOff + kSlots * kTileBytes;
-  // q_full, full[kSlots], empty[kSlots], s_full[2], p_full[2], o_final[2], drain
-  static constexpr int kNumBars = 1 + 2 * kSlots + 7;
+  // q_full, full[kSlots], empty[kSlots], s_full[2], p_full[2][2 halves], o_final[2], drain
+  static constexpr int kNumBars = 1 + 2 * kSlots + 9;
   static constexpr uint32_t kHolderOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kAbortOff = kHolderOff + 4;
   static constexpr uint32_t kSmemBytes = kAbortOff + 4 + 1024;  // + slack for 1024-byte alignment
@@ -126,27 +128,35 @@ __device__ __forceinline__ float exp2_col(int c, float x) {
   return ex2_mufu(x);
 }
 
-// p = 2^(S*sl2 + neg_ms) for the 128 scores of a row (as 64 pairs), rounded
-// to bf16 pairs and stored to TMEM at p_tm; returns the fp32 sum of the
-// unrounded p. The scale-and-shift and the running sums use the packed fp32
-// pair instructions (one issue for two lanes of work).
-template <int EMU, bool MUFU_ONLY>
-__device__ __forceinline__ float softmax_p_store(const float2 (&s)[64], float2 sl2_2, float2 neg_ms_2,
-                                                 uint32_t p_tm) {
-  float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+// p = 2^(S*sl2 + neg_ms) for one half (64 keys, pairs [32 H, 32 H + 32)) of a
+// row's 128 scores, rounded to bf16 pairs and stored to TMEM at p_tm (32 bf16
+// pairs from column 32 H); returns the fp32 sum of the unrounded p. The
+// scale-and-shift and the running sums use the packed fp32 pair instructions
+// (one issue for two lanes of work).
+template <int EMU, bool MUFU_ONLY, int H>
+__device__ __forceinline__ float softmax_p_half(const float2 (&s)[64], float2 sl2_2, float2 neg_ms_2, uint32_t p_tm) {
+  // eight independent accumulators: the packed fp32 add has a long latency,
+  // so a short dependency chain per accumulator keeps it off the critical path
+  float2 acc[8];
 #pragma unroll
-  for (int chunk = 0; chunk < 4; ++chunk) {
+  for (int a = 0; a < 8; ++a) acc[a] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int chunk = 2 * H; chunk < 2 * H + 2; ++chunk) {
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int c = chunk * 16 + i;  // pair index
       const float2 x = __ffma2_rn(s[c], sl2_2, neg_ms_2);
       const float2 p = make_float2(exp2_col<EMU, MUFU_ONLY>(2 * c, x.x), exp2_col<EMU, MUFU_ONLY>(2 * c + 1, x.y));
-      acc[i & 1] = __fadd2_rn(acc[i & 1], p);
+      acc[i & 7] = __fadd2_rn(acc[i & 7], p);
       pk[i] = pack_bf16x2(p.x, p.y);
     }
     tmem_st16(p_tm + chunk * 16, pk);
   }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) acc[a] = __fadd2_rn(acc[a], acc[a + 4]);
+  acc[0] = __fadd2_rn(acc[0], acc[2]);
+  acc[1] = __fadd2_rn(acc[1], acc[3]);
   const float2 t = __fadd2_rn(acc[0], acc[1]);
   return t.x + t.y;
 }
@@ -164,9 +174,11 @@ __global__ void __launch_bounds__(384, 1)
   auto bar_full = [&](int i) { return bar_q + 8u * (1 + i); };
   auto bar_empty = [&](int i) { return bar_q + 8u * (1 + C::kSlots + i); };
   auto bar_s = [&](int t) { return bar_q + 8u * (1 + 2 * C::kSlots + t); };
-  auto bar_p = [&](int t) { return bar_q + 8u * (3 + 2 * C::kSlots + t); };
-  auto bar_o = [&](int t) { return bar_q + 8u * (5 + 2 * C::kSlots + t); };
-  const uint32_t bar_drain = bar_q + 8u * (7 + 2 * C::kSlots);
+  // P of a tile is handed over in two halves of 64 keys, so the O MMA of the
+  // first half overlaps the softmax of the second
+  auto bar_p = [&](int t, int h) { return bar_q + 8u * (3 + 2 * C::kSlots + 2 * t + h); };
+  auto bar_o = [&](int t) { return bar_q + 8u * (7 + 2 * C::kSlots + t); };
+  const uint32_t bar_drain = bar_q + 8u * (9 + 2 * C::kSlots);
   uint32_t* holder = reinterpret_cast<uint32_t*>(smem + C::kHolderOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kAbortOff);
 
@@ -197,7 +209,8 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_s(t), 1);
-      mbar_init(bar_p(t), 128);
+      mbar_init(bar_p(t, 0), 128);
+      mbar_init(bar_p(t, 1), 128);
       mbar_init(bar_o(t), 1);
     }
     mbar_init(bar_drain, 1);
@@ -301,13 +314,15 @@ __global__ void __launch_bounds__(384, 1)
             mma_ss(d, a + kmajor_step(kk), b + kmajor_step(kk), kIdS, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, uint32_t slot, bool first) {
+      // O_t += P_t V for keys [64 h, 64 h + 64) of the block
+      auto issue_pv = [&](int t, uint32_t slot, int h, bool first) {
         const uint64_t b = v_ring + slot * kSlotStep;
         const uint32_t d = tmem + C::col_o(t);
         const uint32_t a = tmem + C::col_s(t);
         if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ts(d, a + kk * 8, b + kk * 128, kIdO, (!first || kk > 0) ? 1u : 0u);
+          for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+            mma_ts(d, a + kk * 8, b + kk * 128, kIdO, (!first || kk > 0) ? 1u : 0u);
         }
       };
       // ring positions: K_j is the (2j)-th load, V_j the (2j+1)-th
@@ -335,9 +350,12 @@ __global__ void __launch_bounds__(384, 1)
         advance2(ks_next, kph_next);
         bool k_next_ready = false;
         if (j < n0) {
-          if (!wait(bar_p(0), j & 1, 5)) break;
+          if (!wait(bar_p(0, 0), j & 1, 5)) break;
           tc_fence_after();
-          issue_pv(0, vs, j == 0);
+          issue_pv(0, vs, 0, j == 0);
+          if (!wait(bar_p(0, 1), j & 1, 11)) break;
+          tc_fence_after();
+          issue_pv(0, vs, 1, false);
           if (j + 1 < n0) {
             if (!wait(bar_full(ks_next), kph_next, 6)) break;
             k_next_ready = true;
@@ -348,9 +366,12 @@ __global__ void __launch_bounds__(384, 1)
             commit(bar_o(0));
           }
         }
-        if (!wait(bar_p(1), j & 1, 7)) break;
+        if (!wait(bar_p(1, 0), j & 1, 7)) break;
         tc_fence_after();
-        issue_pv(1, vs, j == 0);
+        issue_pv(1, vs, 0, j == 0);
+        if (!wait(bar_p(1, 1), j & 1, 12)) break;
+        tc_fence_after();
+        issue_pv(1, vs, 1, false);
         commit(bar_empty(vs));
         if (j + 1 < n1) {
           if (!k_next_ready) {
@@ -441,10 +462,10 @@ __global__ void __launch_bounds__(384, 1)
       m = m_new;
       const float neg_ms = (m == -INFINITY) ? 0.f : -(m * sl2);
       const float2 neg_ms_2 = make_float2(neg_ms, neg_ms);
-      const float psum = need_mask ? softmax_p_store<EMU, true>(s, sl2_2, neg_ms_2, s_tm)
-                                   : softmax_p_store<EMU, false>(s, sl2_2, neg_ms_2, s_tm);
-      // correction of O after the scores are dead (lower register pressure);
-      // it still lands before P_t(j) is handed to the MMA thread below
+      // first 64 keys of P
+      float psum = need_mask ? softmax_p_half<EMU, true, 0>(s, sl2_2, neg_ms_2, s_tm)
+                             : softmax_p_half<EMU, false, 0>(s, sl2_2, neg_ms_2, s_tm);
+      // correction of O (before any O MMA of this block)
       if (j > 0 && __any_sync(0xffffffffu, fire)) {
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
@@ -462,10 +483,16 @@ __global__ void __launch_bounds__(384, 1)
           tmem_st32(o_tm + c, ob);
         }
       }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_p(t, 0));
+      // last 64 keys, while the MMA works on the first
+      psum += need_mask ? softmax_p_half<EMU, true, 1>(s, sl2_2, neg_ms_2, s_tm)
+                        : softmax_p_half<EMU, false, 1>(s, sl2_2, neg_ms_2, s_tm);
       l = l * corr + psum;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar_p(t));
+      mbar_arrive(bar_p(t, 1));
     }
     if (ok) {
       ok = wait_bar(bar_o(t), 0, abort_flag, args.status, 18 + t);

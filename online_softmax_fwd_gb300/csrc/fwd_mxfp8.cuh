@@ -372,7 +372,8 @@ __global__ void __launch_bounds__(384, 1)
         sfw |= sfb << (8 * g);
         const float shift = neg_ms - static_cast<float>(static_cast<int>(sfb) - 127);
         const float2 shift_2 = make_float2(shift, shift);
-        float2 acc = make_float2(0.f, 0.f);
+        // four accumulators: short chains for the long-latency packed add
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
           const int c = 16 * g + i;
@@ -386,10 +387,12 @@ __global__ void __launch_bounds__(384, 1)
             p0 = make_float2(exp2_col<EMU, false>(2 * c, x0.x), exp2_col<EMU, false>(2 * c + 1, x0.y));
             p1 = make_float2(exp2_col<EMU, false>(2 * c + 2, x1.x), exp2_col<EMU, false>(2 * c + 3, x1.y));
           }
-          acc = __fadd2_rn(acc, __fadd2_rn(p0, p1));
+          acc[(i >> 1) & 1] = __fadd2_rn(acc[(i >> 1) & 1], p0);
+          acc[2 + ((i >> 1) & 1)] = __fadd2_rn(acc[2 + ((i >> 1) & 1)], p1);
           pk[8 * g + i / 2] = pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
         }
-        lsum = __fmaf_rn(acc.x + acc.y, __uint_as_float(sfb << 23), lsum);  // * 2^(sfb - 127)
+        acc[0] = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        lsum = __fmaf_rn(acc[0].x + acc[0].y, __uint_as_float(sfb << 23), lsum);  // * 2^(sfb - 127)
       }
       tmem_st32(s_tm, pk);                      // P, 4 keys per column
       tmem_st1(s_tm + C::kPScale + quad, sfw);  // row r's scales at column r / 32
