@@ -93,6 +93,30 @@ attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, 
                           int N, int d, int causal, float scale, float tau, int exp2_emu16, void* stream);
 
 /*
+ * attn_fwd_host -- attn_fwd with Q, K, V, O and LSE in HOST memory.
+ *
+ *   q, k, v, o, lse   host pointers, same layouts as attn_fwd. Page-locked
+ *                     (pinned) memory lets the copies run asynchronously and
+ *                     overlap; pageable memory works but copies synchronously.
+ *   workspace         device memory of at least
+ *                     attn_fwd_host_workspace_bytes(B, H, N, d) bytes,
+ *                     256-byte aligned, owned by the caller; not read or
+ *                     written after the call's work on `stream` completes.
+ * The B*H heads are cut into about eight chunks; each chunk is copied in,
+ * computed (attn_fwd) and copied out on three library-owned streams of the
+ * current device (created on first use and kept), with two chunk buffers in
+ * the workspace, so copies and kernels overlap. The work is ordered after what
+ * is already queued on `stream`, and `stream` waits for its completion: the
+ * host buffers may be read (O, LSE) or reused once `stream` has synchronised.
+ * Results are identical to attn_fwd on the same data (heads are independent).
+ * Errors as attn_fwd; ATTN_ERR_INVALID_ARG for a null or too small workspace.
+ */
+size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d);
+attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                            int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
  * MXFP8 variant ("PyTorch FlashAttention-4 adds MXFP8 block-scaled forward and
  * backward for Blackwell"): Q, K, V in E4M3 with one E8M0 (power-of-two) scale
  * per 32 x 32 block -- Q and K blocked along d for S = Q K^T, V along the

@@ -51,6 +51,10 @@ _SIGNATURES = {
     "attn_fwd_mxfp8_ex": ([ctypes.c_void_p] * 8 + [ctypes.c_int] * 5
                           + [ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
     "attn_exp2_emulated": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p], ctypes.c_int),
+    "attn_fwd_host_workspace_bytes": ([ctypes.c_int] * 4, ctypes.c_size_t),
+    # q, k, v, o, lse (host), B, H, N, d, causal, scale, workspace, workspace_bytes, stream
+    "attn_fwd_host": ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
+                      + [ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
     "attn_get_device_status": ([ctypes.c_void_p], ctypes.c_int),
     "attn_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "attn_version": ([], ctypes.c_int),
@@ -149,32 +153,35 @@ def attn_fwd_from_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal
                        scale: float | None = None, device: int | torch.device = 0,
                        o_host: torch.Tensor | None = None, lse_host: torch.Tensor | None = None,
                        workspace: dict | None = None, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
-    """End-to-end call with host tensors: copy Q, K, V (pinned CPU bf16) to the
-    device, run attn_fwd, copy O and LSE back into host tensors. ``workspace``
-    (a dict) keeps the device buffers between calls of the same shape."""
+    """End-to-end call with host tensors through attn_fwd_host: Q, K, V (CPU
+    bf16 [B,H,N,d], pinned for overlap) in, O and LSE back into host tensors;
+    the library overlaps the copies with the kernels. ``workspace`` (a dict)
+    keeps the device workspace between calls of the same shape. Returns after
+    the results are in host memory."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous() or t.shape != q.shape:
+            raise ValueError(f"{name} must be a contiguous CPU bfloat16 tensor shaped like q")
     B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
     dev = torch.device("cuda", device) if isinstance(device, int) else device
-    ws = workspace if workspace is not None else {}
-    key = (B, H, N, d, str(dev))
-    if ws.get("key") != key:
-        ws.clear()
-        ws["key"] = key
-        ws["q"] = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
-        ws["k"] = torch.empty_like(ws["q"])
-        ws["v"] = torch.empty_like(ws["q"])
-        ws["o"] = torch.empty_like(ws["q"])
-        ws["lse"] = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    ws["q"].copy_(q, non_blocking=True)
-    ws["k"].copy_(k, non_blocking=True)
-    ws["v"].copy_(v, non_blocking=True)
-    attn_fwd(ws["q"], ws["k"], ws["v"], causal, scale, o=ws["o"], lse=ws["lse"], stream=stream)
     if o_host is None:
         o_host = torch.empty((B, H, N, d), dtype=torch.bfloat16, pin_memory=True)
     if lse_host is None:
         lse_host = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
-    o_host.copy_(ws["o"], non_blocking=True)
-    lse_host.copy_(ws["lse"], non_blocking=True)
-    torch.cuda.current_stream(dev).synchronize()
+    need = lib().attn_fwd_host_workspace_bytes(B, H, N, d)
+    ws = workspace if workspace is not None else {}
+    if ws.get("key") != (need, str(dev)):
+        ws.clear()
+        ws["key"] = (need, str(dev))
+        ws["buf"] = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        h = _stream_handle(stream)
+        st = lib().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o_host), _ptr(lse_host), B, H, N, d,
+                                 int(bool(causal)), float(scale), _ptr(ws["buf"]), need, h)
+        _check(st, "attn_fwd_host")
+        torch.cuda.current_stream(dev).synchronize() if stream is None else torch.cuda.Stream(
+            stream_ptr=h, device=dev).synchronize()
     return o_host, lse_host
 
 

@@ -98,3 +98,18 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no CPU or PyTorch fallback"):
         b.lib()
+
+
+def test_host_entry_rejects_bad_arguments(lib):
+    H = A  # fake host addresses, never dereferenced on these paths
+    args = lambda ws, nbytes, d=64, causal=0, scale=0.125, B=1: (H, H, H, H, H, B, 2, 256, d, causal, scale, ws, nbytes,
+                                                                 None)
+    need = lib.attn_fwd_host_workspace_bytes(1, 2, 256, 64)
+    assert need > 0 and lib.attn_fwd_host_workspace_bytes(1, 2, 256, 96) == 0
+    assert lib.attn_fwd_host(*args(0, need)) == 1             # no workspace
+    assert lib.attn_fwd_host(*args(A * 7, need - 1)) == 1     # too small
+    assert lib.attn_fwd_host(*args(A * 7 + 16, need)) == 3    # not 256-byte aligned
+    assert lib.attn_fwd_host(*args(A * 7, need, d=96)) == 2
+    assert lib.attn_fwd_host(*args(A * 7, need, causal=3)) == 1
+    assert lib.attn_fwd_host(*args(A * 7, need, scale=-1.0)) == 1
+    assert lib.attn_fwd_host(*args(A * 7, need, B=0)) == 0    # nothing to do
