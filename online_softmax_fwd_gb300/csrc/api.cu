@@ -7,7 +7,9 @@
 
 #include <atomic>
 #include <cmath>
+#include <algorithm>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "attn.h"
@@ -15,6 +17,7 @@
 #include "fwd_bf16.cuh"
 #include "fwd_dispatch.h"
 #include "fwd_mxfp8.cuh"
+#include "schedule.h"
 
 namespace {
 
@@ -83,6 +86,18 @@ bool make_map_e4m3(CUtensorMap* m, const void* base, int n, long long bh) {
   return r == CUDA_SUCCESS;
 }
 
+// SMs of the current device, queried once per device (the persistent grid size)
+int sm_count() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+  cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 long long band_for(long long kv_head_bytes, long long bh) {
@@ -149,14 +164,26 @@ attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, 
   a.n_pairs = n_pairs;
   a.bh = static_cast<int>(bh);
   a.band = static_cast<int>(band_for(4LL * N * d, bh));
+  const int sms = sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  // persistent grid: one CTA per SM, items from a list schedule when they fit
+  // in one, else in serpentine rounds
+  const long long items = bh * n_pairs;
+  attn::WorkList wl;
+  int ctas = static_cast<int>(std::min<long long>(items, std::min(sms, attn::kListMaxCtas)));
+  a.use_list = attn::work_list_for(a.bh, n_pairs, a.n_kv_blocks, a.band, causal != 0, ctas, &wl) ? 1 : 0;
+  if (!a.use_list) {
+    std::memset(&wl, 0, sizeof(wl));
+    ctas = static_cast<int>(std::min<long long>(items, sms));
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (d == 64)
-    e = causal ? attn::launch_fwd_bf16_d64_c1(exp2_emu16, mq, mk, mv, a, static_cast<int>(bh), n_pairs, s)
-               : attn::launch_fwd_bf16_d64_c0(exp2_emu16, mq, mk, mv, a, static_cast<int>(bh), n_pairs, s);
+    e = causal ? attn::launch_fwd_bf16_d64_c1(exp2_emu16, mq, mk, mv, a, wl, ctas, s)
+               : attn::launch_fwd_bf16_d64_c0(exp2_emu16, mq, mk, mv, a, wl, ctas, s);
   else
-    e = causal ? attn::launch_fwd_bf16_d128_c1(exp2_emu16, mq, mk, mv, a, static_cast<int>(bh), n_pairs, s)
-               : attn::launch_fwd_bf16_d128_c0(exp2_emu16, mq, mk, mv, a, static_cast<int>(bh), n_pairs, s);
+    e = causal ? attn::launch_fwd_bf16_d128_c1(exp2_emu16, mq, mk, mv, a, wl, ctas, s)
+               : attn::launch_fwd_bf16_d128_c0(exp2_emu16, mq, mk, mv, a, wl, ctas, s);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

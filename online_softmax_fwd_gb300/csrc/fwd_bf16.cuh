@@ -41,6 +41,7 @@
 
 #include "exp2_fma.cuh"
 #include "ptx.cuh"
+#include "schedule.h"
 
 namespace attn {
 
@@ -55,6 +56,7 @@ struct FwdArgs {
   int n_pairs;           // ceil(N / 256): Q-tile pairs per head
   int bh;                // B * H
   int band;              // heads per scheduling band (their K/V stay in L2 together)
+  int use_list;          // 1: items from the work list; 0: serpentine rounds
   float scale;           // s
   float scale_log2;      // s * log2(e)
   float tau;             // rescale threshold, log2 units
@@ -69,8 +71,8 @@ struct FwdCfg {
   static constexpr int kSlots = D == 128 ? 5 : 8;           // K/V ring depth
   static constexpr uint32_t kRingOff = 2 * kTileBytes;      // after Q0, Q1
   static constexpr uint32_t kBarOff = kRingOff + kSlots * kTileBytes;
-  // q_full, full[kSlots], empty[kSlots], s_full[2], p_full[2][2 halves], o_final[2], drain
-  static constexpr int kNumBars = 1 + 2 * kSlots + 9;
+  // q_full, full[kSlots], empty[kSlots], s_full[2], p_full[2][2 halves], o_final[2], drain, q_empty
+  static constexpr int kNumBars = 1 + 2 * kSlots + 10;
   static constexpr uint32_t kHolderOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kAbortOff = kHolderOff + 4;
   static constexpr uint32_t kSmemBytes = kAbortOff + 4 + 1024;  // + slack for 1024-byte alignment
@@ -164,7 +166,8 @@ __device__ __forceinline__ float softmax_p_half(const float2 (&s)[64], float2 sl
 template <int D, bool CAUSAL, int EMU>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
+                         const __grid_constant__ CUtensorMap tm_v, const FwdArgs args,
+                         const __grid_constant__ WorkList wl) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzle atoms need 1024-byte aligned tiles (shared-window address)
@@ -179,27 +182,29 @@ __global__ void __launch_bounds__(384, 1)
   auto bar_p = [&](int t, int h) { return bar_q + 8u * (3 + 2 * C::kSlots + 2 * t + h); };
   auto bar_o = [&](int t) { return bar_q + 8u * (7 + 2 * C::kSlots + t); };
   const uint32_t bar_drain = bar_q + 8u * (9 + 2 * C::kSlots);
+  const uint32_t bar_qe = bar_q + 8u * (10 + 2 * C::kSlots);  // Q buffers free again
   uint32_t* holder = reinterpret_cast<uint32_t*>(smem + C::kHolderOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kAbortOff);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // 1-D grid in bands of `band` heads: inside a band the Q-tile pairs of its
-  // heads come heaviest first (causal), so co-resident CTAs share the band's
-  // K/V in L2 and the long causal tiles start early.
-  int bh, pair;
-  {
-    const int per_band = args.band * args.n_pairs;
-    const int band_id = blockIdx.x / per_band;
-    const int r = blockIdx.x - band_id * per_band;
-    const int heads = min(args.band, args.bh - band_id * args.band);
-    pair = args.n_pairs - 1 - r / heads;
-    bh = band_id * args.band + r % heads;
-  }
-  const int row0 = pair * 256;
+  // Persistent: CTA c runs the items of its work list in order; without a
+  // list, in round k it takes item k G + c (k even) or k G + G - 1 - c (k odd),
+  // G = gridDim.x, a serpentine that evens out the causal items' unequal work.
+  const int total_items = args.bh * args.n_pairs;
+  auto item_of = [&](int k) {
+    if (args.use_list) {
+      const int idx = wl.first[blockIdx.x] + k;
+      return idx < wl.first[blockIdx.x + 1] ? static_cast<int>(wl.item[idx]) : total_items;
+    }
+    const long long g = gridDim.x;
+    const long long o = k * g + ((k & 1) ? g - 1 - blockIdx.x : blockIdx.x);
+    return o < total_items ? static_cast<int>(o) : total_items;
+  };
+  auto coords = [&](int it, int& bh, int& pair) { item_coords(it, args.bh, args.n_pairs, args.band, bh, pair); };
   const int nkv = args.n_kv_blocks;
-  const int n0 = CAUSAL ? min(2 * pair + 1, nkv) : nkv;  // key blocks of tile 0
-  const int n1 = CAUSAL ? min(2 * pair + 2, nkv) : nkv;  // key blocks of tile 1 (>= n0)
+  // key blocks of tile 0 and tile 1 (n1 >= n0) of a pair
+  auto blocks_of = [&](int pair, int t) { return CAUSAL ? min(2 * pair + 1 + t, nkv) : nkv; };
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -214,6 +219,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar_o(t), 1);
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_qe, 1);
     *abort_flag = 0u;
     fence_barrier_init();
   }
@@ -236,40 +242,52 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t leader = elect_one();
     const uint64_t pol_q = policy_evict_first();
     const uint64_t pol_kv = policy_evict_last();
-    if (leader) {
-      mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d_hint(sbase + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, bar_q, b * 64, row0 + 128 * t, bh,
-                           pol_q);
-    }
     int seq = 0;
     uint32_t slot = 0, ph = 0;
     bool ok = true;
-    for (int j = 0; ok && j < n1; ++j) {
-      for (int kv = 0; kv < 2; ++kv) {
-        ok = __all_sync(0xffffffffu, wait_bar(bar_empty(slot), ph ^ 1u, abort_flag, args.status, 1));
+    int qi = 0;
+    for (int it = item_of(0); ok && it < total_items; it = item_of(++qi)) {
+      int bh, pair;
+      coords(it, bh, pair);
+      const int row0 = pair * 256;
+      const int n1 = blocks_of(pair, 1);
+      // the Q buffers are free once the previous item's S MMAs are complete
+      if (qi > 0) {
+        ok = __all_sync(0xffffffffu, wait_bar(bar_qe, (qi - 1) & 1, abort_flag, args.status, 13));
         if (!ok) break;
-        if (leader) {
-          mbar_arrive_expect_tx(bar_full(slot), C::kTileBytes);
-          const CUtensorMap* map = kv ? &tm_v : &tm_k;
+      }
+      if (leader) {
+        mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
 #pragma unroll
           for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d_hint(sbase + C::kRingOff + slot * C::kTileBytes + b * C::kBoxBytes, map, bar_full(slot),
-                             b * 64, j * 128, bh, pol_kv);
-        }
-        ++seq;
-        if (++slot == static_cast<uint32_t>(C::kSlots)) {
-          slot = 0;
-          ph ^= 1u;
+            tma_load_3d_hint(sbase + t * C::kTileBytes + b * C::kBoxBytes, &tm_q, bar_q, b * 64, row0 + 128 * t, bh,
+                             pol_q);
+      }
+      for (int j = 0; ok && j < n1; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          ok = __all_sync(0xffffffffu, wait_bar(bar_empty(slot), ph ^ 1u, abort_flag, args.status, 1));
+          if (!ok) break;
+          if (leader) {
+            mbar_arrive_expect_tx(bar_full(slot), C::kTileBytes);
+            const CUtensorMap* map = kv ? &tm_v : &tm_k;
+#pragma unroll
+            for (int b = 0; b < C::kBoxes; ++b)
+              tma_load_3d_hint(sbase + C::kRingOff + slot * C::kTileBytes + b * C::kBoxBytes, map, bar_full(slot),
+                               b * 64, j * 128, bh, pol_kv);
+          }
+          ++seq;
+          if (++slot == static_cast<uint32_t>(C::kSlots)) {
+            slot = 0;
+            ph ^= 1u;
+          }
         }
       }
     }
     if (!ok) {
       // let the copies already in flight land before the CTA's memory is released
-      drain_bar(bar_q, 0);
+      drain_bar(bar_q, (qi & 1) ^ 1);
       for (int s = seq - C::kSlots < 0 ? 0 : seq - C::kSlots; s < seq; ++s)
         drain_bar(bar_full(s % C::kSlots), (s / C::kSlots) & 1);
     }
@@ -289,40 +307,41 @@ __global__ void __launch_bounds__(384, 1)
       };
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t kIdO = idesc_bf16_f32(128, D, true);
-      constexpr uint64_t kSlotStep = C::kTileBytes >> 4;  // descriptor units between ring slots
-      // Descriptors are built once and advanced with constant adds (the start
-      // address is their low field; every operand stays below 256 KiB).
-      // Q and K are K-major: 8-row groups 1024 bytes apart; the next K=16 slice
-      // is 32 bytes further inside a 128-byte swizzle row, the 5th starts the
-      // next 64-column box.
-      const uint64_t q_desc[2] = {smem_desc_sw128(sbase, 16, 1024),
-                                  smem_desc_sw128(sbase + C::kTileBytes, 16, 1024)};
-      const uint64_t k_ring = smem_desc_sw128(sbase + C::kRingOff, 16, 1024);
-      // V is MN-major: 64-column halves kBoxBytes apart, 8-key groups 1024 bytes
-      // apart; the next 16 keys are 2048 bytes further.
-      const uint64_t v_ring = smem_desc_sw128(sbase + C::kRingOff, C::kBoxBytes, 1024);
-      auto kmajor_step = [](int kk) -> uint64_t {
-        return static_cast<uint64_t>(((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4);
-      };
+      constexpr uint32_t kSlotStep = C::kTileBytes >> 4;  // descriptor units between ring slots
+      // Descriptors are built once and advanced with constant adds to their
+      // low word (start address >> 4; every operand lies below 256 KiB, so no
+      // carry leaves the field). The high word (8-row groups 1024 bytes apart,
+      // 128-byte swizzle) is the same for Q, K and V.
+      // Q and K are K-major: the next K=16 slice is 32 bytes further inside a
+      // 128-byte swizzle row, the 5th starts the next 64-column box.
+      const uint64_t q0 = smem_desc_sw128(sbase, 16, 1024);
+      const uint32_t desc_hi = static_cast<uint32_t>(q0 >> 32);
+      const uint32_t q_lo[2] = {static_cast<uint32_t>(q0),
+                                static_cast<uint32_t>(smem_desc_sw128(sbase + C::kTileBytes, 16, 1024))};
+      const uint32_t k_ring = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kRingOff, 16, 1024));
+      // V is MN-major: 64-column halves kBoxBytes apart (the leading offset),
+      // 8-key groups 1024 bytes apart; the next 16 keys are 2048 bytes further.
+      const uint32_t v_ring = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kRingOff, C::kBoxBytes, 1024));
+      auto kmajor_step = [](int kk) -> uint32_t { return ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4; };
       auto issue_s = [&](int t, uint32_t slot) {
-        const uint64_t a = q_desc[t];
-        const uint64_t b = k_ring + slot * kSlotStep;
+        const uint32_t a = q_lo[t];
+        const uint32_t b = k_ring + slot * kSlotStep;
         const uint32_t d = tmem + C::col_s(t);
         if (leader) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(d, a + kmajor_step(kk), b + kmajor_step(kk), kIdS, kk > 0 ? 1u : 0u);
+            mma_ss_lo(d, a + kmajor_step(kk), b + kmajor_step(kk), desc_hi, kIdS, kk > 0 ? 1u : 0u);
         }
       };
       // O_t += P_t V for keys [64 h, 64 h + 64) of the block
       auto issue_pv = [&](int t, uint32_t slot, int h, bool first) {
-        const uint64_t b = v_ring + slot * kSlotStep;
+        const uint32_t b = v_ring + slot * kSlotStep;
         const uint32_t d = tmem + C::col_o(t);
         const uint32_t a = tmem + C::col_s(t);
         if (leader) {
 #pragma unroll
           for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
-            mma_ts(d, a + kk * 8, b + kk * 128, kIdO, (!first || kk > 0) ? 1u : 0u);
+            mma_ts_lo(d, a + kk * 8, b + kk * 128, desc_hi, kIdO, (!first || kk > 0) ? 1u : 0u);
         }
       };
       // ring positions: K_j is the (2j)-th load, V_j the (2j+1)-th
@@ -333,60 +352,86 @@ __global__ void __launch_bounds__(384, 1)
           phase ^= 1u;
         }
       };
+      // ring positions continue across items: K_j of an item follows the
+      // previous item's last V
       uint32_t ks = 0, kph = 0;  // K_j
       uint32_t vs = 1, vph = 0;  // V_j
-      bool ok = wait(bar_q, 0, 2) && wait(bar_full(ks), kph, 3);
-      if (ok) {
+      uint32_t gb0 = 0, gb1 = 0;  // blocks of tile 0 / tile 1 before this item (barrier phases)
+      bool ok = true;
+      int qi = 0;
+      for (int it = item_of(0); ok && it < total_items; it = item_of(++qi)) {
+        int bh, pair;
+        coords(it, bh, pair);
+        (void)bh;
+        const int n0 = blocks_of(pair, 0);
+        const int n1 = blocks_of(pair, 1);
+        ok = wait(bar_q, qi & 1, 2) && wait(bar_full(ks), kph, 3);
+        if (!ok) break;
         tc_fence_after();
         issue_s(0, ks);
         commit(bar_s(0));
         issue_s(1, ks);
         commit(bar_s(1));
         commit(bar_empty(ks));
-      }
-      for (int j = 0; ok && j < n1; ++j) {
-        if (!wait(bar_full(vs), vph, 4)) break;
-        uint32_t ks_next = ks, kph_next = kph;
-        advance2(ks_next, kph_next);
-        bool k_next_ready = false;
-        if (j < n0) {
-          if (!wait(bar_p(0, 0), j & 1, 5)) break;
-          tc_fence_after();
-          issue_pv(0, vs, 0, j == 0);
-          if (!wait(bar_p(0, 1), j & 1, 11)) break;
-          tc_fence_after();
-          issue_pv(0, vs, 1, false);
-          if (j + 1 < n0) {
-            if (!wait(bar_full(ks_next), kph_next, 6)) break;
-            k_next_ready = true;
+        if (n1 == 1) commit(bar_qe);  // this item's S MMAs are all issued
+        for (int j = 0; ok && j < n1; ++j) {
+          if (!wait(bar_full(vs), vph, 4)) {
+            ok = false;
+            break;
+          }
+          uint32_t ks_next = ks, kph_next = kph;
+          advance2(ks_next, kph_next);
+          bool k_next_ready = false;
+          if (j < n0) {
+            const uint32_t par = (gb0 + j) & 1;
+            ok = wait(bar_p(0, 0), par, 5);
+            if (!ok) break;
             tc_fence_after();
-            issue_s(0, ks_next);
-            commit(bar_s(0));
+            issue_pv(0, vs, 0, j == 0);
+            ok = wait(bar_p(0, 1), par, 11);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(0, vs, 1, false);
+            if (j + 1 < n0) {
+              ok = wait(bar_full(ks_next), kph_next, 6);
+              if (!ok) break;
+              k_next_ready = true;
+              tc_fence_after();
+              issue_s(0, ks_next);
+              commit(bar_s(0));
+            } else {
+              commit(bar_o(0));
+            }
+          }
+          const uint32_t par1 = (gb1 + j) & 1;
+          ok = wait(bar_p(1, 0), par1, 7);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(1, vs, 0, j == 0);
+          ok = wait(bar_p(1, 1), par1, 12);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(1, vs, 1, false);
+          commit(bar_empty(vs));
+          if (j + 1 < n1) {
+            if (!k_next_ready) {
+              ok = wait(bar_full(ks_next), kph_next, 8);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            issue_s(1, ks_next);
+            commit(bar_s(1));
+            commit(bar_empty(ks_next));
+            if (j + 2 == n1) commit(bar_qe);  // that was this item's last S MMA
           } else {
-            commit(bar_o(0));
+            commit(bar_o(1));
           }
+          ks = ks_next;
+          kph = kph_next;
+          advance2(vs, vph);
         }
-        if (!wait(bar_p(1, 0), j & 1, 7)) break;
-        tc_fence_after();
-        issue_pv(1, vs, 0, j == 0);
-        if (!wait(bar_p(1, 1), j & 1, 12)) break;
-        tc_fence_after();
-        issue_pv(1, vs, 1, false);
-        commit(bar_empty(vs));
-        if (j + 1 < n1) {
-          if (!k_next_ready) {
-            if (!wait(bar_full(ks_next), kph_next, 8)) break;
-            tc_fence_after();
-          }
-          issue_s(1, ks_next);
-          commit(bar_s(1));
-          commit(bar_empty(ks_next));
-        } else {
-          commit(bar_o(1));
-        }
-        ks = ks_next;
-        kph = kph_next;
-        advance2(vs, vph);
+        gb0 += n0;
+        gb1 += n1;
       }
       // nothing may still be executing when TMEM is released
       commit(bar_drain);
@@ -400,19 +445,25 @@ __global__ void __launch_bounds__(384, 1)
     const int t = warp >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const int tile_row0 = row0 + 128 * t;
-    const int grow = tile_row0 + r;
-    const int nt = t ? n1 : n0;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_tm = tmem + lane_off + C::col_s(t);
     const uint32_t o_tm = tmem + lane_off + C::col_o(t);
     const float sl2 = args.scale_log2;
     const float2 sl2_2 = make_float2(sl2, sl2);
+    bool ok = true;
+    uint32_t gb = 0;  // this tile's blocks before the current item (barrier phases)
+    int qi = 0;
+    for (int it = item_of(0); ok && it < total_items; it = item_of(++qi)) {
+    int bh, pair;
+    coords(it, bh, pair);
+    const int tile_row0 = pair * 256 + 128 * t;
+    const int grow = tile_row0 + r;
+    const int nt = blocks_of(pair, t);
     float m = -INFINITY;
     float l = 0.f;
-    bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      ok = wait_bar(bar_s(t), j & 1, abort_flag, args.status, 16 + t);
+      const uint32_t par = (gb + j) & 1;
+      ok = wait_bar(bar_s(t), par, abort_flag, args.status, 16 + t);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -495,7 +546,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_arrive(bar_p(t, 1));
     }
     if (ok) {
-      ok = wait_bar(bar_o(t), 0, abort_flag, args.status, 18 + t);
+      ok = wait_bar(bar_o(t), qi & 1, abort_flag, args.status, 18 + t);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
@@ -524,7 +575,11 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (valid) args.lse[static_cast<size_t>(bh) * args.n + grow] = (m * sl2 + lg2_mufu(l)) * 0.69314718055994531f;
     }
+    // the next item's O MMAs overwrite O_t only after this warpgroup's next
+    // P is ready, i.e. after these reads
     tc_fence_before();
+    gb += nt;
+    }
   }
 
   __syncthreads();
@@ -534,10 +589,12 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-// Launch one instantiation: B*H*ceil(N/256) CTAs of 384 threads, one CTA per SM.
+// Launch one instantiation: a persistent grid of `ctas` CTAs of 384 threads,
+// one per SM (at most one per item; the work list, when used, is built for
+// that many).
 template <int D, bool CAUSAL, int EMU>
 cudaError_t launch_fwd_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                            const FwdArgs& args, int bh, int n_pairs, cudaStream_t stream) {
+                            const FwdArgs& args, const WorkList& wl, int ctas, cudaStream_t stream) {
   using C = FwdCfg<D>;
   auto kernel = attn_fwd_bf16_kernel<D, CAUSAL, EMU>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -549,10 +606,7 @@ cudaError_t launch_fwd_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, co
   e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < C::kLaunchRegs) return cudaErrorInvalidConfiguration;
-  (void)bh;
-  (void)n_pairs;
-  const long long ctas = static_cast<long long>(args.bh) * args.n_pairs;
-  kernel<<<static_cast<unsigned>(ctas), C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, args);
+  kernel<<<static_cast<unsigned>(ctas), C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, args, wl);
   return cudaGetLastError();
 }
 

@@ -6,13 +6,13 @@
 namespace attn {
 
 cudaError_t launch_fwd_bf16_d64_c0(int emu16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                   const FwdArgs& a, int bh, int n_pairs, cudaStream_t s) {
+                                   const FwdArgs& a, const WorkList& wl, int ctas, cudaStream_t s) {
   switch (emu16) {
-    case 0: return launch_fwd_bf16<64, false, 0>(q, k, v, a, bh, n_pairs, s);
-    case 1: return launch_fwd_bf16<64, false, 1>(q, k, v, a, bh, n_pairs, s);
-    case 2: return launch_fwd_bf16<64, false, 2>(q, k, v, a, bh, n_pairs, s);
-    case 3: return launch_fwd_bf16<64, false, 3>(q, k, v, a, bh, n_pairs, s);
-    case 4: return launch_fwd_bf16<64, false, 4>(q, k, v, a, bh, n_pairs, s);
+    case 0: return launch_fwd_bf16<64, false, 0>(q, k, v, a, wl, ctas, s);
+    case 1: return launch_fwd_bf16<64, false, 1>(q, k, v, a, wl, ctas, s);
+    case 2: return launch_fwd_bf16<64, false, 2>(q, k, v, a, wl, ctas, s);
+    case 3: return launch_fwd_bf16<64, false, 3>(q, k, v, a, wl, ctas, s);
+    case 4: return launch_fwd_bf16<64, false, 4>(q, k, v, a, wl, ctas, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -9,16 +9,17 @@
 namespace attn {
 
 struct FwdArgs;
+struct WorkList;
 struct FwdMxArgs;
 
 cudaError_t launch_fwd_bf16_d64_c0(int emu16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                   const FwdArgs& a, int bh, int n_pairs, cudaStream_t s);
+                                   const FwdArgs& a, const WorkList& wl, int ctas, cudaStream_t s);
 cudaError_t launch_fwd_bf16_d64_c1(int emu16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                   const FwdArgs& a, int bh, int n_pairs, cudaStream_t s);
+                                   const FwdArgs& a, const WorkList& wl, int ctas, cudaStream_t s);
 cudaError_t launch_fwd_bf16_d128_c0(int emu16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                    const FwdArgs& a, int bh, int n_pairs, cudaStream_t s);
+                                    const FwdArgs& a, const WorkList& wl, int ctas, cudaStream_t s);
 cudaError_t launch_fwd_bf16_d128_c1(int emu16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                                    const FwdArgs& a, int bh, int n_pairs, cudaStream_t s);
+                                    const FwdArgs& a, const WorkList& wl, int ctas, cudaStream_t s);
 
 cudaError_t launch_fwd_mxfp8_d128(int causal, int emu16, const CUtensorMap& q, const CUtensorMap& k,
                                   const CUtensorMap& v, const FwdMxArgs& a, cudaStream_t s);

@@ -118,6 +118,27 @@ def test_empty_problems(attn):
     assert attn.device_status() == attn.Status.OK
 
 
+# The kernel is persistent: each CTA loops over work items (one pair of
+# 128-row Q tiles of one head). Up to 8192 items go through a host-built work
+# list; beyond that the CTAs take them in serpentine rounds. Every item must be
+# computed exactly once either way: the outputs start as NaN and every row is
+# compared with the oracle.
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(2, 40, 1000, 64), (1, 8193, 33, 128), (1, 4097, 260, 64)],
+                         ids=["list_320_items", "rounds_8193_items", "rounds_8194_items"])
+def test_every_work_item_once(attn, shape, causal):
+    B, H, N, d = shape
+    q, k, v = (I.to_bf16(x) for x in I.draw_fp32(B, H, N, d, seed=H + N))
+    o = torch.full((B, H, N, d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=DEV)
+    attn.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, scale=d ** -0.5, o=o, lse=lse)
+    torch.cuda.synchronize()
+    assert attn.device_status() == attn.Status.OK
+    assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+    o_ref, lse_ref = attention_fwd(I.as_f64(q), I.as_f64(k), I.as_f64(v), causal, d ** -0.5)
+    compare(I.as_f64(o.cpu()), lse.cpu().double().numpy(), o_ref, lse_ref, f"{shape} causal={causal}")
+
+
 def test_repeat_calls_are_identical(attn):
     q, k, v = (I.to_bf16(x).to(DEV) for x in I.draw_fp32(2, 2, 777, 128, seed=17))
     o1, l1 = attn.attn_fwd(q, k, v, causal=True)
