@@ -43,7 +43,8 @@ L2_BYTES = 129 * 1024 * 1024
 # reported while these are unchanged)
 KERNEL_SOURCES = {
     "bf16": ["online_softmax_fwd_gb300/csrc/fwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/ptx.cuh",
-             "online_softmax_fwd_gb300/csrc/exp2_fma.cuh"],
+             "online_softmax_fwd_gb300/csrc/exp2_fma.cuh", "online_softmax_fwd_gb300/csrc/schedule.h",
+             "online_softmax_fwd_gb300/csrc/schedule.cu"],
     "mxfp8": ["online_softmax_fwd_gb300/csrc/fwd_mxfp8.cuh", "online_softmax_fwd_gb300/csrc/mxfp8_common.cuh",
               "online_softmax_fwd_gb300/csrc/fwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/ptx.cuh",
               "online_softmax_fwd_gb300/csrc/exp2_fma.cuh"],
