@@ -132,16 +132,13 @@ __device__ __forceinline__ float exp2_col(int c, float x) {
 
 // p = 2^(S*sl2 + neg_ms) for one half (64 keys, pairs [32 H, 32 H + 32)) of a
 // row's 128 scores, rounded to bf16 pairs and stored to TMEM at p_tm (32 bf16
-// pairs from column 32 H); returns the fp32 sum of the unrounded p. The
-// scale-and-shift and the running sums use the packed fp32 pair instructions
-// (one issue for two lanes of work).
+// pairs from column 32 H); the unrounded p are added to the row's partial sums
+// acc. The scale-and-shift and the sums use the packed fp32 pair instructions
+// (one issue for two lanes of work); eight independent partial sums keep the
+// long-latency packed add off the critical path.
 template <int EMU, bool MUFU_ONLY, int H>
-__device__ __forceinline__ float softmax_p_half(const float2 (&s)[64], float2 sl2_2, float2 neg_ms_2, uint32_t p_tm) {
-  // eight independent accumulators: the packed fp32 add has a long latency,
-  // so a short dependency chain per accumulator keeps it off the critical path
-  float2 acc[8];
-#pragma unroll
-  for (int a = 0; a < 8; ++a) acc[a] = make_float2(0.f, 0.f);
+__device__ __forceinline__ void softmax_p_half(const float2 (&s)[64], float2 sl2_2, float2 neg_ms_2, uint32_t p_tm,
+                                               float2 (&acc)[8]) {
 #pragma unroll
   for (int chunk = 2 * H; chunk < 2 * H + 2; ++chunk) {
     uint32_t pk[16];
@@ -155,12 +152,6 @@ __device__ __forceinline__ float softmax_p_half(const float2 (&s)[64], float2 sl
     }
     tmem_st16(p_tm + chunk * 16, pk);
   }
-#pragma unroll
-  for (int a = 0; a < 4; ++a) acc[a] = __fadd2_rn(acc[a], acc[a + 4]);
-  acc[0] = __fadd2_rn(acc[0], acc[2]);
-  acc[1] = __fadd2_rn(acc[1], acc[3]);
-  const float2 t = __fadd2_rn(acc[0], acc[1]);
-  return t.x + t.y;
 }
 
 template <int D, bool CAUSAL, int EMU>
@@ -460,7 +451,10 @@ __global__ void __launch_bounds__(384, 1)
     const int grow = tile_row0 + r;
     const int nt = blocks_of(pair, t);
     float m = -INFINITY;
-    float l = 0.f;
+    // the row sum l as 16 partial sums, reduced once after the last block
+    float2 acc[8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a) acc[a] = make_float2(0.f, 0.f);
     for (int j = 0; j < nt; ++j) {
       const uint32_t par = (gb + j) & 1;
       ok = wait_bar(bar_s(t), par, abort_flag, args.status, 16 + t);
@@ -513,9 +507,16 @@ __global__ void __launch_bounds__(384, 1)
       m = m_new;
       const float neg_ms = (m == -INFINITY) ? 0.f : -(m * sl2);
       const float2 neg_ms_2 = make_float2(neg_ms, neg_ms);
+      if (fire) {
+        const float2 corr_2 = make_float2(corr, corr);
+#pragma unroll
+        for (int a = 0; a < 8; ++a) acc[a] = __fmul2_rn(acc[a], corr_2);
+      }
       // first 64 keys of P
-      float psum = need_mask ? softmax_p_half<EMU, true, 0>(s, sl2_2, neg_ms_2, s_tm)
-                             : softmax_p_half<EMU, false, 0>(s, sl2_2, neg_ms_2, s_tm);
+      if (need_mask)
+        softmax_p_half<EMU, true, 0>(s, sl2_2, neg_ms_2, s_tm, acc);
+      else
+        softmax_p_half<EMU, false, 0>(s, sl2_2, neg_ms_2, s_tm, acc);
       // correction of O (before any O MMA of this block)
       if (j > 0 && __any_sync(0xffffffffu, fire)) {
 #pragma unroll
@@ -538,9 +539,10 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(bar_p(t, 0));
       // last 64 keys, while the MMA works on the first
-      psum += need_mask ? softmax_p_half<EMU, true, 1>(s, sl2_2, neg_ms_2, s_tm)
-                        : softmax_p_half<EMU, false, 1>(s, sl2_2, neg_ms_2, s_tm);
-      l = l * corr + psum;
+      if (need_mask)
+        softmax_p_half<EMU, true, 1>(s, sl2_2, neg_ms_2, s_tm, acc);
+      else
+        softmax_p_half<EMU, false, 1>(s, sl2_2, neg_ms_2, s_tm, acc);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_p(t, 1));
@@ -551,6 +553,12 @@ __global__ void __launch_bounds__(384, 1)
     }
     if (ok) {
       tc_fence_after();
+#pragma unroll
+      for (int a = 0; a < 4; ++a) acc[a] = __fadd2_rn(acc[a], acc[a + 4]);
+      acc[0] = __fadd2_rn(acc[0], acc[2]);
+      acc[1] = __fadd2_rn(acc[1], acc[3]);
+      const float2 l2 = __fadd2_rn(acc[0], acc[1]);
+      const float l = l2.x + l2.y;
       const float inv_l = 1.0f / l;
       const bool valid = grow < args.n;
       __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * args.n + (valid ? grow : 0)) * D;
