@@ -82,7 +82,7 @@ def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool, sca
 
 def blockwise_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool, scale: float,
                         block: int = 128, tau: float | None = None, dtype=np.float64,
-                        p_cast=None) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+                        p_cast=None, row_index: np.ndarray | None = None) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
     """The streaming recurrence over key blocks, for one (batch, head) per call
     or for [..., N, d] batched inputs.
 
@@ -102,7 +102,8 @@ def blockwise_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: boo
     matrix-multiply input type before P V while the sum uses the unrounded P
     (the reading of "FlashAttention-4's Softmax Tricks", section "Conditional
     rescaling": the sum is taken from fp32 P, and P is cast to the MMA input
-    type). Returns (O, LSE, fired) where fired
+    type). ``row_index`` gives the sequence positions of q's rows (default
+    0 .. n_q - 1) for the causal mask. Returns (O, LSE, fired) where fired
     [..., N, nblocks] is True where the running max moved (block 0 included).
     """
     f = dtype
@@ -117,10 +118,11 @@ def blockwise_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: boo
     o = np.zeros(lead + (n_q, v.shape[-1]), dtype=f)
     nblocks = (n_k + block - 1) // block
     fired = np.zeros(lead + (n_q, nblocks), dtype=bool)
-    rows = np.arange(n_q)
+    rows = np.arange(n_q) if row_index is None else np.asarray(row_index)
+    last_row = int(rows.max()) if rows.size else -1
     for jb in range(nblocks):
         j0, j1 = jb * block, min(n_k, (jb + 1) * block)
-        if causal and j0 > n_q - 1:
+        if causal and j0 > last_row:
             break                                   # every remaining block is above the diagonal
         s = q @ np.swapaxes(k[..., j0:j1, :], -1, -2)   # raw scores [..., n_q, bk]
         if causal and j1 - 1 > 0:

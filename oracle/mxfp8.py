@@ -11,6 +11,12 @@ E4M3 value), so the block's largest element lands in the top binade of E4M3
 without saturating; an all-zero block takes e = 0. Elements are divided by 2^e
 (exact) and rounded to E4M3, nearest with ties to even, saturating at +-448.
 
+The same page, section "Softmax conversion and unroll-KV", converts P (the
+probabilities, all in [0, 1]) to MXFP8 inside the kernel for the P V product,
+one E8M0 scale per 32 consecutive keys of a row: ``p_to_mxfp8`` applies the
+same scale rule to each such group of a row (the group's amax is the largest
+P in it).
+
 E4M3 (the OCP "E4M3FN" encoding): 1 sign bit, 4 exponent bits with bias 7,
 3 mantissa bits; exponent field 0 encodes subnormals m * 2^-9; the code
 S.1111.111 is NaN and there are no infinities, so the largest finite value is
@@ -89,3 +95,17 @@ def quantize_blocks(x: np.ndarray) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
     codes = codes_full[..., :R, :C]
     deq = e4m3_decode(codes) * scale_full[..., :R, :C]
     return codes, e, deq
+
+
+def p_to_mxfp8(p: np.ndarray) -> np.ndarray:
+    """Values of P [..., rows, keys] after the MXFP8 conversion: each run of 32
+    consecutive keys of a row (from key 0 of the block) shares one E8M0 scale
+    chosen by the rule above from the run's largest P, and every P is divided
+    by it and rounded to E4M3. Returns the dequantised values (float64)."""
+    p = np.asarray(p, dtype=np.float64)
+    out = np.empty_like(p)
+    for g0 in range(0, p.shape[-1], BLOCK):
+        run = p[..., g0:g0 + BLOCK]
+        scale = np.exp2(e8m0_exponent(np.abs(run).max(axis=-1)).astype(np.float64))[..., None]
+        out[..., g0:g0 + BLOCK] = e4m3_decode(e4m3_encode(run / scale)) * scale
+    return out

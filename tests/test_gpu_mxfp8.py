@@ -2,9 +2,13 @@
 
 The quantiser must equal the oracle's bit for bit (E4M3 codes and E8M0 scales,
 the latter expanded into the documented 512-byte atom layout). The attention
-output is compared with the float64 oracle run on the dequantised inputs, with
-the MXFP8 bound of 6e-2 on O (P is quantised to E4M3 inside the kernel) and
-1e-3 on LSE (computed from fp32 P).
+output is compared with the float64 oracle of the MXFP8 method: the
+recurrence on the dequantised inputs with P converted to MXFP8 per 32 keys
+before P V (the sum from unconverted P), within the MXFP8 bound of 6e-2 on O
+and 1e-3 on LSE. Against exact attention of the dequantised inputs, the P
+conversion alone moves O by up to ~6.5e-2 on causal rows with very few keys
+(3 mantissa bits on a handful of terms), so the exact result is not the
+parity target here.
 """
 import numpy as np
 import pytest
@@ -12,7 +16,7 @@ import torch
 
 import attn_inputs as I
 from oracle import mxfp8 as M
-from oracle.attention import attention_fwd, attention_rows
+from oracle.attention import attention_fwd, blockwise_attention
 from parity import sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -86,12 +90,26 @@ def run_mxfp8(attn, w_causal, x_q, x_k, x_v, scale, **kw):
     return o.cpu(), lse.cpu()
 
 
+def mx_reference(xq, xk, xv, causal, scale, rows=None, tau=0.0):
+    """The MXFP8 method in float64 for one head ([N, 128] fp32 inputs): Q, K, V
+    quantised by the oracle's quantiser, P converted per 32 keys; rows = the
+    query positions to compute (default all)."""
+    dq, dk, dv = (M.quantize_blocks(x)[2] for x in (xq, xk, xv))
+    if rows is None:
+        rows = np.arange(dq.shape[0])
+    o, lse, _ = blockwise_attention(dq[rows], dk, dv, causal, scale, tau=tau, p_cast=M.p_to_mxfp8, row_index=rows)
+    return o, lse
+
+
 def check(o, lse, o_ref, lse_ref, what):
     err = np.abs(I.as_f64(o) - o_ref)
     lerr = np.abs(lse.double().numpy() - lse_ref)
     assert np.isfinite(err).all() and np.isfinite(lerr).all(), what
     assert err.max() <= O_MAX_ABS_MXFP8, f"{what}: O max abs {err.max():.4g} mean {err.mean():.3g}"
     assert lerr.max() <= LSE_MAX_ABS, f"{what}: LSE max abs {lerr.max():.3g}"
+    import os
+    if os.environ.get("MX_ERR_LOG"):
+        print(f"MXERR {what}: max {err.max():.4g} mean {err.mean():.3g} lse {lerr.max():.3g}")
     return err.max(), err.mean()
 
 
@@ -102,9 +120,37 @@ def test_small_shapes(attn, shape, causal):
     B, H, N = shape
     xq, xk, xv = I.draw_fp32(B, H, N, 128, seed=N + 7)
     o, lse = run_mxfp8(attn, causal, xq, xk, xv, 128 ** -0.5)
-    deq = [M.quantize_blocks(x.reshape(B * H, N, 128))[2].reshape(B, H, N, 128) for x in (xq, xk, xv)]
-    o_ref, lse_ref = attention_fwd(*deq, causal, 128 ** -0.5)
-    check(o, lse, o_ref, lse_ref, f"{shape} causal={causal}")
+    for b in range(B):
+        for h in range(H):
+            o_ref, lse_ref = mx_reference(xq[b, h], xk[b, h], xv[b, h], causal, 128 ** -0.5)
+            check(o[b, h], lse[b, h], o_ref, lse_ref, f"{shape} causal={causal} b={b} h={h}")
+
+
+# Persistent CTAs: up to 8192 (head, Q-tile pair) items follow a host-built
+# work list, more go in serpentine rounds; every item must be computed exactly
+# once: the outputs start as NaN and must all be written, and every row of a
+# sample of heads (first, last, random) matches the oracle.
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(2, 40, 1000), (1, 8193, 33), (1, 4097, 260)],
+                         ids=["list_320_items", "rounds_8193_items", "rounds_8194_items"])
+def test_every_work_item_once(attn, shape, causal):
+    B, H, N = shape
+    xq, xk, xv = I.draw_fp32(B, H, N, 128, seed=H + N)
+    q8, q_sf = quantize_gpu(attn, xq, 0)
+    k8, k_sf = quantize_gpu(attn, xk, 0)
+    v8, v_sf = quantize_gpu(attn, xv, 1)
+    o = torch.full((B, H, N, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=DEV)
+    attn.attn_fwd_mxfp8(q8, q_sf, k8, k_sf, v8, v_sf, causal=causal, scale=128 ** -0.5, o=o, lse=lse)
+    torch.cuda.synchronize()
+    assert attn.device_status() == attn.Status.OK
+    assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+    o, lse = o.cpu(), lse.cpu()
+    rng = np.random.default_rng(H)
+    heads = {(0, 0), (B - 1, H - 1)} | {(int(rng.integers(B)), int(rng.integers(H))) for _ in range(6)}
+    for b, h in sorted(heads):
+        o_ref, lse_ref = mx_reference(xq[b, h], xk[b, h], xv[b, h], causal, 128 ** -0.5)
+        check(o[b, h], lse[b, h], o_ref, lse_ref, f"{shape} causal={causal} b={b} h={h}")
 
 
 def peaked_case():
@@ -116,9 +162,11 @@ def peaked_case():
 
 @pytest.mark.parametrize("emu", [0, 2, 4])
 def test_software_exp2_shares_on_peaked_rows(attn, emu):
-    (xq, xk, xv), (o_ref, lse_ref) = peaked_case()
+    (xq, xk, xv), _ = peaked_case()
     o, lse = run_mxfp8(attn, True, xq, xk, xv, 128 ** -0.5, exp2_emu16=emu)
-    check(o, lse, o_ref, lse_ref, f"emu={emu}")
+    for h in range(2):
+        o_ref, lse_ref = mx_reference(xq[0, h], xk[0, h], xv[0, h], True, 128 ** -0.5)
+        check(o[0, h], lse[0, h], o_ref, lse_ref, f"emu={emu} h={h}")
 
 
 def test_lagging_max_costs_accuracy_with_fp8_p(attn):
@@ -140,7 +188,6 @@ def test_full_size_workload_sampled(attn):
     assert torch.isfinite(lse).all()
     rng = np.random.default_rng(3)
     for b, h in ((0, 0), (w.B - 1, w.H - 1), (int(rng.integers(w.B)), int(rng.integers(w.H)))):
-        dq, dk, dv = (M.quantize_blocks(x[b, h])[2] for x in (xq, xk, xv))
         rows = sample_rows(w.N, rng)
-        o_ref, lse_ref = attention_rows(dq[rows], dk, dv, rows, w.causal, w.scale)
+        o_ref, lse_ref = mx_reference(xq[b, h], xk[b, h], xv[b, h], w.causal, w.scale, rows=rows)
         check(o[b, h, rows], lse[b, h, rows], o_ref, lse_ref, f"{w.name} b={b} h={h}")

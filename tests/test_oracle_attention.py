@@ -176,3 +176,14 @@ def test_precision_bands():
     ob = bf16_round(ob)
     eb = np.max(np.abs(ob - o_refb[0]))
     assert eb < g["bf16_max_abs_hi"]
+
+
+def test_blockwise_row_index_selects_rows():
+    # the recurrence on a subset of query rows, given their positions, equals
+    # the same rows of the full computation (causal mask by position)
+    rng = np.random.default_rng(11)
+    q, k, v = (rng.standard_normal((300, 32)) for _ in range(3))
+    o, lse, _ = A.blockwise_attention(q, k, v, True, 0.2, block=64, tau=8.0)
+    rows = np.array([0, 1, 63, 64, 150, 299])
+    o_s, lse_s, _ = A.blockwise_attention(q[rows], k, v, True, 0.2, block=64, tau=8.0, row_index=rows)
+    assert np.allclose(o_s, o[rows], rtol=0, atol=1e-12) and np.allclose(lse_s, lse[rows], rtol=0, atol=1e-12)

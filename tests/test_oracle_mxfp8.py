@@ -72,3 +72,54 @@ def test_ragged_rows_are_padded_for_amax_only():
     codes, e, deq = M.quantize_blocks(x)
     assert codes.shape == (1, 1, 40, 64) and e.shape == (1, 1, 2, 2)
     assert np.array_equal(deq, x)
+
+
+# ---- P converted to MXFP8 (one scale per 32 consecutive keys of a row)
+
+def test_p_runs_of_representable_values_are_unchanged():
+    # a run whose largest value is 1 takes scale 2^-8; values k/8 * 2^-n are
+    # E4M3 values times that scale when they stay in E4M3's range
+    vals = M.e4m3_decode(np.arange(0x08, 0x7F)) * 2.0 ** -8      # normal E4M3 values, scaled
+    vals = vals[vals <= 1.0]
+    rng = np.random.default_rng(5)
+    p = rng.choice(vals, size=(7, 32))
+    p[:, 0] = 1.0
+    assert np.array_equal(M.p_to_mxfp8(p), p)
+
+
+def test_p_runs_follow_the_scale_rule_and_nearest_rounding():
+    # brute force: every element is the nearest of all E4M3 values times the
+    # run's 2^e, e the smallest exponent with amax <= 448 * 2^e
+    rng = np.random.default_rng(6)
+    p = np.exp2(-rng.uniform(0, 12, size=(5, 96)))
+    p[2, 32:64] *= 1e-3                         # a quiet run must get its own, smaller scale
+    got = M.p_to_mxfp8(p)
+    grid = M.e4m3_decode(np.arange(0x00, 0x7F))
+    for r in range(p.shape[0]):
+        for g0 in range(0, 96, 32):
+            run = p[r, g0:g0 + 32]
+            e = 0
+            while run.max() > 448.0 * 2.0 ** e:
+                e += 1
+            while run.max() <= 448.0 * 2.0 ** (e - 1):
+                e -= 1
+            cand = grid * 2.0 ** e
+            want = cand[np.abs(run[:, None] - cand[None, :]).argmin(axis=1)]
+            assert np.array_equal(got[r, g0:g0 + 32], want)
+
+
+def test_p_relative_error_and_run_boundaries():
+    rng = np.random.default_rng(7)
+    p = rng.uniform(0.0, 1.0, size=(4, 70))     # runs [0, 32), [32, 64), [64, 70)
+    got = M.p_to_mxfp8(p)
+    for a, b in ((0, 32), (32, 64), (64, 70)):
+        run, out = p[:, a:b], got[:, a:b]
+        scale = np.exp2(M.e8m0_exponent(run.max(axis=1)).astype(float))[:, None]
+        normal = run / scale >= 2.0 ** -6       # E4M3's normal range after scaling
+        rel = np.abs(out - run)[normal] / run[normal]
+        assert rel.max() <= 2.0 ** -4 + 1e-12
+    # changing one run leaves the others alone
+    q = p.copy()
+    q[:, 32:64] *= 1e-4
+    got_q = M.p_to_mxfp8(q)
+    assert np.array_equal(got_q[:, :32], got[:, :32]) and np.array_equal(got_q[:, 64:], got[:, 64:])
