@@ -246,7 +246,19 @@ attn_status_t attn_fwd_mxfp8_ex(const void* q8, const void* q_sf, const void* k8
   a.scale = scale;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.tau = tau;
-  cudaError_t e = attn::launch_fwd_mxfp8_d128(causal, exp2_emu16, mq, mk, mv, a, static_cast<cudaStream_t>(stream));
+  const int sms = sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  // persistent grid with the same work-list schedule as the bf16 kernel
+  const long long items = bh * a.n_pairs;
+  attn::WorkList wl;
+  int ctas = static_cast<int>(std::min<long long>(items, std::min(sms, attn::kListMaxCtas)));
+  a.use_list = attn::work_list_for(a.bh, a.n_pairs, a.n_tiles, a.band, causal != 0, ctas, &wl) ? 1 : 0;
+  if (!a.use_list) {
+    std::memset(&wl, 0, sizeof(wl));
+    ctas = static_cast<int>(std::min<long long>(items, sms));
+  }
+  cudaError_t e =
+      attn::launch_fwd_mxfp8_d128(causal, exp2_emu16, mq, mk, mv, a, wl, ctas, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -8,13 +8,17 @@
 // mantissa bits). The online-softmax recurrence, lagging-max rescale and
 // epilogue are those of the bf16 kernel (fwd_bf16.cuh).
 //
-// Structure: the bf16 kernel's two 128-row Q tiles in ping-pong, one CTA per
-// (tile pair, head), warps 0-7 softmax (thread = row), warp 8 TMA, warp 9 MMA.
-// The 512 TMEM columns hold S0, S1, O0, O1 (128 each) as in the bf16 kernel,
-// so the scale factors go where the same page's section "TMEM allocation and
-// scale factor placement" puts them:
-//   * the two first S GEMMs read their Q and K scales from the O regions,
-//     which no MMA has written yet;
+// Structure: the bf16 kernel's two 128-row Q tiles in ping-pong, persistent
+// CTAs over (tile pair, head) work items from the same list schedule, warps
+// 0-7 softmax (thread = row), warp 8 TMA, warp 9 MMA. The 512 TMEM columns
+// hold S0, S1, O0, O1 (128 each) as in the bf16 kernel, so the scale factors
+// go where the same page's section "TMEM allocation and scale factor
+// placement" puts them:
+//   * the two first S GEMMs of a CTA read their Q and K scales from the O
+//     regions, which no MMA has written yet; for later items S0(0) takes the
+//     S1 columns 40-47 below, and S1(0) the O1 region again as soon as the
+//     softmax of tile 1 has read the previous item's O1 into registers (its
+//     epilogue loads all of O before converting and storing it);
 //   * an O GEMM of tile t reads P's scales (written by the softmax) and V's
 //     scales from free columns of S_t: P as E4M3 takes columns 0-31, so
 //     32-35 (P) and 36-39 (V) are free once the softmax has read S_t;
@@ -33,6 +37,7 @@
 #include "fwd_bf16.cuh"
 #include "mxfp8_common.cuh"
 #include "ptx.cuh"
+#include "schedule.h"
 
 namespace attn {
 
@@ -48,6 +53,7 @@ struct FwdMxArgs {
   int n_pairs;           // ceil(N / 256)
   int bh;
   int band;
+  int use_list;          // 1: items from the work list; 0: serpentine rounds
   float scale;
   float scale_log2;
   float tau;
@@ -61,8 +67,9 @@ struct MxCfg {
   static constexpr uint32_t kQAtomOff = kRingOff + kSlots * kTileBytes;  // Q0, Q1 atoms
   static constexpr uint32_t kAtomOff = kQAtomOff + 2 * kAtomBytes;       // one atom per ring slot
   static constexpr uint32_t kBarOff = kAtomOff + kSlots * kAtomBytes;
-  // q_full, full[kSlots], empty[kSlots], s_full[2], p_full[2], o_final[2], s_loaded[2], drain
-  static constexpr int kNumBars = 1 + 2 * kSlots + 9;
+  // q_full, full[kSlots], empty[kSlots], s_full[2], p_full[2], o_final[2], s_loaded[2], drain, q_empty,
+  // o_read[2]
+  static constexpr int kNumBars = 1 + 2 * kSlots + 12;
   static constexpr uint32_t kHolderOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kAbortOff = kHolderOff + 4;
   static constexpr uint32_t kSmemBytes = kAbortOff + 4 + 1024;
@@ -85,7 +92,8 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
 template <bool CAUSAL, int EMU>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_mxfp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v, const FwdMxArgs args) {
+                          const __grid_constant__ CUtensorMap tm_v, const FwdMxArgs args,
+                          const __grid_constant__ WorkList wl) {
   using C = MxCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -98,24 +106,28 @@ __global__ void __launch_bounds__(384, 1)
   auto bar_o = [&](int t) { return bar_q + 8u * (5 + 2 * C::kSlots + t); };
   auto bar_ld = [&](int t) { return bar_q + 8u * (7 + 2 * C::kSlots + t); };
   const uint32_t bar_drain = bar_q + 8u * (9 + 2 * C::kSlots);
+  const uint32_t bar_qe = bar_q + 8u * (10 + 2 * C::kSlots);  // Q buffers and atoms free again
+  // the softmax of tile t has read O_t into registers (epilogue)
+  auto bar_oread = [&](int t) { return bar_q + 8u * (11 + 2 * C::kSlots + t); };
   uint32_t* holder = reinterpret_cast<uint32_t*>(smem + C::kHolderOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kAbortOff);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int bh, pair;
-  {
-    const int per_band = args.band * args.n_pairs;
-    const int band_id = blockIdx.x / per_band;
-    const int r = blockIdx.x - band_id * per_band;
-    const int heads = min(args.band, args.bh - band_id * args.band);
-    pair = args.n_pairs - 1 - r / heads;  // heaviest causal pairs first
-    bh = band_id * args.band + r % heads;
-  }
-  const int row0 = pair * 256;
+  // work items as in the bf16 kernel: the list, else serpentine rounds
+  const int total_items = args.bh * args.n_pairs;
+  auto item_of = [&](int k) {
+    if (args.use_list) {
+      const int idx = wl.first[blockIdx.x] + k;
+      return idx < wl.first[blockIdx.x + 1] ? static_cast<int>(wl.item[idx]) : total_items;
+    }
+    const long long g = gridDim.x;
+    const long long o = k * g + ((k & 1) ? g - 1 - blockIdx.x : blockIdx.x);
+    return o < total_items ? static_cast<int>(o) : total_items;
+  };
+  auto coords = [&](int it, int& bh, int& pair) { item_coords(it, args.bh, args.n_pairs, args.band, bh, pair); };
   const int nkv = args.n_tiles;
-  const int n0 = CAUSAL ? min(2 * pair + 1, nkv) : nkv;
-  const int n1 = CAUSAL ? min(2 * pair + 2, nkv) : nkv;
+  auto blocks_of = [&](int pair, int t) { return CAUSAL ? min(2 * pair + 1 + t, nkv) : nkv; };
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -130,6 +142,9 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar_ld(t), 128);
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_qe, 1);
+    mbar_init(bar_oread(0), 128);
+    mbar_init(bar_oread(1), 128);
     *abort_flag = 0u;
     fence_barrier_init();
   }
@@ -150,42 +165,54 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t leader = elect_one();
       const uint64_t pol_q = policy_evict_first();
       const uint64_t pol_kv = policy_evict_last();
-      const size_t head_atoms = static_cast<size_t>(bh) * nkv;
-      if (leader) {
-        mbar_arrive_expect_tx(bar_q, 2 * (C::kTileBytes + C::kAtomBytes));
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          tma_load_3d_hint(sbase + t * C::kTileBytes, &tm_q, bar_q, 0, row0 + 128 * t, bh, pol_q);
-          // a tile past N reads zeros through the map; its scales may be any valid atom
-          const int qt = min(2 * pair + t, nkv - 1);
-          bulk_load(sbase + C::kQAtomOff + t * C::kAtomBytes, args.q_sf + (head_atoms + qt) * C::kAtomBytes,
-                    C::kAtomBytes, bar_q);
-        }
-      }
       int seq = 0;
       uint32_t slot = 0, ph = 0;
       bool ok = true;
-      for (int j = 0; ok && j < n1; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
-          ok = __all_sync(0xffffffffu, wait_bar(bar_empty(slot), ph ^ 1u, abort_flag, args.status, 1));
+      int qi = 0;
+      for (int it = item_of(0); ok && it < total_items; it = item_of(++qi)) {
+        int bh, pair;
+        coords(it, bh, pair);
+        const int row0 = pair * 256;
+        const int n1 = blocks_of(pair, 1);
+        const size_t head_atoms = static_cast<size_t>(bh) * nkv;
+        // the Q buffers and atoms are free once the previous item's S GEMMs are complete
+        if (qi > 0) {
+          ok = __all_sync(0xffffffffu, wait_bar(bar_qe, (qi - 1) & 1, abort_flag, args.status, 13));
           if (!ok) break;
-          if (leader) {
-            mbar_arrive_expect_tx(bar_full(slot), C::kTileBytes + C::kAtomBytes);
-            tma_load_3d_hint(sbase + C::kRingOff + slot * C::kTileBytes, kv ? &tm_v : &tm_k, bar_full(slot), 0,
-                             j * 128, bh, pol_kv);
-            bulk_load(sbase + C::kAtomOff + slot * C::kAtomBytes,
-                      (kv ? args.v_sf : args.k_sf) + (head_atoms + j) * C::kAtomBytes, C::kAtomBytes,
-                      bar_full(slot));
+        }
+        if (leader) {
+          mbar_arrive_expect_tx(bar_q, 2 * (C::kTileBytes + C::kAtomBytes));
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            tma_load_3d_hint(sbase + t * C::kTileBytes, &tm_q, bar_q, 0, row0 + 128 * t, bh, pol_q);
+            // a tile past N reads zeros through the map; its scales may be any valid atom
+            const int qt = min(2 * pair + t, nkv - 1);
+            bulk_load(sbase + C::kQAtomOff + t * C::kAtomBytes, args.q_sf + (head_atoms + qt) * C::kAtomBytes,
+                      C::kAtomBytes, bar_q);
           }
-          ++seq;
-          if (++slot == static_cast<uint32_t>(C::kSlots)) {
-            slot = 0;
-            ph ^= 1u;
+        }
+        for (int j = 0; ok && j < n1; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            ok = __all_sync(0xffffffffu, wait_bar(bar_empty(slot), ph ^ 1u, abort_flag, args.status, 1));
+            if (!ok) break;
+            if (leader) {
+              mbar_arrive_expect_tx(bar_full(slot), C::kTileBytes + C::kAtomBytes);
+              tma_load_3d_hint(sbase + C::kRingOff + slot * C::kTileBytes, kv ? &tm_v : &tm_k, bar_full(slot), 0,
+                               j * 128, bh, pol_kv);
+              bulk_load(sbase + C::kAtomOff + slot * C::kAtomBytes,
+                        (kv ? args.v_sf : args.k_sf) + (head_atoms + j) * C::kAtomBytes, C::kAtomBytes,
+                        bar_full(slot));
+            }
+            ++seq;
+            if (++slot == static_cast<uint32_t>(C::kSlots)) {
+              slot = 0;
+              ph ^= 1u;
+            }
           }
         }
       }
       if (!ok) {
-        drain_bar(bar_q, 0);
+        drain_bar(bar_q, (qi & 1) ^ 1);
         for (int s = seq - C::kSlots < 0 ? 0 : seq - C::kSlots; s < seq; ++s)
           drain_bar(bar_full(s % C::kSlots), (s / C::kSlots) & 1);
       }
@@ -199,10 +226,15 @@ __global__ void __launch_bounds__(384, 1)
       auto wait = [&](uint32_t bar, uint32_t parity, uint32_t where) {
         return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, args.status, where));
       };
-      constexpr uint64_t kSlotStep = C::kTileBytes >> 4;
-      const uint64_t q_desc[2] = {smem_desc_sw128(sbase, 16, 1024), smem_desc_sw128(sbase + C::kTileBytes, 16, 1024)};
-      const uint64_t ring_k = smem_desc_sw128(sbase + C::kRingOff, 16, 1024);
-      const uint64_t ring_v = smem_desc_sw128(sbase + C::kRingOff, C::kTileBytes, 1024);
+      constexpr uint32_t kSlotStep = C::kTileBytes >> 4;
+      // descriptors as low words (start address, leading offset) plus one
+      // shared high word (8-row groups 1024 bytes apart, 128-byte swizzle)
+      const uint64_t q0 = smem_desc_sw128(sbase, 16, 1024);
+      const uint32_t desc_hi = static_cast<uint32_t>(q0 >> 32);
+      const uint32_t q_desc[2] = {static_cast<uint32_t>(q0),
+                                  static_cast<uint32_t>(smem_desc_sw128(sbase + C::kTileBytes, 16, 1024))};
+      const uint32_t ring_k = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kRingOff, 16, 1024));
+      const uint32_t ring_v = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kRingOff, C::kTileBytes, 1024));
       auto slot_atom = [&](uint32_t slot) { return sbase + C::kAtomOff + slot * C::kAtomBytes; };
       // S_t = Q_t K^T from ring slot kslot; scales copied to TMEM columns sf_cols (Q) and sf_cols + 4 (K)
       auto issue_s = [&](int t, uint32_t kslot, uint32_t sf_cols) {
@@ -211,8 +243,8 @@ __global__ void __launch_bounds__(384, 1)
           sf_copy_to_tmem(tmem + sf_cols + 4, slot_atom(kslot));
 #pragma unroll
           for (uint32_t kk = 0; kk < 4; ++kk)
-            mma_mxf8_ss(tmem + C::col_s(t), q_desc[t] + 2 * kk, ring_k + kslot * kSlotStep + 2 * kk,
-                        idesc_mxf8(128, 128, false, kk, kk), kk > 0 ? 1u : 0u, tmem + sf_cols, tmem + sf_cols + 4);
+            mma_mxf8_ss_lo(tmem + C::col_s(t), q_desc[t] + 2 * kk, ring_k + kslot * kSlotStep + 2 * kk, desc_hi,
+                           idesc_mxf8(128, 128, false, kk, kk), kk > 0 ? 1u : 0u, tmem + sf_cols, tmem + sf_cols + 4);
         }
       };
       // O_t += P_t V from ring slot vslot; P_t and its scales in S_t, V's scales copied beside them
@@ -222,9 +254,9 @@ __global__ void __launch_bounds__(384, 1)
           sf_copy_to_tmem(s_cols + C::kVScale, slot_atom(vslot));
 #pragma unroll
           for (uint32_t kk = 0; kk < 4; ++kk)
-            mma_mxf8_ts(tmem + C::col_o(t), s_cols + 8 * kk, ring_v + vslot * kSlotStep + 256 * kk,
-                        idesc_mxf8(128, 128, true, kk, kk), (!first || kk > 0) ? 1u : 0u, s_cols + C::kPScale,
-                        s_cols + C::kVScale);
+            mma_mxf8_ts_lo(tmem + C::col_o(t), s_cols + 8 * kk, ring_v + vslot * kSlotStep + 256 * kk, desc_hi,
+                           idesc_mxf8(128, 128, true, kk, kk), (!first || kk > 0) ? 1u : 0u, s_cols + C::kPScale,
+                           s_cols + C::kVScale);
         }
       };
       auto advance2 = [](uint32_t& slot, uint32_t& phase) {
@@ -234,57 +266,95 @@ __global__ void __launch_bounds__(384, 1)
           phase ^= 1u;
         }
       };
+      // ring positions and barrier phases continue across items
       uint32_t ks = 0, kph = 0;  // K_j
       uint32_t vs = 1, vph = 0;  // V_j
-      bool ok = wait(bar_q, 0, 2) && wait(bar_full(ks), kph, 3);
-      if (ok) {
+      uint32_t gb0 = 0, gb1 = 0;  // blocks of tile 0 / tile 1 before this item
+      bool ok = true;
+      int qi = 0;
+      for (int it = item_of(0); ok && it < total_items; it = item_of(++qi)) {
+        int bh, pair;
+        coords(it, bh, pair);
+        (void)bh;
+        const int n0 = blocks_of(pair, 0);
+        const int n1 = blocks_of(pair, 1);
+        ok = wait(bar_q, qi & 1, 2) && wait(bar_full(ks), kph, 3);
+        if (!ok) break;
         tc_fence_after();
-        // first S GEMMs: scales in the O regions, which no MMA has written yet
-        issue_s(0, ks, C::col_o(0));
-        commit(bar_s(0));
-        issue_s(1, ks, C::col_o(1));
-        commit(bar_s(1));
-        commit(bar_empty(ks));
-      }
-      for (int j = 0; ok && j < n1; ++j) {
-        if (!wait(bar_full(vs), vph, 4)) break;
-        uint32_t ks_next = ks, kph_next = kph;
-        advance2(ks_next, kph_next);
-        bool k_next_ready = false;
-        if (j < n0) {
-          if (!wait(bar_p(0), j & 1, 5)) break;
-          tc_fence_after();
-          issue_pv(0, vs, j == 0);
-          if (j + 1 < n0) {
-            // S0(j+1)'s scales go into S1's columns 40-47: S1(j) must be loaded
-            if (!wait(bar_full(ks_next), kph_next, 6) || !wait(bar_ld(1), j & 1, 9)) break;
-            k_next_ready = true;
-            tc_fence_after();
-            issue_s(0, ks_next, C::col_s(1) + C::kQScale);
-            commit(bar_s(0));
-          } else {
-            commit(bar_o(0));
-          }
-        }
-        if (!wait(bar_p(1), j & 1, 7)) break;
-        tc_fence_after();
-        issue_pv(1, vs, j == 0);
-        commit(bar_empty(vs));
-        if (j + 1 < n1) {
-          if (!k_next_ready && !wait(bar_full(ks_next), kph_next, 8)) break;
-          // S1(j+1)'s scales go into S0's columns 40-47: if tile 0 has block
-          // j+1, its scores there must have been loaded first
-          if (j + 1 < n0 && !wait(bar_ld(0), (j + 1) & 1, 10)) break;
-          tc_fence_after();
-          issue_s(1, ks_next, C::col_s(0) + C::kQScale);
+        if (qi == 0) {
+          // first S GEMMs of the CTA: scales in the O regions, which no MMA has written yet
+          issue_s(0, ks, C::col_o(0));
+          commit(bar_s(0));
+          issue_s(1, ks, C::col_o(1));
           commit(bar_s(1));
-          commit(bar_empty(ks_next));
         } else {
-          commit(bar_o(1));
+          // S1's columns 40-47 are free (its last scores were loaded before its last P)
+          issue_s(0, ks, C::col_s(1) + C::kQScale);
+          commit(bar_s(0));
+          // S1(0)'s scales go into O1 once the previous item's O1 has been read
+          ok = wait(bar_oread(1), (qi - 1) & 1, 14);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(1, ks, C::col_o(1));
+          commit(bar_s(1));
         }
-        ks = ks_next;
-        kph = kph_next;
-        advance2(vs, vph);
+        commit(bar_empty(ks));
+        if (n1 == 1) commit(bar_qe);  // this item's S GEMMs are all issued
+        for (int j = 0; ok && j < n1; ++j) {
+          if (!wait(bar_full(vs), vph, 4)) {
+            ok = false;
+            break;
+          }
+          uint32_t ks_next = ks, kph_next = kph;
+          advance2(ks_next, kph_next);
+          bool k_next_ready = false;
+          if (j < n0) {
+            ok = wait(bar_p(0), (gb0 + j) & 1, 5);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(0, vs, j == 0);
+            if (j + 1 < n0) {
+              // S0(j+1)'s scales go into S1's columns 40-47: S1(j) must be loaded
+              ok = wait(bar_full(ks_next), kph_next, 6) && wait(bar_ld(1), (gb1 + j) & 1, 9);
+              if (!ok) break;
+              k_next_ready = true;
+              tc_fence_after();
+              issue_s(0, ks_next, C::col_s(1) + C::kQScale);
+              commit(bar_s(0));
+            } else {
+              commit(bar_o(0));
+            }
+          }
+          ok = wait(bar_p(1), (gb1 + j) & 1, 7);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(1, vs, j == 0);
+          commit(bar_empty(vs));
+          if (j + 1 < n1) {
+            if (!k_next_ready) {
+              ok = wait(bar_full(ks_next), kph_next, 8);
+              if (!ok) break;
+            }
+            // S1(j+1)'s scales go into S0's columns 40-47: if tile 0 has block
+            // j+1, its scores there must have been loaded first
+            if (j + 1 < n0) {
+              ok = wait(bar_ld(0), (gb0 + j + 1) & 1, 10);
+              if (!ok) break;
+            }
+            tc_fence_after();
+            issue_s(1, ks_next, C::col_s(0) + C::kQScale);
+            commit(bar_s(1));
+            commit(bar_empty(ks_next));
+            if (j + 2 == n1) commit(bar_qe);  // that was this item's last S GEMM
+          } else {
+            commit(bar_o(1));
+          }
+          ks = ks_next;
+          kph = kph_next;
+          advance2(vs, vph);
+        }
+        gb0 += n0;
+        gb1 += n1;
       }
       commit(bar_drain);
       drain_bar(bar_drain, 0);
@@ -296,19 +366,24 @@ __global__ void __launch_bounds__(384, 1)
     const int t = warp >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const int tile_row0 = row0 + 128 * t;
-    const int grow = tile_row0 + r;
-    const int nt = t ? n1 : n0;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_tm = tmem + lane_off + C::col_s(t);
     const uint32_t o_tm = tmem + lane_off + C::col_o(t);
     const float sl2 = args.scale_log2;
     const float2 sl2_2 = make_float2(sl2, sl2);
+    bool ok = true;
+    uint32_t gb = 0;  // this tile's blocks before the current item (barrier phases)
+    int qi = 0;
+    for (int it = item_of(0); ok && it < total_items; it = item_of(++qi)) {
+    int bh, pair;
+    coords(it, bh, pair);
+    const int tile_row0 = pair * 256 + 128 * t;
+    const int grow = tile_row0 + r;
+    const int nt = blocks_of(pair, t);
     float m = -INFINITY;
     float l = 0.f;
-    bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      ok = __all_sync(0xffffffffu, wait_bar(bar_s(t), j & 1, abort_flag, args.status, 16 + t));
+      ok = __all_sync(0xffffffffu, wait_bar(bar_s(t), (gb + j) & 1, abort_flag, args.status, 16 + t));
       if (!ok) break;
       tc_fence_after();
       float2 s[64];
@@ -360,10 +435,10 @@ __global__ void __launch_bounds__(384, 1)
       const float corr = fire ? (m == -INFINITY ? 0.f : ex2_mufu((m - m_new) * sl2)) : 1.0f;
       m = m_new;
       const float neg_ms = (m == -INFINITY) ? 0.f : -(m * sl2);
+      float lsum = 0.f;
       // P per 32-key block: E8M0 scale from one exp of the block max; P / 2^e
       // = 2^(x - e), so the scale rides in the exp's shift; the fp32 row sum
-      // takes each block's sum times 2^e
-      float lsum = 0.f;
+      // takes each block's P / 2^e times 2^e
       uint32_t pk[32];
       uint32_t sfw = 0;
 #pragma unroll
@@ -372,7 +447,6 @@ __global__ void __launch_bounds__(384, 1)
         sfw |= sfb << (8 * g);
         const float shift = neg_ms - static_cast<float>(static_cast<int>(sfb) - 127);
         const float2 shift_2 = make_float2(shift, shift);
-        // four accumulators: short chains for the long-latency packed add
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
@@ -392,7 +466,7 @@ __global__ void __launch_bounds__(384, 1)
           pk[8 * g + i / 2] = pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
         }
         acc[0] = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-        lsum = __fmaf_rn(acc[0].x + acc[0].y, __uint_as_float(sfb << 23), lsum);  // * 2^(sfb - 127)
+        lsum = __fmaf_rn(acc[0].x + acc[0].y, __uint_as_float(sfb << 23), lsum);
       }
       tmem_st32(s_tm, pk);                      // P, 4 keys per column
       tmem_st1(s_tm + C::kPScale + quad, sfw);  // row r's scales at column r / 32
@@ -419,34 +493,44 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(bar_p(t));
     }
-    if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar_o(t), 0, abort_flag, args.status, 18 + t));
+    if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar_o(t), qi & 1, abort_flag, args.status, 18 + t));
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
       const bool valid = grow < args.n;
       __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * args.n + (valid ? grow : 0)) * 128;
       const float2 inv_l_2 = make_float2(inv_l, inv_l);
+      // all of O_t into registers first: the next item's S1 GEMM may then put
+      // its scale factors into O1
+      uint32_t ob[4][32];
 #pragma unroll
-      for (int c = 0; c < 128; c += 32) {
-        uint32_t ob[32];
-        tmem_ld32(o_tm + c, ob);
-        tmem_ld_wait();
-        reg_fence32(ob);
+      for (int c = 0; c < 4; ++c) tmem_ld32(o_tm + 32 * c, ob[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(bar_oread(t));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        reg_fence32(ob[c]);
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(ob[2 * i]), __uint_as_float(ob[2 * i + 1])), inv_l_2);
+          const float2 o2 =
+              __fmul2_rn(make_float2(__uint_as_float(ob[c][2 * i]), __uint_as_float(ob[c][2 * i + 1])), inv_l_2);
           w[i] = pack_bf16x2(o2.x, o2.y);
         }
         if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c);
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
           for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
         }
       }
       if (valid) args.lse[static_cast<size_t>(bh) * args.n + grow] = (m * sl2 + lg2_mufu(l)) * 0.69314718055994531f;
     }
+    // the next item's O GEMMs overwrite O_t only after this warpgroup's next
+    // P is ready, i.e. after these reads
     tc_fence_before();
+    gb += nt;
+    }
   }
 
   __syncthreads();
@@ -458,7 +542,7 @@ __global__ void __launch_bounds__(384, 1)
 
 template <bool CAUSAL, int EMU>
 cudaError_t launch_fwd_mxfp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                             const FwdMxArgs& args, cudaStream_t stream) {
+                             const FwdMxArgs& args, const WorkList& wl, int ctas, cudaStream_t stream) {
   auto kernel = attn_fwd_mxfp8_kernel<CAUSAL, EMU>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MxCfg::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -467,8 +551,7 @@ cudaError_t launch_fwd_mxfp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, c
   e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < MxCfg::kLaunchRegs) return cudaErrorInvalidConfiguration;
-  const long long ctas = static_cast<long long>(args.bh) * args.n_pairs;
-  kernel<<<static_cast<unsigned>(ctas), MxCfg::kThreads, MxCfg::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, args);
+  kernel<<<static_cast<unsigned>(ctas), MxCfg::kThreads, MxCfg::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, args, wl);
   return cudaGetLastError();
 }
 

@@ -97,6 +97,28 @@ __device__ __forceinline__ void mma_mxf8_ts(uint32_t d, uint32_t a, uint64_t b, 
       : "memory");
 }
 
+// The same two MMAs with each shared-memory descriptor given as its low word
+// and a high word common to both operands (only the low words change from one
+// MMA to the next).
+__device__ __forceinline__ void mma_mxf8_ss_lo(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t desc_hi,
+                                               uint32_t idesc, uint32_t acc, uint32_t sfa, uint32_t sfb) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 ad, {%1, %3};\n\tmov.b64 bd, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], ad, bd, %4, [%6], [%7], p;\n\t}" ::"r"(d),
+      "r"(a_lo), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+__device__ __forceinline__ void mma_mxf8_ts_lo(uint32_t d, uint32_t a, uint32_t b_lo, uint32_t desc_hi,
+                                               uint32_t idesc, uint32_t acc, uint32_t sfa, uint32_t sfb) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 bd, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], bd, %4, [%6], [%7], p;\n\t}" ::"r"(d),
+      "r"(a), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+
 // Bulk copy of `bytes` (multiple of 16, 16-byte aligned both sides) global ->
 // shared, completing on an mbarrier's transaction count.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
