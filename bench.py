@@ -47,7 +47,8 @@ KERNEL_SOURCES = {
              "online_softmax_fwd_gb300/csrc/schedule.cu"],
     "mxfp8": ["online_softmax_fwd_gb300/csrc/fwd_mxfp8.cuh", "online_softmax_fwd_gb300/csrc/mxfp8_common.cuh",
               "online_softmax_fwd_gb300/csrc/fwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/ptx.cuh",
-              "online_softmax_fwd_gb300/csrc/exp2_fma.cuh"],
+              "online_softmax_fwd_gb300/csrc/exp2_fma.cuh", "online_softmax_fwd_gb300/csrc/schedule.h",
+              "online_softmax_fwd_gb300/csrc/schedule.cu"],
 }
 
 
