@@ -1,7 +1,7 @@
 """Benchmark of the fused attention forward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference] [--exp2-emu16 E] [--tau T]
+                    [--impl ours|reference] [--exp2-emu16 E] [--tau T] [--p-scaling 0|1]
 
 A step is one attention forward (O and LSE) over the whole workload, inputs
 resident in HBM (Q, K, V together exceed the 129 MB L2, so no flush is
@@ -349,7 +349,8 @@ class Mxfp8Step:
         st = L.attn_fwd_mxfp8_ex(self.codes[0].data_ptr(), self.sf[0].data_ptr(), self.codes[1].data_ptr(),
                                  self.sf[1].data_ptr(), self.codes[2].data_ptr(), self.sf[2].data_ptr(),
                                  self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N, w.d, int(w.causal),
-                                 float(w.scale), float(self.tau), int(self.args.exp2_emu16), sh)
+                                 float(w.scale), float(self.tau), int(self.args.exp2_emu16),
+                                 int(self.args.p_scaling), sh)
         if ev:
             ev[1].record()
         if st != 0:
@@ -452,7 +453,9 @@ def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
                "data": "synthetic",
                "config": {**w.describe(), "parallelism": f"replicas{world}" if world > 1 else "single",
                           "l2": f"inputs larger than L2 ({step.input_bytes() / 2**20:.0f} MiB > 129 MB)",
-                          "tau": step.tau if w.dtype == "mxfp8" else args.tau, "exp2_emu16": args.exp2_emu16},
+                          "tau": step.tau if w.dtype == "mxfp8" else args.tau, "exp2_emu16": args.exp2_emu16,
+                          **({"p_scaling": ["block_amax", "constant_2^-8"][args.p_scaling]}
+                             if w.dtype == "mxfp8" else {})},
                "e2e": e2e, "gpu_launches": args.steps * step.launches, "roofline": roofline, "cpu_baseline": cpu,
                "clocks": clocks, "kernel_ms": {"mean": float(np.mean(launch_ms)), "min": float(np.min(launch_ms)),
                                                "max": float(np.max(launch_ms))}}
@@ -479,6 +482,8 @@ def main() -> None:
     ap.add_argument("--exp2-emu16", type=int, default=0)
     ap.add_argument("--tau", type=float, default=None,
                     help="rescale threshold (default 8 for bf16 P, 0 for FP8 P)")
+    ap.add_argument("--p-scaling", type=int, default=0, choices=[0, 1],
+                    help="MXFP8 P scale: 0 one per 32 keys from the block amax, 1 the constant 2^-8")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--no-e2e", action="store_true")

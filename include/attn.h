@@ -166,11 +166,25 @@ attn_status_t attn_fwd_mxfp8(const void* q8, const void* q_sf, const void* k8, c
                              const void* v_sf, void* o, float* lse, int B, int H, int N, int d, int causal,
                              float scale, void* stream);
 
-/* attn_fwd_mxfp8 with tau in [0, 16] and a software-exp2 share of 0, 2 or 4
- * of every 16 score columns (others: ATTN_ERR_UNSUPPORTED). */
+/* How attn_fwd_mxfp8_ex scales P before converting it to E4M3. */
+enum {
+  /* one E8M0 scale per 32 keys of a row, from the group's largest P (the
+   * exp of its largest score): the conversion attn_fwd_mxfp8 uses */
+  ATTN_P_SCALE_BLOCK_AMAX = 0,
+  /* the constant 2^-8 ("PyTorch FlashAttention-4 adds MXFP8 block-scaled
+   * forward and backward for Blackwell", section "Softmax conversion and
+   * unroll-KV": softmax keeps P in [0, 1], so a fixed scale is robust): P = 1
+   * maps to 256; needs tau <= log2(448 / 256) ~ 0.807 so that 2^tau * 256
+   * stays within E4M3 (else ATTN_ERR_INVALID_ARG) */
+  ATTN_P_SCALE_CONSTANT = 1
+};
+
+/* attn_fwd_mxfp8 with tau in [0, 16], a software-exp2 share of 0, 2 or 4 of
+ * every 16 score columns (others: ATTN_ERR_UNSUPPORTED) and p_scaling one of
+ * ATTN_P_SCALE_* (else ATTN_ERR_INVALID_ARG). */
 attn_status_t attn_fwd_mxfp8_ex(const void* q8, const void* q_sf, const void* k8, const void* k_sf, const void* v8,
                                 const void* v_sf, void* o, float* lse, int B, int H, int N, int d, int causal,
-                                float scale, float tau, int exp2_emu16, void* stream);
+                                float scale, float tau, int exp2_emu16, int p_scaling, void* stream);
 
 /*
  * attn_exp2_emulated -- y[i] = software exp2 of x[i] for i < n, computed by

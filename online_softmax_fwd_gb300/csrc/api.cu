@@ -23,6 +23,8 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr long long kMaxN = 1LL << 24;
+// log2(448 / 256), rounded down: the largest tau for which P * 2^8 <= 448
+constexpr float kPConstMaxTau = 0.807f;
 
 // Device error word, one per device (each device holds its own copy).
 __device__ unsigned int g_attn_status;
@@ -212,13 +214,16 @@ attn_status_t attn_mxfp8_quantize(const float* x, void* x_e4m3, void* x_scales, 
 
 attn_status_t attn_fwd_mxfp8_ex(const void* q8, const void* q_sf, const void* k8, const void* k_sf, const void* v8,
                                 const void* v_sf, void* o, float* lse, int B, int H, int N, int d, int causal,
-                                float scale, float tau, int exp2_emu16, void* stream) {
+                                float scale, float tau, int exp2_emu16, int p_scaling, void* stream) {
   if (B < 0 || H < 0 || N < 0 || (causal != 0 && causal != 1)) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(tau) || tau < 0.f || tau > 16.f) return ATTN_ERR_INVALID_ARG;
   if (d != 128) return d > 0 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
   if (exp2_emu16 < 0 || exp2_emu16 > 16) return ATTN_ERR_INVALID_ARG;
   if (exp2_emu16 != 0 && exp2_emu16 != 2 && exp2_emu16 != 4) return ATTN_ERR_UNSUPPORTED;
+  if (p_scaling != ATTN_P_SCALE_BLOCK_AMAX && p_scaling != ATTN_P_SCALE_CONSTANT) return ATTN_ERR_INVALID_ARG;
+  // constant 2^-8: the largest P, 2^tau, must stay within E4M3's 448 / 256
+  if (p_scaling == ATTN_P_SCALE_CONSTANT && !(tau <= kPConstMaxTau)) return ATTN_ERR_INVALID_ARG;
   if (N > kMaxN || static_cast<long long>(B) * H * ((N + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
   if (!q8 || !q_sf || !k8 || !k_sf || !v8 || !v_sf || !o || !lse) return ATTN_ERR_INVALID_ARG;
@@ -257,8 +262,10 @@ attn_status_t attn_fwd_mxfp8_ex(const void* q8, const void* q_sf, const void* k8
     std::memset(&wl, 0, sizeof(wl));
     ctas = static_cast<int>(std::min<long long>(items, sms));
   }
-  cudaError_t e =
-      attn::launch_fwd_mxfp8_d128(causal, exp2_emu16, mq, mk, mv, a, wl, ctas, static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = p_scaling == ATTN_P_SCALE_CONSTANT
+                      ? attn::launch_fwd_mxfp8_d128_pconst(causal, exp2_emu16, mq, mk, mv, a, wl, ctas, st)
+                      : attn::launch_fwd_mxfp8_d128(causal, exp2_emu16, mq, mk, mv, a, wl, ctas, st);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -268,7 +275,8 @@ attn_status_t attn_fwd_mxfp8(const void* q8, const void* q_sf, const void* k8, c
   // tau = 0 for FP8 P: with a stale max a row's largest P is 2^delta instead of
   // exactly 1 and E4M3 rounds it by up to 2^-4 (FlashAttention-4's Softmax
   // Tricks, "Where exact breaks: P in FP8": tau 8 for 16-bit P, 0 for FP8)
-  return attn_fwd_mxfp8_ex(q8, q_sf, k8, k_sf, v8, v_sf, o, lse, B, H, N, d, causal, scale, 0.0f, 0, stream);
+  return attn_fwd_mxfp8_ex(q8, q_sf, k8, k_sf, v8, v_sf, o, lse, B, H, N, d, causal, scale, 0.0f, 0,
+                           ATTN_P_SCALE_BLOCK_AMAX, stream);
 }
 
 attn_status_t attn_exp2_emulated(const float* x, float* y, long long n, void* stream) {

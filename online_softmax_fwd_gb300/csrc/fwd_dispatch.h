@@ -24,6 +24,9 @@ cudaError_t launch_fwd_bf16_d128_c1(int emu16, const CUtensorMap& q, const CUten
 cudaError_t launch_fwd_mxfp8_d128(int causal, int emu16, const CUtensorMap& q, const CUtensorMap& k,
                                   const CUtensorMap& v, const FwdMxArgs& a, const WorkList& wl, int ctas,
                                   cudaStream_t s);
+cudaError_t launch_fwd_mxfp8_d128_pconst(int causal, int emu16, const CUtensorMap& q, const CUtensorMap& k,
+                                         const CUtensorMap& v, const FwdMxArgs& a, const WorkList& wl, int ctas,
+                                         cudaStream_t s);
 cudaError_t launch_mxfp8_quantize(const float* x, uint8_t* q, uint8_t* atoms, long long bh, int n, int role,
                                   cudaStream_t stream);
 

@@ -89,7 +89,11 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
 
-template <bool CAUSAL, int EMU>
+// PCONST: P's scale is the constant 2^-8 (E8M0 byte 119) instead of one per
+// 32 keys from the block amax (same page, same section: constant scaling of P
+// stays robust because softmax keeps P in [0, 1]; with a stale maximum P
+// reaches 2^tau, so 256 * 2^tau <= 448 needs tau <= log2(1.75)).
+template <bool CAUSAL, int EMU, bool PCONST>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_mxfp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const FwdMxArgs args,
@@ -443,7 +447,7 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t sfw = 0;
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        const uint32_t sfb = e8m0_for_amax(ex2_mufu(__fmaf_rn(bmx[g], sl2, neg_ms)));
+        const uint32_t sfb = PCONST ? 119u : e8m0_for_amax(ex2_mufu(__fmaf_rn(bmx[g], sl2, neg_ms)));
         sfw |= sfb << (8 * g);
         const float shift = neg_ms - static_cast<float>(static_cast<int>(sfb) - 127);
         const float2 shift_2 = make_float2(shift, shift);
@@ -540,10 +544,10 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <bool CAUSAL, int EMU>
+template <bool CAUSAL, int EMU, bool PCONST>
 cudaError_t launch_fwd_mxfp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const FwdMxArgs& args, const WorkList& wl, int ctas, cudaStream_t stream) {
-  auto kernel = attn_fwd_mxfp8_kernel<CAUSAL, EMU>;
+  auto kernel = attn_fwd_mxfp8_kernel<CAUSAL, EMU, PCONST>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MxCfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   // the setmaxnreg split must fit the registers the CTA is launched with

@@ -15,7 +15,9 @@ The same page, section "Softmax conversion and unroll-KV", converts P (the
 probabilities, all in [0, 1]) to MXFP8 inside the kernel for the P V product,
 one E8M0 scale per 32 consecutive keys of a row: ``p_to_mxfp8`` applies the
 same scale rule to each such group of a row (the group's amax is the largest
-P in it).
+P in it). The same section notes that a constant scale for P also works,
+since softmax keeps P in [0, 1]: ``p_to_mxfp8_constant`` divides every P by
+2^-8 (P = 1 lands on 256, inside E4M3's 448) and rounds it to E4M3.
 
 E4M3 (the OCP "E4M3FN" encoding): 1 sign bit, 4 exponent bits with bias 7,
 3 mantissa bits; exponent field 0 encodes subnormals m * 2^-9; the code
@@ -109,3 +111,14 @@ def p_to_mxfp8(p: np.ndarray) -> np.ndarray:
         scale = np.exp2(e8m0_exponent(np.abs(run).max(axis=-1)).astype(np.float64))[..., None]
         out[..., g0:g0 + BLOCK] = e4m3_decode(e4m3_encode(run / scale)) * scale
     return out
+
+
+P_CONST_EXP = -8
+
+
+def p_to_mxfp8_constant(p: np.ndarray) -> np.ndarray:
+    """Values of P after conversion to E4M3 with the constant scale 2^-8
+    (float64): P / 2^-8 rounded to E4M3 (nearest even, saturating at 448),
+    times 2^-8."""
+    scale = 2.0 ** P_CONST_EXP
+    return e4m3_decode(e4m3_encode(np.asarray(p, dtype=np.float64) / scale)) * scale

@@ -90,14 +90,16 @@ def run_mxfp8(attn, w_causal, x_q, x_k, x_v, scale, **kw):
     return o.cpu(), lse.cpu()
 
 
-def mx_reference(xq, xk, xv, causal, scale, rows=None, tau=0.0):
+def mx_reference(xq, xk, xv, causal, scale, rows=None, tau=0.0, p_scaling=0):
     """The MXFP8 method in float64 for one head ([N, 128] fp32 inputs): Q, K, V
-    quantised by the oracle's quantiser, P converted per 32 keys; rows = the
-    query positions to compute (default all)."""
+    quantised by the oracle's quantiser, P converted per 32 keys (p_scaling 0)
+    or with the constant scale (1); rows = the query positions to compute
+    (default all)."""
     dq, dk, dv = (M.quantize_blocks(x)[2] for x in (xq, xk, xv))
     if rows is None:
         rows = np.arange(dq.shape[0])
-    o, lse, _ = blockwise_attention(dq[rows], dk, dv, causal, scale, tau=tau, p_cast=M.p_to_mxfp8, row_index=rows)
+    p_cast = M.p_to_mxfp8_constant if p_scaling else M.p_to_mxfp8
+    o, lse, _ = blockwise_attention(dq[rows], dk, dv, causal, scale, tau=tau, p_cast=p_cast, row_index=rows)
     return o, lse
 
 
@@ -113,17 +115,28 @@ def check(o, lse, o_ref, lse_ref, what):
     return err.max(), err.mean()
 
 
+@pytest.mark.parametrize("p_scaling", [0, 1], ids=["p_block_amax", "p_constant"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shape", [(1, 1, 128), (1, 2, 256), (2, 1, 300), (1, 2, 1000), (1, 1, 1024)],
                          ids=lambda s: "x".join(map(str, s)))
-def test_small_shapes(attn, shape, causal):
+def test_small_shapes(attn, shape, causal, p_scaling):
     B, H, N = shape
     xq, xk, xv = I.draw_fp32(B, H, N, 128, seed=N + 7)
-    o, lse = run_mxfp8(attn, causal, xq, xk, xv, 128 ** -0.5)
+    o, lse = run_mxfp8(attn, causal, xq, xk, xv, 128 ** -0.5, p_scaling=p_scaling)
     for b in range(B):
         for h in range(H):
-            o_ref, lse_ref = mx_reference(xq[b, h], xk[b, h], xv[b, h], causal, 128 ** -0.5)
-            check(o[b, h], lse[b, h], o_ref, lse_ref, f"{shape} causal={causal} b={b} h={h}")
+            o_ref, lse_ref = mx_reference(xq[b, h], xk[b, h], xv[b, h], causal, 128 ** -0.5, p_scaling=p_scaling)
+            check(o[b, h], lse[b, h], o_ref, lse_ref, f"{shape} causal={causal} b={b} h={h} p={p_scaling}")
+
+
+def test_constant_p_scale_with_largest_allowed_tau(attn):
+    # tau = 0.8: a stale maximum lets P reach 2^0.8 ~ 1.74, i.e. 446 after the
+    # constant scale, still inside E4M3 -- the peaked rows exercise it
+    (xq, xk, xv), _ = peaked_case()
+    o, lse = run_mxfp8(attn, True, xq, xk, xv, 128 ** -0.5, tau=0.8, p_scaling=1)
+    for h in range(2):
+        o_ref, lse_ref = mx_reference(xq[0, h], xk[0, h], xv[0, h], True, 128 ** -0.5, tau=0.8, p_scaling=1)
+        check(o[0, h], lse[0, h], o_ref, lse_ref, f"tau=0.8 constant P scale h={h}")
 
 
 # Persistent CTAs: up to 8192 (head, Q-tile pair) items follow a host-built
@@ -181,13 +194,15 @@ def test_lagging_max_costs_accuracy_with_fp8_p(attn):
     assert np.abs(lse8.double().numpy() - lse_ref).max() <= LSE_MAX_ABS  # LSE comes from fp32 P either way
 
 
-def test_full_size_workload_sampled(attn):
+@pytest.mark.parametrize("p_scaling", [0, 1], ids=["p_block_amax", "p_constant"])
+def test_full_size_workload_sampled(attn, p_scaling):
     w = I.MXFP8_CAUSAL
     xq, xk, xv = I.draw_fp32(w.B, w.H, w.N, w.d, w.qk_std, w.v_std, w.seed)
-    o, lse = run_mxfp8(attn, w.causal, xq, xk, xv, w.scale)
+    o, lse = run_mxfp8(attn, w.causal, xq, xk, xv, w.scale, p_scaling=p_scaling)
     assert torch.isfinite(lse).all()
     rng = np.random.default_rng(3)
     for b, h in ((0, 0), (w.B - 1, w.H - 1), (int(rng.integers(w.B)), int(rng.integers(w.H)))):
         rows = sample_rows(w.N, rng)
-        o_ref, lse_ref = mx_reference(xq[b, h], xk[b, h], xv[b, h], w.causal, w.scale, rows=rows)
+        o_ref, lse_ref = mx_reference(xq[b, h], xk[b, h], xv[b, h], w.causal, w.scale, rows=rows,
+                                      p_scaling=p_scaling)
         check(o[b, h, rows], lse[b, h, rows], o_ref, lse_ref, f"{w.name} b={b} h={h}")

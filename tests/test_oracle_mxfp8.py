@@ -123,3 +123,18 @@ def test_p_relative_error_and_run_boundaries():
     q[:, 32:64] *= 1e-4
     got_q = M.p_to_mxfp8(q)
     assert np.array_equal(got_q[:, :32], got[:, :32]) and np.array_equal(got_q[:, 64:], got[:, 64:])
+
+
+def test_p_constant_scale_conversion():
+    # P in [0, 1.75] with the constant scale 2^-8: every E4M3 value times
+    # 2^-8 is kept, everything else goes to the nearest one (brute force), and
+    # nothing saturates below 448 / 256
+    grid = M.e4m3_decode(np.arange(0x00, 0x7F)) * 2.0 ** -8
+    keep = grid[grid <= 1.75]
+    assert np.array_equal(M.p_to_mxfp8_constant(keep), keep)
+    rng = np.random.default_rng(8)
+    p = np.concatenate([rng.uniform(0, 1.75, 5000), np.exp2(-rng.uniform(0, 20, 5000))])
+    want = grid[np.abs(p[:, None] - grid[None, :]).argmin(axis=1)]
+    assert np.array_equal(M.p_to_mxfp8_constant(p), want)
+    assert M.p_to_mxfp8_constant(np.array([1.0]))[0] == 1.0
+    assert M.p_to_mxfp8_constant(np.array([2.0]))[0] == 1.75   # saturates at 448 * 2^-8
