@@ -561,6 +561,8 @@ __global__ void __launch_bounds__(384, 1)
       const float l = l2.x + l2.y;
       const float inv_l = 1.0f / l;
       const bool valid = grow < args.n;
+      // rows are 128 or 256 bytes: 32-byte alignment of O decides the store width for all of them
+      const bool o_aligned32 = (reinterpret_cast<uintptr_t>(args.o) & 31u) == 0;
       __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * args.n + (valid ? grow : 0)) * D;
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
@@ -575,11 +577,7 @@ __global__ void __launch_bounds__(384, 1)
           const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(ob[2 * i]), __uint_as_float(ob[2 * i + 1])), inv_l_2);
           pk[i] = pack_bf16x2(o2.x, o2.y);
         }
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-        }
+        if (valid) store_row64(orow + c, pk, o_aligned32);
       }
       if (valid) args.lse[static_cast<size_t>(bh) * args.n + grow] = (m * sl2 + lg2_mufu(l)) * 0.69314718055994531f;
     }

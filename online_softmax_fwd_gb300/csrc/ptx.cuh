@@ -138,6 +138,24 @@ __device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// 64 bytes of a row to global memory: two 256-bit stores when the address is
+// 32-byte aligned (each thread then writes whole 32-byte sectors), else four
+// 128-bit stores.
+__device__ __forceinline__ void store_row64(void* dst, const uint32_t (&w)[16], bool aligned32) {
+  if (aligned32) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(static_cast<uint8_t*>(dst) + 32 * h),
+                   "r"(w[8 * h]), "r"(w[8 * h + 1]), "r"(w[8 * h + 2]), "r"(w[8 * h + 3]), "r"(w[8 * h + 4]),
+                   "r"(w[8 * h + 5]), "r"(w[8 * h + 6]), "r"(w[8 * h + 7])
+                   : "memory");
+  } else {
+    uint4* d = static_cast<uint4*>(dst);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) d[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+  }
+}
+
 // TMEM -> registers, 32 lanes x 32 consecutive 32-bit columns (one column
 // per register). The values are valid only after tmem_ld_wait(); pass them
 // through reg_fence32() after the wait so no use is scheduled before it.

@@ -139,6 +139,25 @@ def test_every_work_item_once(attn, shape, causal):
     compare(I.as_f64(o.cpu()), lse.cpu().double().numpy(), o_ref, lse_ref, f"{shape} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_output_only_16_byte_aligned(attn, d):
+    # O 16-byte but not 32-byte aligned: the epilogue falls back from 256-bit
+    # to 128-bit stores; both must write the same rows
+    B, H, N = 1, 2, 300
+    q, k, v = (I.to_bf16(x) for x in I.draw_fp32(B, H, N, d, seed=d + 5))
+    n = B * H * N * d
+    buf = torch.full((n + 16,), float("nan"), dtype=torch.bfloat16, device=DEV)
+    o = buf[8:8 + n].view(B, H, N, d)
+    assert o.data_ptr() % 32 == 16
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=DEV)
+    attn.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, scale=d ** -0.5, o=o, lse=lse)
+    torch.cuda.synchronize()
+    assert attn.device_status() == attn.Status.OK
+    assert torch.isnan(buf[:8]).all() and torch.isnan(buf[8 + n:]).all()   # nothing written outside O
+    o_ref, lse_ref = attention_fwd(I.as_f64(q), I.as_f64(k), I.as_f64(v), True, d ** -0.5)
+    compare(I.as_f64(o.cpu()), lse.cpu().double().numpy(), o_ref, lse_ref, f"misaligned O d={d}")
+
+
 def test_repeat_calls_are_identical(attn):
     q, k, v = (I.to_bf16(x).to(DEV) for x in I.draw_fp32(2, 2, 777, 128, seed=17))
     o1, l1 = attn.attn_fwd(q, k, v, causal=True)
