@@ -18,56 +18,46 @@
 
 namespace attn {
 
+// One CTA per (128-row tile, head), 8 warps; warp w takes rows 16w .. 16w+15
+// and lane l columns 4l .. 4l+3 of each, so every load and store of a warp
+// covers one whole row (512 bytes in, 128 bytes out).
 __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const float* __restrict__ x, uint8_t* __restrict__ q,
                                                              uint8_t* __restrict__ atoms, int n, int ntiles,
                                                              int role) {
-  __shared__ float row_amax[128][4];
-  __shared__ uint32_t eb[4][4];  // [row block][d block] E8M0 bytes
+  __shared__ float part_amax[8][4];  // [warp][d block]: amax over the warp's 16 rows
+  __shared__ uint32_t eb[4][4];      // [row block][d block] E8M0 bytes
   const int tid = threadIdx.x;
-  const int r = tid >> 1;        // row within the tile
-  const int h = tid & 1;         // columns [64h, 64h + 64)
+  const int warp = tid >> 5, lane = tid & 31;
   const int tile = blockIdx.x;
   const long long bh = blockIdx.y;
-  const int row = tile * 128 + r;
-  const bool valid = row < n;
-  float v[64];
-  const float4* src = reinterpret_cast<const float4*>(x + ((bh * n + (valid ? row : 0)) * 128 + 64 * h));
+  const int row0 = tile * 128 + 16 * warp;
+  float4 v[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const float4 f = valid ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-    v[4 * i] = f.x;
-    v[4 * i + 1] = f.y;
-    v[4 * i + 2] = f.z;
-    v[4 * i + 3] = f.w;
+    const int row = row0 + i;
+    v[i] = row < n ? reinterpret_cast<const float4*>(x + (bh * n + row) * 128)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  float a0 = 0.f, a1 = 0.f;
+  float a = 0.f;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    a0 = fmaxf(a0, fabsf(v[i]));
-    a1 = fmaxf(a1, fabsf(v[32 + i]));
-  }
-  row_amax[r][2 * h] = a0;
-  row_amax[r][2 * h + 1] = a1;
+  for (int i = 0; i < 16; ++i) a = fmaxf(a, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+  // d block = lane / 8: reduce over the 8 lanes of the block
+#pragma unroll
+  for (int sh = 1; sh <= 4; sh <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, sh));
+  if ((lane & 7) == 0) part_amax[warp][lane >> 3] = a;
   __syncthreads();
+  // a 32-row block spans warps 2 rb and 2 rb + 1
   if (tid < 16) {
     const int rb = tid >> 2, db = tid & 3;
-    float m = 0.f;
-    for (int i = 0; i < 32; ++i) m = fmaxf(m, row_amax[32 * rb + i][db]);
-    eb[rb][db] = e8m0_for_amax(m);
+    eb[rb][db] = e8m0_for_amax(fmaxf(part_amax[2 * rb][db], part_amax[2 * rb + 1][db]));
   }
   __syncthreads();
-  if (valid) {
-    const float s0 = e8m0_inverse(eb[r >> 5][2 * h]);
-    const float s1 = e8m0_inverse(eb[r >> 5][2 * h + 1]);
-    uint32_t w[16];
+  const float sc = e8m0_inverse(eb[warp >> 1][lane >> 3]);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = pack_e4m3x4(v[4 * i] * s0, v[4 * i + 1] * s0, v[4 * i + 2] * s0, v[4 * i + 3] * s0);
-#pragma unroll
-    for (int i = 8; i < 16; ++i)
-      w[i] = pack_e4m3x4(v[4 * i] * s1, v[4 * i + 1] * s1, v[4 * i + 2] * s1, v[4 * i + 3] * s1);
-    uint4* dst = reinterpret_cast<uint4*>(q + (bh * n + row) * 128 + 64 * h);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  for (int i = 0; i < 16; ++i) {
+    const int row = row0 + i;
+    if (row < n)
+      reinterpret_cast<uint32_t*>(q + (bh * n + row) * 128)[lane] =
+          pack_e4m3x4(v[i].x * sc, v[i].y * sc, v[i].z * sc, v[i].w * sc);
   }
   // the tile's atom: 512 bytes, two per thread
   uint8_t* atom = atoms + (bh * ntiles + tile) * 512;
