@@ -563,6 +563,7 @@ __global__ void __launch_bounds__(384, 1)
       const bool valid = grow < args.n;
       // rows are 128 or 256 bytes: 32-byte alignment of O decides the store width for all of them
       const bool o_aligned32 = (reinterpret_cast<uintptr_t>(args.o) & 31u) == 0;
+      const uint64_t pol_o = policy_evict_first();
       __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * args.n + (valid ? grow : 0)) * D;
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
@@ -577,7 +578,7 @@ __global__ void __launch_bounds__(384, 1)
           const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(ob[2 * i]), __uint_as_float(ob[2 * i + 1])), inv_l_2);
           pk[i] = pack_bf16x2(o2.x, o2.y);
         }
-        if (valid) store_row64(orow + c, pk, o_aligned32);
+        if (valid) store_row64(orow + c, pk, o_aligned32, pol_o);
       }
       if (valid) args.lse[static_cast<size_t>(bh) * args.n + grow] = (m * sl2 + lg2_mufu(l)) * 0.69314718055994531f;
     }

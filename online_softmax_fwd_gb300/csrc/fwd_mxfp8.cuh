@@ -504,6 +504,7 @@ __global__ void __launch_bounds__(384, 1)
       const bool valid = grow < args.n;
       // rows are 128 or 256 bytes: 32-byte alignment of O decides the store width for all of them
       const bool o_aligned32 = (reinterpret_cast<uintptr_t>(args.o) & 31u) == 0;
+      const uint64_t pol_o = policy_evict_first();
       __nv_bfloat16* orow = args.o + (static_cast<size_t>(bh) * args.n + (valid ? grow : 0)) * 128;
       const float2 inv_l_2 = make_float2(inv_l, inv_l);
       // all of O_t into registers first: the next item's S1 GEMM may then put
@@ -524,7 +525,7 @@ __global__ void __launch_bounds__(384, 1)
               __fmul2_rn(make_float2(__uint_as_float(ob[c][2 * i]), __uint_as_float(ob[c][2 * i + 1])), inv_l_2);
           w[i] = pack_bf16x2(o2.x, o2.y);
         }
-        if (valid) store_row64(orow + 32 * c, w, o_aligned32);
+        if (valid) store_row64(orow + 32 * c, w, o_aligned32, pol_o);
       }
       if (valid) args.lse[static_cast<size_t>(bh) * args.n + grow] = (m * sl2 + lg2_mufu(l)) * 0.69314718055994531f;
     }

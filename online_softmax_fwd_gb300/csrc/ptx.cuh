@@ -139,15 +139,17 @@ __device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint
 }
 
 // 64 bytes of a row to global memory: two 256-bit stores when the address is
-// 32-byte aligned (each thread then writes whole 32-byte sectors), else four
-// 128-bit stores.
-__device__ __forceinline__ void store_row64(void* dst, const uint32_t (&w)[16], bool aligned32) {
+// 32-byte aligned (each thread then writes whole 32-byte sectors), with an L2
+// policy (evict-first for the output, so it does not push K and V out), else
+// four 128-bit stores.
+__device__ __forceinline__ void store_row64(void* dst, const uint32_t (&w)[16], bool aligned32, uint64_t policy) {
   if (aligned32) {
 #pragma unroll
     for (int h = 0; h < 2; ++h)
-      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(static_cast<uint8_t*>(dst) + 32 * h),
+      asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(
+                       static_cast<uint8_t*>(dst) + 32 * h),
                    "r"(w[8 * h]), "r"(w[8 * h + 1]), "r"(w[8 * h + 2]), "r"(w[8 * h + 3]), "r"(w[8 * h + 4]),
-                   "r"(w[8 * h + 5]), "r"(w[8 * h + 6]), "r"(w[8 * h + 7])
+                   "r"(w[8 * h + 5]), "r"(w[8 * h + 6]), "r"(w[8 * h + 7]), "l"(policy)
                    : "memory");
   } else {
     uint4* d = static_cast<uint4*>(dst);
