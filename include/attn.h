@@ -187,6 +187,19 @@ attn_status_t attn_fwd_mxfp8_ex(const void* q8, const void* q_sf, const void* k8
                                 float scale, float tau, int exp2_emu16, int p_scaling, void* stream);
 
 /*
+ * attn_selftest_wait_timeout -- exercises the kernels' failure detection
+ * without a fault: launches one small kernel on stream whose warps wait, with
+ * the same bounded wait the attention kernels use, on barriers that nothing
+ * completes. One wait gives up after limit_cycles SM clock cycles, records
+ * ATTN_ERR_TIMEOUT in the device status word and raises the block's abort
+ * flag; the other (64 times the limit) returns early on that flag, so the
+ * kernel ends after about limit_cycles. attn_get_device_status then reports
+ * ATTN_ERR_TIMEOUT (and clears it); the context stays usable.
+ * limit_cycles in [1000, 1e10], else ATTN_ERR_INVALID_ARG. Asynchronous.
+ */
+attn_status_t attn_selftest_wait_timeout(long long limit_cycles, void* stream);
+
+/*
  * attn_exp2_emulated -- y[i] = software exp2 of x[i] for i < n, computed by
  * the very device function the attention kernels use on the FMA pipe (see
  * attn_fwd_ex). For checking that function bit for bit against a scalar model.

@@ -315,6 +315,15 @@ const char* attn_status_string(attn_status_t status) {
   return "ATTN_ERR_UNKNOWN";
 }
 
+attn_status_t attn_selftest_wait_timeout(long long limit_cycles, void* stream) {
+  if (limit_cycles < 1000 || limit_cycles > 10000000000LL) return ATTN_ERR_INVALID_ARG;
+  unsigned int* status = status_word();
+  if (!status) return ATTN_ERR_CUDA;
+  return attn::launch_wait_timeout_selftest(status, limit_cycles, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_CUDA;
+}
+
 int attn_version(void) { return 100; }
 
 }  // extern "C"

@@ -98,20 +98,25 @@ __device__ __forceinline__ void record_status(unsigned int* status, uint32_t cod
 }
 
 // Wait for phase `parity` of an mbarrier, giving up when another role raised
-// the CTA's abort flag or after kWaitLimitCycles (then raising it).
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                         unsigned int* status, uint32_t where) {
+// the CTA's abort flag or after limit_cycles (then raising it and recording
+// ATTN_ERR_TIMEOUT with `where` in the status word).
+__device__ __forceinline__ bool wait_bar_limit(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                               unsigned int* status, uint32_t where, long long limit_cycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit_cycles) {
       *abort_flag = 1u;
       record_status(status, kStatusTimeout, where);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                         unsigned int* status, uint32_t where) {
+  return wait_bar_limit(bar, parity, abort_flag, status, where, kWaitLimitCycles);
 }
 
 // Bounded wait used only while draining after an abort.

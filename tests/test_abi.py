@@ -126,3 +126,8 @@ def test_mxfp8_ex_rejects_bad_p_scaling(lib):
     zero = lambda tau, ps: args(tau, ps)[:9] + (0,) + args(tau, ps)[10:]   # H = 0: valid, nothing to do
     assert lib.attn_fwd_mxfp8_ex(*zero(0.8, 1)) == 0
     assert lib.attn_fwd_mxfp8_ex(*zero(8.0, 0)) == 0
+
+
+def test_selftest_rejects_bad_limits(lib):
+    assert lib.attn_selftest_wait_timeout(999, None) == 1
+    assert lib.attn_selftest_wait_timeout(10 ** 10 + 1, None) == 1
