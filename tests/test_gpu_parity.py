@@ -181,6 +181,23 @@ def test_full_size_workloads_sampled(attn, w):
                 f"{w.name} b={b} h={h}")
 
 
+@pytest.mark.parametrize("shape,causal", [((1, 1, (1 << 20) + 37, 64), True), ((1, 2, (1 << 18) + 5, 128), False)],
+                         ids=["n1M_d64_causal", "n256K_d128"])
+def test_long_sequences_sampled(attn, shape, causal):
+    # a million keys per row (and a ragged tail): long key loops, many work
+    # items per head, the last rows of the causal case see every key
+    B, H, N, d = shape
+    q, k, v = (I.to_bf16(x) for x in I.draw_fp32(B, H, N, d, seed=N % 1000))
+    o, lse = run(attn, q, k, v, causal, d ** -0.5)
+    assert torch.isfinite(lse).all()
+    rng = np.random.default_rng(4)
+    for b, h in {(0, 0), (B - 1, H - 1)}:
+        rows = np.unique(np.concatenate([sample_rows(N, rng)[:24], [N - 1, N - 2, N // 2]]))
+        o_ref, lse_ref = attention_rows(I.as_f64(q[b, h, rows]), I.as_f64(k[b, h]), I.as_f64(v[b, h]), rows,
+                                        causal, d ** -0.5)
+        compare(I.as_f64(o[b, h, rows]), lse[b, h, rows].double().numpy(), o_ref, lse_ref, f"{shape} b={b} h={h}")
+
+
 def test_exp_bound_workload_with_software_share(attn):
     w = I.CAUSAL_D64
     q, k, v = I.bf16_qkv(w)
