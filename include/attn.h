@@ -102,7 +102,7 @@ attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, 
  *                     attn_fwd_host_workspace_bytes(B, H, N, d) bytes,
  *                     256-byte aligned, owned by the caller; not read or
  *                     written after the call's work on `stream` completes.
- * The B*H heads are cut into about eight chunks; each chunk is copied in,
+ * The B*H heads are cut into about six chunks; each chunk is copied in,
  * computed (attn_fwd) and copied out on three library-owned streams of the
  * current device (created on first use and kept), with two chunk buffers in
  * the workspace, so copies and kernels overlap. The work is ordered after what
@@ -115,6 +115,21 @@ size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d);
 attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                             int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
                             void* stream);
+
+/*
+ * attn_fwd_host_noalloc -- attn_fwd_host without a caller workspace: the chunk
+ * buffers live in a fixed device array of the library,
+ * attn_fwd_host_noalloc_max_workspace() bytes (128 MiB), found once per
+ * device; nothing is allocated or freed. Problems whose
+ * attn_fwd_host_workspace_bytes(B, H, N, d) exceeds that size are rejected
+ * with ATTN_ERR_UNSUPPORTED before any work. Calls on one device share the
+ * array and are serialised: each call's work starts after the previous call's
+ * copies back have finished, whatever streams the calls use. Other arguments,
+ * ordering and errors as attn_fwd_host; results identical to it.
+ */
+size_t attn_fwd_host_noalloc_max_workspace(void);
+attn_status_t attn_fwd_host_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                    int N, int d, int causal, float scale, void* stream);
 
 /*
  * MXFP8 variant ("PyTorch FlashAttention-4 adds MXFP8 block-scaled forward and

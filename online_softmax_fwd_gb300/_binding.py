@@ -57,6 +57,10 @@ _SIGNATURES = {
     # q, k, v, o, lse (host), B, H, N, d, causal, scale, workspace, workspace_bytes, stream
     "attn_fwd_host": ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
                       + [ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
+    "attn_fwd_host_noalloc_max_workspace": ([], ctypes.c_size_t),
+    # q, k, v, o, lse (host), B, H, N, d, causal, scale, stream
+    "attn_fwd_host_noalloc": ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_void_p],
+                              ctypes.c_int),
     "attn_get_device_status": ([ctypes.c_void_p], ctypes.c_int),
     "attn_selftest_wait_timeout": ([ctypes.c_longlong, ctypes.c_void_p], ctypes.c_int),
     "attn_status_string": ([ctypes.c_int], ctypes.c_char_p),

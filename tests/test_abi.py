@@ -131,3 +131,16 @@ def test_mxfp8_ex_rejects_bad_p_scaling(lib):
 def test_selftest_rejects_bad_limits(lib):
     assert lib.attn_selftest_wait_timeout(999, None) == 1
     assert lib.attn_selftest_wait_timeout(10 ** 10 + 1, None) == 1
+
+
+def test_host_noalloc_limits_and_validation(lib):
+    H = A  # fake host addresses, never dereferenced on these paths
+    cap = lib.attn_fwd_host_noalloc_max_workspace()
+    assert cap == 128 << 20
+    call = lambda B, Hh, N, d, causal=0, scale=0.125: lib.attn_fwd_host_noalloc(H, H, H, H, H, B, Hh, N, d, causal,
+                                                                                 scale, None)
+    assert lib.attn_fwd_host_workspace_bytes(1, 64, 65536, 128) > cap
+    assert call(1, 64, 65536, 128) == 2     # needs more than the fixed array: rejected before any work
+    assert call(1, 2, 256, 96) == 2         # unsupported head dim, as attn_fwd_host
+    assert call(1, -2, 256, 64) == 1
+    assert call(0, 2, 256, 64) == 0         # nothing to do
