@@ -128,3 +128,10 @@ def rescale_scores(kind: str, rows: int = 256, keys: int = 8192, seed: int = 0) 
         top = 24.0 if kind == "rise24" else 96.0
         return 1.5 * noise + np.linspace(0.0, top, keys)[None, :]
     raise ValueError(kind)
+
+
+def fp8_sim_values(keys: int = 8192, d: int = 64, seed: int = 1) -> np.ndarray:
+    """V [keys, d] for the P-in-FP8 error table of "FlashAttention-4's Softmax
+    Tricks", section "Where 'exact' breaks: P in FP8": the page does not state
+    V or d; iid N(0, 1) values and d = 64 are the reading taken here."""
+    return np.random.default_rng(seed).standard_normal((keys, d))

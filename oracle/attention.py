@@ -82,7 +82,8 @@ def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool, sca
 
 def blockwise_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool, scale: float,
                         block: int = 128, tau: float | None = None, dtype=np.float64,
-                        p_cast=None, row_index: np.ndarray | None = None) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+                        p_cast=None, row_index: np.ndarray | None = None,
+                        scores: np.ndarray | None = None) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
     """The streaming recurrence over key blocks, for one (batch, head) per call
     or for [..., N, d] batched inputs.
 
@@ -103,15 +104,22 @@ def blockwise_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: boo
     (the reading of "FlashAttention-4's Softmax Tricks", section "Conditional
     rescaling": the sum is taken from fp32 P, and P is cast to the MMA input
     type). ``row_index`` gives the sequence positions of q's rows (default
-    0 .. n_q - 1) for the causal mask. Returns (O, LSE, fired) where fired
+    0 .. n_q - 1) for the causal mask. ``scores`` (optional) gives the raw
+    scores Q K^T [..., n_q, n_k] directly, for simulations over a chosen score
+    distribution; q and k are then not used (pass None). Returns (O, LSE, fired) where fired
     [..., N, nblocks] is True where the running max moved (block 0 included).
     """
     f = dtype
-    q = np.asarray(q).astype(f)
-    k = np.asarray(k).astype(f)
     v = np.asarray(v).astype(f)
-    n_q, n_k = q.shape[-2], k.shape[-2]
-    lead = q.shape[:-2]
+    if scores is None:
+        q = np.asarray(q).astype(f)
+        k = np.asarray(k).astype(f)
+        n_q, n_k = q.shape[-2], k.shape[-2]
+        lead = q.shape[:-2]
+    else:
+        scores = np.asarray(scores).astype(f)
+        n_q, n_k = scores.shape[-2], scores.shape[-1]
+        lead = scores.shape[:-2]
     sl2 = f(scale * LOG2E)
     m = np.full(lead + (n_q,), -np.inf, dtype=f)
     l = np.zeros(lead + (n_q,), dtype=f)
@@ -124,7 +132,10 @@ def blockwise_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: boo
         j0, j1 = jb * block, min(n_k, (jb + 1) * block)
         if causal and j0 > last_row:
             break                                   # every remaining block is above the diagonal
-        s = q @ np.swapaxes(k[..., j0:j1, :], -1, -2)   # raw scores [..., n_q, bk]
+        if scores is None:
+            s = q @ np.swapaxes(k[..., j0:j1, :], -1, -2)   # raw scores [..., n_q, bk]
+        else:
+            s = scores[..., j0:j1]
         if causal and j1 - 1 > 0:
             cols = np.arange(j0, j1)
             s = np.where(cols[None, :] <= rows[:, None], s, f(-np.inf))

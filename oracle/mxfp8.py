@@ -23,6 +23,14 @@ E4M3 (the OCP "E4M3FN" encoding): 1 sign bit, 4 exponent bits with bias 7,
 3 mantissa bits; exponent field 0 encodes subnormals m * 2^-9; the code
 S.1111.111 is NaN and there are no infinities, so the largest finite value is
 1.75 * 2^8 = 448 and the smallest subnormal 2^-9.
+
+"FlashAttention-4's Softmax Tricks", section "Where 'exact' breaks: P in
+FP8", compares P held in E4M3 with P held in E5M2 under a constant 2^8
+offset: E5M2 (OCP): 1 sign bit, 5 exponent bits with bias 15, 2 mantissa
+bits; exponent field 0 encodes subnormals m * 2^-16, exponent field 31 the
+infinities and NaNs, so the largest finite value is 1.75 * 2^15 = 57344.
+``p_to_fp8_constant`` converts P to either format with the constant scale;
+conversions saturate to the largest finite value (the kernels' "satfinite").
 """
 from __future__ import annotations
 
@@ -43,28 +51,52 @@ def e4m3_decode(codes) -> np.ndarray:
     return sign * mag
 
 
-def _all_finite_values() -> tuple[np.ndarray, np.ndarray]:
-    codes = np.arange(0, 0x7F)  # non-negative finite codes 0x00 .. 0x7E, ascending values
-    return codes, e4m3_decode(codes)
+E5M2_MAX = 57344.0
 
 
-_POS_CODES, _POS_VALUES = _all_finite_values()
+def e5m2_decode(codes) -> np.ndarray:
+    """Values (float64) of E5M2 byte codes; +-inf and NaN for exponent field 31."""
+    c = np.asarray(codes, dtype=np.int64) & 0xFF
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 2) & 0x1F
+    m = c & 0x3
+    mag = np.where(e == 0, m * 2.0 ** -16, (1.0 + m / 4.0) * np.exp2(e - 15.0))
+    mag = np.where(e == 31, np.where(m == 0, np.inf, np.nan), mag)
+    return sign * mag
+
+
+def _round_to_codes(x, codes: np.ndarray, values: np.ndarray, vmax: float) -> np.ndarray:
+    """Nearest of the ascending non-negative finite ``values`` (with their byte
+    ``codes``), ties to the even code (even mantissa), magnitudes above vmax
+    saturating to vmax; the sign bit (0x80) is kept, also for a zero result."""
+    x = np.asarray(x, dtype=np.float64)
+    mag = np.minimum(np.abs(x), vmax)
+    # index of the largest representable value <= mag
+    lo = np.clip(np.searchsorted(values, mag, side="right") - 1, 0, len(values) - 1)
+    hi = np.minimum(lo + 1, len(values) - 1)
+    vlo, vhi = values[lo], values[hi]
+    dlo, dhi = mag - vlo, vhi - mag
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi != lo) & ((codes[lo] & 1) == 1))
+    code = np.where(pick_hi, codes[hi], codes[lo])
+    return np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
+
+
+_POS_CODES = np.arange(0, 0x7F)      # E4M3 non-negative finite codes 0x00 .. 0x7E, ascending values
+_POS_VALUES = e4m3_decode(_POS_CODES)
+_E5_CODES = np.arange(0, 0x7C)       # E5M2 non-negative finite codes 0x00 .. 0x7B
+_E5_VALUES = e5m2_decode(_E5_CODES)
 
 
 def e4m3_encode(x) -> np.ndarray:
     """Round float values to E4M3 codes: nearest, ties to the even code
     (even mantissa), magnitudes above 448 saturate to 448. NaN is not expected."""
-    x = np.asarray(x, dtype=np.float64)
-    mag = np.minimum(np.abs(x), E4M3_MAX)
-    # index of the largest representable value <= mag
-    lo = np.clip(np.searchsorted(_POS_VALUES, mag, side="right") - 1, 0, len(_POS_VALUES) - 1)
-    hi = np.minimum(lo + 1, len(_POS_VALUES) - 1)
-    vlo, vhi = _POS_VALUES[lo], _POS_VALUES[hi]
-    dlo, dhi = mag - vlo, vhi - mag
-    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi != lo) & ((_POS_CODES[lo] & 1) == 1))
-    code = np.where(pick_hi, _POS_CODES[hi], _POS_CODES[lo])
-    # the sign is kept, also when the magnitude rounds to zero (IEEE style)
-    return np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
+    return _round_to_codes(x, _POS_CODES, _POS_VALUES, E4M3_MAX)
+
+
+def e5m2_encode(x) -> np.ndarray:
+    """Round float values to E5M2 codes: nearest, ties to the even code,
+    magnitudes above 57344 saturate to 57344. NaN is not expected."""
+    return _round_to_codes(x, _E5_CODES, _E5_VALUES, E5M2_MAX)
 
 
 def e8m0_exponent(amax) -> np.ndarray:
@@ -120,5 +152,20 @@ def p_to_mxfp8_constant(p: np.ndarray) -> np.ndarray:
     """Values of P after conversion to E4M3 with the constant scale 2^-8
     (float64): P / 2^-8 rounded to E4M3 (nearest even, saturating at 448),
     times 2^-8."""
+    return p_to_fp8_constant(p, "e4m3")
+
+
+def p_to_fp8_constant(p: np.ndarray, fmt: str) -> np.ndarray:
+    """Values of P after conversion to ``fmt`` ("e4m3" or "e5m2") with the
+    constant scale 2^-8 (the 2^8 offset of "FlashAttention-4's Softmax
+    Tricks", section "Where 'exact' breaks: P in FP8"): P / 2^-8 rounded to the
+    format (nearest even, saturating at its largest finite value), times 2^-8.
+    A stale maximum lets P reach 2^tau: E4M3 saturates once 2^(tau + 8) > 448,
+    E5M2 once 2^(tau + 8) > 57344."""
     scale = 2.0 ** P_CONST_EXP
-    return e4m3_decode(e4m3_encode(np.asarray(p, dtype=np.float64) / scale)) * scale
+    x = np.asarray(p, dtype=np.float64) / scale
+    if fmt == "e4m3":
+        return e4m3_decode(e4m3_encode(x)) * scale
+    if fmt == "e5m2":
+        return e5m2_decode(e5m2_encode(x)) * scale
+    raise ValueError(f"unknown FP8 format {fmt!r}")
