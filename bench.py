@@ -1,7 +1,7 @@
 """Benchmark of the fused attention forward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference] [--exp2-emu16 E] [--tau T] [--p-scaling 0|1]
+                    [--impl ours|reference] [--exp2-emu16 E] [--tau T] [--p-scaling 0|1|2]
 
 A step is one attention forward (O and LSE) over the whole workload, inputs
 resident in HBM (Q, K, V together exceed the 129 MB L2, so no flush is
@@ -454,7 +454,7 @@ def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
                "config": {**w.describe(), "parallelism": f"replicas{world}" if world > 1 else "single",
                           "l2": f"inputs larger than L2 ({step.input_bytes() / 2**20:.0f} MiB > 129 MB)",
                           "tau": step.tau if w.dtype == "mxfp8" else args.tau, "exp2_emu16": args.exp2_emu16,
-                          **({"p_scaling": ["block_amax", "constant_2^-8"][args.p_scaling]}
+                          **({"p_scaling": ["block_amax", "constant_2^-8", "constant_2^-8_e5m2"][args.p_scaling]}
                              if w.dtype == "mxfp8" else {})},
                "e2e": e2e, "gpu_launches": args.steps * step.launches, "roofline": roofline, "cpu_baseline": cpu,
                "clocks": clocks, "kernel_ms": {"mean": float(np.mean(launch_ms)), "min": float(np.min(launch_ms)),
@@ -482,8 +482,9 @@ def main() -> None:
     ap.add_argument("--exp2-emu16", type=int, default=0)
     ap.add_argument("--tau", type=float, default=None,
                     help="rescale threshold (default 8 for bf16 P, 0 for FP8 P)")
-    ap.add_argument("--p-scaling", type=int, default=0, choices=[0, 1],
-                    help="MXFP8 P scale: 0 one per 32 keys from the block amax, 1 the constant 2^-8")
+    ap.add_argument("--p-scaling", type=int, default=0, choices=[0, 1, 2],
+                    help="MXFP8 P scale: 0 one per 32 keys from the block amax, 1 the constant 2^-8, "
+                         "2 the constant 2^-8 with P in E5M2")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--no-e2e", action="store_true")

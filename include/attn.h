@@ -181,7 +181,8 @@ attn_status_t attn_fwd_mxfp8(const void* q8, const void* q_sf, const void* k8, c
                              const void* v_sf, void* o, float* lse, int B, int H, int N, int d, int causal,
                              float scale, void* stream);
 
-/* How attn_fwd_mxfp8_ex scales P before converting it to E4M3. */
+/* How attn_fwd_mxfp8_ex scales P before converting it to FP8 for the P V
+ * product (V stays E4M3). */
 enum {
   /* one E8M0 scale per 32 keys of a row, from the group's largest P (the
    * exp of its largest score): the conversion attn_fwd_mxfp8 uses */
@@ -191,7 +192,13 @@ enum {
    * unroll-KV": softmax keeps P in [0, 1], so a fixed scale is robust): P = 1
    * maps to 256; needs tau <= log2(448 / 256) ~ 0.807 so that 2^tau * 256
    * stays within E4M3 (else ATTN_ERR_INVALID_ARG) */
-  ATTN_P_SCALE_CONSTANT = 1
+  ATTN_P_SCALE_CONSTANT = 1,
+  /* the same constant 2^-8 with P held in E5M2 ("FlashAttention-4's Softmax
+   * Tricks", section "Where 'exact' breaks: P in FP8": E5M2's largest value
+   * 57344 leaves room for a stale maximum that E4M3 lacks, at 2 mantissa
+   * bits instead of 3): needs tau <= log2(57344 / 256) ~ 7.807 (else
+   * ATTN_ERR_INVALID_ARG) */
+  ATTN_P_SCALE_CONSTANT_E5M2 = 2
 };
 
 /* attn_fwd_mxfp8 with tau in [0, 16], a software-exp2 share of 0, 2 or 4 of

@@ -212,6 +212,7 @@ def mxfp8_quantize(x: torch.Tensor, role: int, stream=None) -> tuple[torch.Tenso
 
 P_SCALE_BLOCK_AMAX = 0
 P_SCALE_CONSTANT = 1
+P_SCALE_CONSTANT_E5M2 = 2
 
 
 def attn_fwd_mxfp8(q8: torch.Tensor, q_sf: torch.Tensor, k8: torch.Tensor, k_sf: torch.Tensor, v8: torch.Tensor,
@@ -221,7 +222,8 @@ def attn_fwd_mxfp8(q8: torch.Tensor, q_sf: torch.Tensor, k8: torch.Tensor, k_sf:
     """Attention forward from MXFP8 inputs (outputs of mxfp8_quantize); tau
     defaults to 0, the FP8 setting (attn_fwd_mxfp8). p_scaling: 0 = one scale
     per 32 keys from the block amax (P_SCALE_BLOCK_AMAX), 1 = the constant 2^-8
-    (P_SCALE_CONSTANT, tau <= 0.807)."""
+    (P_SCALE_CONSTANT, tau <= 0.807), 2 = the same constant with P held in
+    E5M2 (P_SCALE_CONSTANT_E5M2, tau <= 7.807)."""
     for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
         if not t.is_cuda or t.dtype != torch.uint8 or t.dim() != 4 or not t.is_contiguous() or t.shape != q8.shape:
             raise ValueError(f"{name} must be contiguous CUDA uint8 (E4M3 codes) shaped like q8")

@@ -25,6 +25,8 @@ constexpr int kMaxDevices = 64;
 constexpr long long kMaxN = 1LL << 24;
 // log2(448 / 256), rounded down: the largest tau for which P * 2^8 <= 448
 constexpr float kPConstMaxTau = 0.807f;
+// log2(57344 / 256), rounded down: the same bound for P held in E5M2
+constexpr float kPConstE5m2MaxTau = 7.807f;
 
 // Device error word, one per device (each device holds its own copy).
 __device__ unsigned int g_attn_status;
@@ -221,9 +223,13 @@ attn_status_t attn_fwd_mxfp8_ex(const void* q8, const void* q_sf, const void* k8
   if (d != 128) return d > 0 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
   if (exp2_emu16 < 0 || exp2_emu16 > 16) return ATTN_ERR_INVALID_ARG;
   if (exp2_emu16 != 0 && exp2_emu16 != 2 && exp2_emu16 != 4) return ATTN_ERR_UNSUPPORTED;
-  if (p_scaling != ATTN_P_SCALE_BLOCK_AMAX && p_scaling != ATTN_P_SCALE_CONSTANT) return ATTN_ERR_INVALID_ARG;
-  // constant 2^-8: the largest P, 2^tau, must stay within E4M3's 448 / 256
+  if (p_scaling != ATTN_P_SCALE_BLOCK_AMAX && p_scaling != ATTN_P_SCALE_CONSTANT &&
+      p_scaling != ATTN_P_SCALE_CONSTANT_E5M2)
+    return ATTN_ERR_INVALID_ARG;
+  // constant 2^-8: the largest P, 2^tau, must stay within the format's largest
+  // value / 256 (E4M3 448, E5M2 57344)
   if (p_scaling == ATTN_P_SCALE_CONSTANT && !(tau <= kPConstMaxTau)) return ATTN_ERR_INVALID_ARG;
+  if (p_scaling == ATTN_P_SCALE_CONSTANT_E5M2 && !(tau <= kPConstE5m2MaxTau)) return ATTN_ERR_INVALID_ARG;
   if (N > kMaxN || static_cast<long long>(B) * H * ((N + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
   if (!q8 || !q_sf || !k8 || !k_sf || !v8 || !v_sf || !o || !lse) return ATTN_ERR_INVALID_ARG;
@@ -263,9 +269,13 @@ attn_status_t attn_fwd_mxfp8_ex(const void* q8, const void* q_sf, const void* k8
     ctas = static_cast<int>(std::min<long long>(items, sms));
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = p_scaling == ATTN_P_SCALE_CONSTANT
-                      ? attn::launch_fwd_mxfp8_d128_pconst(causal, exp2_emu16, mq, mk, mv, a, wl, ctas, st)
-                      : attn::launch_fwd_mxfp8_d128(causal, exp2_emu16, mq, mk, mv, a, wl, ctas, st);
+  cudaError_t e;
+  if (p_scaling == ATTN_P_SCALE_CONSTANT)
+    e = attn::launch_fwd_mxfp8_d128_pconst(causal, exp2_emu16, mq, mk, mv, a, wl, ctas, st);
+  else if (p_scaling == ATTN_P_SCALE_CONSTANT_E5M2)
+    e = attn::launch_fwd_mxfp8_d128_pconst_e5m2(causal, exp2_emu16, mq, mk, mv, a, wl, ctas, st);
+  else
+    e = attn::launch_fwd_mxfp8_d128(causal, exp2_emu16, mq, mk, mv, a, wl, ctas, st);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -9,16 +9,16 @@ cudaError_t launch_fwd_mxfp8_d128(int causal, int emu16, const CUtensorMap& q, c
                              const FwdMxArgs& a, const WorkList& wl, int ctas, cudaStream_t s) {
   if (causal) {
     switch (emu16) {
-      case 0: return launch_fwd_mxfp8<true, 0, false>(q, k, v, a, wl, ctas, s);
-      case 2: return launch_fwd_mxfp8<true, 2, false>(q, k, v, a, wl, ctas, s);
-      case 4: return launch_fwd_mxfp8<true, 4, false>(q, k, v, a, wl, ctas, s);
+      case 0: return launch_fwd_mxfp8<true, 0, 0>(q, k, v, a, wl, ctas, s);
+      case 2: return launch_fwd_mxfp8<true, 2, 0>(q, k, v, a, wl, ctas, s);
+      case 4: return launch_fwd_mxfp8<true, 4, 0>(q, k, v, a, wl, ctas, s);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (emu16) {
-    case 0: return launch_fwd_mxfp8<false, 0, false>(q, k, v, a, wl, ctas, s);
-    case 2: return launch_fwd_mxfp8<false, 2, false>(q, k, v, a, wl, ctas, s);
-    case 4: return launch_fwd_mxfp8<false, 4, false>(q, k, v, a, wl, ctas, s);
+    case 0: return launch_fwd_mxfp8<false, 0, 0>(q, k, v, a, wl, ctas, s);
+    case 2: return launch_fwd_mxfp8<false, 2, 0>(q, k, v, a, wl, ctas, s);
+    case 4: return launch_fwd_mxfp8<false, 4, 0>(q, k, v, a, wl, ctas, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -89,11 +89,14 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
 
-// PCONST: P's scale is the constant 2^-8 (E8M0 byte 119) instead of one per
-// 32 keys from the block amax (same page, same section: constant scaling of P
-// stays robust because softmax keeps P in [0, 1]; with a stale maximum P
-// reaches 2^tau, so 256 * 2^tau <= 448 needs tau <= log2(1.75)).
-template <bool CAUSAL, int EMU, bool PCONST>
+// PS, the scaling of P: 0 = one E8M0 scale per 32 keys from the block amax;
+// 1 = the constant 2^-8 (E8M0 byte 119) with P in E4M3 (same page, same
+// section: constant scaling of P stays robust because softmax keeps P in
+// [0, 1]; with a stale maximum P reaches 2^tau, so 256 * 2^tau <= 448 needs
+// tau <= log2(1.75)); 2 = the same constant with P in E5M2, whose 57344
+// leaves room for tau <= log2(224) ("FlashAttention-4's Softmax Tricks",
+// section "Where 'exact' breaks: P in FP8"). V stays E4M3.
+template <bool CAUSAL, int EMU, int PS>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_mxfp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const FwdMxArgs args,
@@ -259,7 +262,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (uint32_t kk = 0; kk < 4; ++kk)
             mma_mxf8_ts_lo(tmem + C::col_o(t), s_cols + 8 * kk, ring_v + vslot * kSlotStep + 256 * kk, desc_hi,
-                           idesc_mxf8(128, 128, true, kk, kk), (!first || kk > 0) ? 1u : 0u, s_cols + C::kPScale,
+                           idesc_mxf8(128, 128, true, kk, kk, PS == 2), (!first || kk > 0) ? 1u : 0u, s_cols + C::kPScale,
                            s_cols + C::kVScale);
         }
       };
@@ -447,7 +450,7 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t sfw = 0;
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        const uint32_t sfb = PCONST ? 119u : e8m0_for_amax(ex2_mufu(__fmaf_rn(bmx[g], sl2, neg_ms)));
+        const uint32_t sfb = PS != 0 ? 119u : e8m0_for_amax(ex2_mufu(__fmaf_rn(bmx[g], sl2, neg_ms)));
         sfw |= sfb << (8 * g);
         const float shift = neg_ms - static_cast<float>(static_cast<int>(sfb) - 127);
         const float2 shift_2 = make_float2(shift, shift);
@@ -467,7 +470,7 @@ __global__ void __launch_bounds__(384, 1)
           }
           acc[(i >> 1) & 1] = __fadd2_rn(acc[(i >> 1) & 1], p0);
           acc[2 + ((i >> 1) & 1)] = __fadd2_rn(acc[2 + ((i >> 1) & 1)], p1);
-          pk[8 * g + i / 2] = pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
+          pk[8 * g + i / 2] = PS == 2 ? pack_e5m2x4(p0.x, p0.y, p1.x, p1.y) : pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
         }
         acc[0] = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
         lsum = __fmaf_rn(acc[0].x + acc[0].y, __uint_as_float(sfb << 23), lsum);
@@ -543,10 +546,10 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <bool CAUSAL, int EMU, bool PCONST>
+template <bool CAUSAL, int EMU, int PS>
 cudaError_t launch_fwd_mxfp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const FwdMxArgs& args, const WorkList& wl, int ctas, cudaStream_t stream) {
-  auto kernel = attn_fwd_mxfp8_kernel<CAUSAL, EMU, PCONST>;
+  auto kernel = attn_fwd_mxfp8_kernel<CAUSAL, EMU, PS>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MxCfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   // the setmaxnreg split must fit the registers the CTA is launched with

@@ -9,16 +9,16 @@ cudaError_t launch_fwd_mxfp8_d128_pconst(int causal, int emu16, const CUtensorMa
                              const FwdMxArgs& a, const WorkList& wl, int ctas, cudaStream_t s) {
   if (causal) {
     switch (emu16) {
-      case 0: return launch_fwd_mxfp8<true, 0, true>(q, k, v, a, wl, ctas, s);
-      case 2: return launch_fwd_mxfp8<true, 2, true>(q, k, v, a, wl, ctas, s);
-      case 4: return launch_fwd_mxfp8<true, 4, true>(q, k, v, a, wl, ctas, s);
+      case 0: return launch_fwd_mxfp8<true, 0, 1>(q, k, v, a, wl, ctas, s);
+      case 2: return launch_fwd_mxfp8<true, 2, 1>(q, k, v, a, wl, ctas, s);
+      case 4: return launch_fwd_mxfp8<true, 4, 1>(q, k, v, a, wl, ctas, s);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (emu16) {
-    case 0: return launch_fwd_mxfp8<false, 0, true>(q, k, v, a, wl, ctas, s);
-    case 2: return launch_fwd_mxfp8<false, 2, true>(q, k, v, a, wl, ctas, s);
-    case 4: return launch_fwd_mxfp8<false, 4, true>(q, k, v, a, wl, ctas, s);
+    case 0: return launch_fwd_mxfp8<false, 0, 1>(q, k, v, a, wl, ctas, s);
+    case 2: return launch_fwd_mxfp8<false, 2, 1>(q, k, v, a, wl, ctas, s);
+    case 4: return launch_fwd_mxfp8<false, 4, 1>(q, k, v, a, wl, ctas, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -40,6 +40,15 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
+// Four floats -> four E5M2 bytes (round to nearest even, saturating to
+// +-57344), first value in the lowest byte.
+__device__ __forceinline__ uint32_t pack_e5m2x4(float a, float b, float c, float d) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
 // Scale-factor atom: 512 bytes holding the E8M0 scales of 128 rows x 4 blocks
 // of 32 along the MMA's K dimension; row r, block kb at byte
 // (r % 32) * 16 + (r / 32) * 4 + kb. tcgen05.cp 32x128b.warpx4 moves it into 4
@@ -66,11 +75,13 @@ __device__ __forceinline__ void sf_copy_to_tmem(uint32_t tmem_cols, uint32_t ato
                : "memory");
 }
 
-// Instruction descriptor, kind::mxf8f6f4 with E4M3 A and B, E8M0 scales,
-// fp32 accumulator; a_sf / b_sf pick the scale byte of this K=32 step.
-__host__ __device__ constexpr uint32_t idesc_mxf8(int m, int n, bool b_mn_major, uint32_t a_sf, uint32_t b_sf) {
+// Instruction descriptor, kind::mxf8f6f4 with E4M3 B, E4M3 or E5M2 A, E8M0
+// scales, fp32 accumulator; a_sf / b_sf pick the scale byte of this K=32 step.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int m, int n, bool b_mn_major, uint32_t a_sf, uint32_t b_sf,
+                                                  bool a_e5m2 = false) {
   return ((b_sf & 3u) << 4)                         // B scale-factor id
-         | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness (A and B E4M3: format 0)
+         | ((a_e5m2 ? 1u : 0u) << 7)                 // A format: E4M3 0, E5M2 1 (B stays E4M3)
+         | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
          | (static_cast<uint32_t>(n >> 3) << 17)     // N / 8
          | (1u << 23)                                // scale type E8M0
          | (static_cast<uint32_t>(m >> 4) << 24)     // M / 16

@@ -119,13 +119,16 @@ def test_mxfp8_ex_rejects_bad_p_scaling(lib):
     a = dict(GOOD, d=128)
     args = lambda tau, ps: (a["q"], a["q"], a["k"], a["k"], a["v"], a["v"], a["o"], a["lse"], a["B"], a["H"],
                             a["N"], 128, 1, a["scale"], tau, 0, ps, None)
-    assert lib.attn_fwd_mxfp8_ex(*args(0.0, 2)) == 1          # unknown mode
+    assert lib.attn_fwd_mxfp8_ex(*args(0.0, 3)) == 1          # unknown mode
     assert lib.attn_fwd_mxfp8_ex(*args(0.0, -1)) == 1
     assert lib.attn_fwd_mxfp8_ex(*args(0.9, 1)) == 1          # 2^0.9 * 256 > 448
     assert lib.attn_fwd_mxfp8_ex(*args(8.0, 1)) == 1
+    assert lib.attn_fwd_mxfp8_ex(*args(7.81, 2)) == 1         # 2^7.81 * 256 > 57344 (E5M2)
+    assert lib.attn_fwd_mxfp8_ex(*args(16.0, 2)) == 1
     zero = lambda tau, ps: args(tau, ps)[:9] + (0,) + args(tau, ps)[10:]   # H = 0: valid, nothing to do
     assert lib.attn_fwd_mxfp8_ex(*zero(0.8, 1)) == 0
     assert lib.attn_fwd_mxfp8_ex(*zero(8.0, 0)) == 0
+    assert lib.attn_fwd_mxfp8_ex(*zero(7.8, 2)) == 0
 
 
 def test_selftest_rejects_bad_limits(lib):

@@ -93,12 +93,13 @@ def run_mxfp8(attn, w_causal, x_q, x_k, x_v, scale, **kw):
 def mx_reference(xq, xk, xv, causal, scale, rows=None, tau=0.0, p_scaling=0):
     """The MXFP8 method in float64 for one head ([N, 128] fp32 inputs): Q, K, V
     quantised by the oracle's quantiser, P converted per 32 keys (p_scaling 0)
-    or with the constant scale (1); rows = the query positions to compute
-    (default all)."""
+    or with the constant scale to E4M3 (1) or E5M2 (2); rows = the query
+    positions to compute (default all)."""
     dq, dk, dv = (M.quantize_blocks(x)[2] for x in (xq, xk, xv))
     if rows is None:
         rows = np.arange(dq.shape[0])
-    p_cast = M.p_to_mxfp8_constant if p_scaling else M.p_to_mxfp8
+    p_cast = {0: M.p_to_mxfp8, 1: M.p_to_mxfp8_constant,
+              2: lambda p: M.p_to_fp8_constant(p, "e5m2")}[p_scaling]
     o, lse, _ = blockwise_attention(dq[rows], dk, dv, causal, scale, tau=tau, p_cast=p_cast, row_index=rows)
     return o, lse
 
@@ -115,7 +116,7 @@ def check(o, lse, o_ref, lse_ref, what):
     return err.max(), err.mean()
 
 
-@pytest.mark.parametrize("p_scaling", [0, 1], ids=["p_block_amax", "p_constant"])
+@pytest.mark.parametrize("p_scaling", [0, 1, 2], ids=["p_block_amax", "p_constant", "p_constant_e5m2"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shape", [(1, 1, 128), (1, 2, 256), (2, 1, 300), (1, 2, 1000), (1, 1, 1024)],
                          ids=lambda s: "x".join(map(str, s)))
@@ -137,6 +138,33 @@ def test_constant_p_scale_with_largest_allowed_tau(attn):
     for h in range(2):
         o_ref, lse_ref = mx_reference(xq[0, h], xk[0, h], xv[0, h], True, 128 ** -0.5, tau=0.8, p_scaling=1)
         check(o[0, h], lse[0, h], o_ref, lse_ref, f"tau=0.8 constant P scale h={h}")
+
+
+@pytest.mark.parametrize("tau", [0.0, 4.0, 7.8])
+def test_constant_p_scale_e5m2(attn, tau):
+    # P in E5M2 under the constant 2^-8: a stale maximum up to tau = 7.8 keeps
+    # 2^(tau + 8) inside 57344; the method's own result (the oracle with the
+    # same conversion) is the target, on peaked rows where the max moves
+    (xq, xk, xv), _ = peaked_case()
+    o, lse = run_mxfp8(attn, True, xq, xk, xv, 128 ** -0.5, tau=tau, p_scaling=2)
+    for h in range(2):
+        o_ref, lse_ref = mx_reference(xq[0, h], xk[0, h], xv[0, h], True, 128 ** -0.5, tau=tau, p_scaling=2)
+        check(o[0, h], lse[0, h], o_ref, lse_ref, f"tau={tau} E5M2 constant P scale h={h}")
+
+
+def test_fp8_p_formats_against_exact_attention(attn):
+    # the trade the error table of "FlashAttention-4's Softmax Tricks" ("Where
+    # 'exact' breaks: P in FP8") shows, on the kernel: at tau = 0 E5M2's two
+    # mantissa bits cost about twice E4M3's error; at tau = 4 E4M3 under the
+    # constant scale would saturate (refused by the library), E5M2 does not
+    (xq, xk, xv), (o_ref, _) = peaked_case()
+    err = {}
+    for ps, tau in ((1, 0.0), (2, 0.0), (2, 4.0)):
+        o, _ = run_mxfp8(attn, True, xq, xk, xv, 128 ** -0.5, tau=tau, p_scaling=ps)
+        d = I.as_f64(o) - o_ref
+        err[ps, tau] = np.sqrt((d ** 2).sum() / (o_ref ** 2).sum())
+    assert 1.3 * err[1, 0.0] < err[2, 0.0] < 4.0 * err[1, 0.0]
+    assert err[2, 4.0] < 2.5 * err[2, 0.0]
 
 
 # Persistent CTAs: up to 8192 (head, Q-tile pair) items follow a host-built
@@ -194,7 +222,7 @@ def test_lagging_max_costs_accuracy_with_fp8_p(attn):
     assert np.abs(lse8.double().numpy() - lse_ref).max() <= LSE_MAX_ABS  # LSE comes from fp32 P either way
 
 
-@pytest.mark.parametrize("p_scaling", [0, 1], ids=["p_block_amax", "p_constant"])
+@pytest.mark.parametrize("p_scaling", [0, 1, 2], ids=["p_block_amax", "p_constant", "p_constant_e5m2"])
 def test_full_size_workload_sampled(attn, p_scaling):
     w = I.MXFP8_CAUSAL
     xq, xk, xv = I.draw_fp32(w.B, w.H, w.N, w.d, w.qk_std, w.v_std, w.seed)
