@@ -477,22 +477,26 @@ __global__ void __launch_bounds__(384, 1)
       }
       tmem_st32(s_tm, pk);                      // P, 4 keys per column
       tmem_st1(s_tm + C::kPScale + quad, sfw);  // row r's scales at column r / 32
-      // correction of O once the scores are dead; lands before P is handed over
+      // correction of O once the scores are dead; lands before P is handed
+      // over. All of O is loaded at once (one load latency, overlapping the
+      // store of P), scaled and stored back.
       if (j > 0 && __any_sync(0xffffffffu, fire)) {
-        const float2 corr_2 = make_float2(corr, corr);
+        uint32_t ob[4][32];
 #pragma unroll
-        for (int c = 0; c < 128; c += 32) {
-          uint32_t ob[32];
-          tmem_ld32(o_tm + c, ob);
-          tmem_ld_wait();
-          reg_fence32(ob);
+        for (int c = 0; c < 4; ++c) tmem_ld32(o_tm + 32 * c, ob[c]);
+        const float2 corr_2 = make_float2(corr, corr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          reg_fence32(ob[c]);
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(ob[i]), __uint_as_float(ob[i + 1])), corr_2);
-            ob[i] = __float_as_uint(o2.x);
-            ob[i + 1] = __float_as_uint(o2.y);
+            const float2 o2 =
+                __fmul2_rn(make_float2(__uint_as_float(ob[c][i]), __uint_as_float(ob[c][i + 1])), corr_2);
+            ob[c][i] = __float_as_uint(o2.x);
+            ob[c][i + 1] = __float_as_uint(o2.y);
           }
-          tmem_st32(o_tm + c, ob);
+          tmem_st32(o_tm + 32 * c, ob[c]);
         }
       }
       l = l * corr + lsum;
