@@ -15,6 +15,8 @@ Modules
                  scalar C with a fused multiply-add, for bit-exact comparison.
   rescale_stats  the lagging-max (tau) rescale simulator and its statistics.
   mxfp8          the E4M3 / E8M0 32x32 block quantiser and its dequantisation.
+  backward       the gradient of the forward (dQ, dK, dV) with P rebuilt from
+                 the LSE: the five products of the backward pass.
 
 Parity pins (tests/test_oracle_*.py, marked "not gpu") tie every function here
 to something other than itself: brute force, closed forms, and the numbers the

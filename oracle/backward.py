@@ -1,0 +1,67 @@
+"""Float64 attention backward -- TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).
+
+The pages do not print the backward equations; they say what it consumes and
+how it is organised: "Lecture 2 - Online Softmax and Numerical Correctness",
+section "Use it in the real stack", notes that the forward's per-row
+log-sum-exp side output is what makes the backward pass cheap, and "PyTorch
+FlashAttention-4 adds MXFP8 block-scaled forward and backward for Blackwell",
+section "TMEM allocation and scale factor placement", describes a backward of
+five matrix products with dK and dV accumulated per key tile.
+
+The reading taken here is the plain gradient of the forward's definition
+O = softmax(s Q K^T [causal mask]) V for an upstream gradient dO:
+
+  P  = exp(s Q K^T - LSE)          the probabilities, rebuilt from the LSE
+  dV = P^T dO
+  dP = dO V^T
+  D  = rowsum(dO * O)              = rowsum(P * dP), since O = P V
+  dS = P * (dP - D)                the chain rule through the row softmax
+  dQ = s dS K,   dK = s dS^T Q
+
+(the five products: S, dP, dV, dK, dQ). Masked scores have P = 0, so they
+contribute nothing. Everything is float64, one (batch, head) at a time, rows
+in chunks only to bound memory.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def attention_bwd_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarray, do: np.ndarray,
+                       lse: np.ndarray, causal: bool, scale: float,
+                       row_chunk: int = 512) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """dQ, dK, dV (float64) of one (batch, head): q [N, d], k [N, d], v [N, dv],
+    o and do [N, dv], lse [N] (natural log of the scaled scores' row sums)."""
+    q, k, v, o, do, lse = (np.asarray(x, dtype=np.float64) for x in (q, k, v, o, do, lse))
+    n = q.shape[0]
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    d_row = (do * o).sum(axis=1)                     # D_i
+    for i0 in range(0, n, row_chunk):
+        i1 = min(n, i0 + row_chunk)
+        s = scale * (q[i0:i1] @ k.T)                 # [R, N] scaled scores
+        p = np.exp(s - lse[i0:i1, None])
+        if causal:
+            j = np.arange(k.shape[0])[None, :]
+            p = np.where(j <= np.arange(i0, i1)[:, None], p, 0.0)
+        dv += p.T @ do[i0:i1]
+        dp = do[i0:i1] @ v.T
+        ds = p * (dp - d_row[i0:i1, None])
+        dq[i0:i1] = scale * (ds @ k)
+        dk += scale * (ds.T @ q[i0:i1])
+    return dq, dk, dv
+
+
+def attention_bwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarray, do: np.ndarray,
+                  lse: np.ndarray, causal: bool, scale: float) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """dQ, dK, dV (float64) for [B, H, N, d] inputs and lse [B, H, N]."""
+    q = np.asarray(q)
+    B, H = q.shape[:2]
+    out = [np.empty(np.shape(x), dtype=np.float64) for x in (q, k, v)]
+    for b in range(B):
+        for h in range(H):
+            g = attention_bwd_head(q[b, h], k[b, h], v[b, h], o[b, h], do[b, h], lse[b, h], causal, scale)
+            for dst, src in zip(out, g):
+                dst[b, h] = src
+    return out[0], out[1], out[2]
