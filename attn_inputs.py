@@ -36,6 +36,7 @@ class Workload:
     v_std: float = 1.0
     dtype: str = "bf16"  # "bf16" or "mxfp8"
     seed: int = 0
+    direction: str = "fwd"  # "fwd", or "bwd" for the backward pass
 
     @property
     def scale(self) -> float:
@@ -43,8 +44,11 @@ class Workload:
 
     @property
     def flops(self) -> float:
-        """4*B*H*N^2*d, halved for causal (the counting convention of the task)."""
+        """4*B*H*N^2*d, halved for causal (the counting convention of the task);
+        the backward's five products count 2.5 times that."""
         f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        if self.direction == "bwd":
+            f *= 2.5
         return f / 2.0 if self.causal else f
 
     def describe(self) -> dict:
@@ -59,6 +63,7 @@ class Workload:
             "v_std": self.v_std,
             "dtype": self.dtype,
             "seed": self.seed,
+            "pass": self.direction,
         }
 
 
@@ -70,7 +75,14 @@ CAUSAL_D128_WIDE = Workload("bf16_causal_b2h16n8192d128_qk2", 2, 16, 8192, 128, 
 CAUSAL_D64 = Workload("bf16_causal_b8h16n4096d64", 8, 16, 4096, 64, True)
 MXFP8_CAUSAL = Workload("mxfp8_causal_b2h16n16384d128", 2, 16, 16384, 128, True, dtype="mxfp8")
 
-WORKLOADS = {w.name: w for w in (TINY, NONCAUSAL_D128, CAUSAL_D128_WIDE, CAUSAL_D64, MXFP8_CAUSAL)}
+# The backward pass on the two d = 128 shapes (dO from draw_grad; O and LSE
+# from the forward).
+BWD_D128 = Workload("bwd_bf16_b4h16n4096d128", 4, 16, 4096, 128, False, direction="bwd")
+BWD_CAUSAL_D128 = Workload("bwd_bf16_causal_b2h16n8192d128_qk2", 2, 16, 8192, 128, True, qk_std=2.0,
+                           direction="bwd")
+
+WORKLOADS = {w.name: w for w in (TINY, NONCAUSAL_D128, CAUSAL_D128_WIDE, CAUSAL_D64, MXFP8_CAUSAL, BWD_D128,
+                                 BWD_CAUSAL_D128)}
 
 
 def draw_fp32(B: int, H: int, N: int, d: int, qk_std: float = 1.0, v_std: float = 1.0,
@@ -135,3 +147,10 @@ def fp8_sim_values(keys: int = 8192, d: int = 64, seed: int = 1) -> np.ndarray:
     Tricks", section "Where 'exact' breaks: P in FP8": the page does not state
     V or d; iid N(0, 1) values and d = 64 are the reading taken here."""
     return np.random.default_rng(seed).standard_normal((keys, d))
+
+
+def draw_grad(B: int, H: int, N: int, d: int, seed: int = 1) -> np.ndarray:
+    """An upstream gradient dO for the backward pass: float32 [B,H,N,d]
+    standard normals from its own generator (the pages state no recipe for it)."""
+    return np.random.default_rng(seed).standard_normal((B, H, N, d), dtype=np.float32)
+

@@ -36,6 +36,7 @@ if ROOT not in sys.path:
 import attn_inputs as I  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s on 1xGB300 and fraction of dense BF16/FP8 peak"
+METRIC_BWD = "attention bwd TFLOP/s on 1xGB300 and fraction of dense BF16 peak"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = I.NONCAUSAL_D128.name
 L2_BYTES = 129 * 1024 * 1024
@@ -246,8 +247,65 @@ def oracle_sample(w: I.Workload, q, k, v, seconds: float, rows_per_call: int = 5
             "flop": flops}
 
 
+def oracle_bwd_sample(w: I.Workload, q, k, v, o, do, lse, seconds: float) -> dict:
+    """Time the float64 backward oracle on whole heads of the workload (at
+    least one) until `seconds` have passed; useful FLOP as the metric counts
+    them (10 N^2 d per head, halved for causal)."""
+    from oracle.backward import attention_bwd_head
+    t0 = time.perf_counter()
+    heads = 0
+    for b in range(w.B):
+        for h in range(w.H):
+            attention_bwd_head(I.as_f64(q[b, h]), I.as_f64(k[b, h]), I.as_f64(v[b, h]), I.as_f64(o[b, h]),
+                               I.as_f64(do[b, h]), lse[b, h].double().numpy(), w.causal, w.scale)
+            heads += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    flops = w.flops / (w.B * w.H) * heads
+    return {"value": flops / dt / 1e12, "seconds": dt, "heads_touched": heads, "flop": flops}
+
+
+def bench_reference_bwd(args, w: I.Workload) -> None:
+    """The reference arm of a backward workload: the float64 backward oracle on
+    the workload's first head, its O and LSE from the float64 forward oracle
+    (computed once, outside the timed steps)."""
+    from oracle.attention import attention_fwd
+    from oracle.backward import attention_bwd_head
+    q, k, v = (t[:1, :1] for t in I.bf16_qkv(w))
+    do = I.to_bf16(I.draw_grad(w.B, w.H, w.N, w.d, seed=w.seed + 1)[:1, :1])
+    qq, kk, vv, dd = (I.as_f64(t)[0, 0] for t in (q, k, v, do))
+    o, lse = attention_fwd(qq[None, None], kk[None, None], vv[None, None], w.causal, w.scale)
+    o = I.as_f64(torch.from_numpy(o).to(torch.bfloat16))[0, 0]
+    lse = lse.astype(np.float32).astype(np.float64)[0, 0]
+    head_flop = w.flops / (w.B * w.H)
+
+    def one_step():
+        t0 = time.perf_counter()
+        attention_bwd_head(qq, kk, vv, o, dd, lse, w.causal, w.scale)
+        return time.perf_counter() - t0
+    for _ in range(args.warmup):
+        one_step()
+    secs = [one_step() for _ in range(args.steps)]
+    value = head_flop / float(np.mean(secs)) / 1e12
+    cores = torch.get_num_threads()
+    sample = f"float64 backward oracle on one whole head (N = {w.N}, d = {w.d}) of the workload per step"
+    out = {"impl": "reference", "metric": METRIC_BWD, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(secs)), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {**w.describe(), "workload": w.name},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
 def bench_reference(args, w: I.Workload, world: int, rank: int) -> None:
     if rank != 0:
+        return
+    if w.direction == "bwd":
+        bench_reference_bwd(args, w)
         return
     q, k, v = I.bf16_qkv(w) if w.dtype == "bf16" else tuple(torch.from_numpy(x) for x in I.draw_fp32(
         w.B, w.H, w.N, w.d, w.qk_std, w.v_std, w.seed))
@@ -385,12 +443,74 @@ class Mxfp8Step:
                 "d2h_bytes_per_step": o_host.numel() * 2 + lse_host.numel() * 4, "steps": n_steps}
 
 
+class BwdStep:
+    """One backward pass: attn_bwd (preparation, main kernel, dQ conversion)
+    over resident Q, K, V, O, dO, LSE; O and LSE come from attn_fwd once,
+    before the timed region."""
+
+    launches = 3
+
+    def __init__(self, attn, w, dev, args):
+        self.attn, self.w, self.args = attn, w, args
+        self.tau = args.tau
+        self.q_h, self.k_h, self.v_h = I.bf16_qkv(w)
+        self.do_h = I.to_bf16(I.draw_grad(w.B, w.H, w.N, w.d, seed=w.seed + 1))
+        self.q, self.k, self.v, self.do = (t.to(dev) for t in (self.q_h, self.k_h, self.v_h, self.do_h))
+        self.o, self.lse = attn.attn_fwd(self.q, self.k, self.v, causal=w.causal, scale=w.scale)
+        torch.cuda.synchronize(dev)
+        self.o_h, self.lse_h = self.o.cpu(), self.lse.cpu()
+        self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        self.ws_bytes = attn.lib().attn_bwd_workspace_bytes(w.B, w.H, w.N, w.d)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.ptrs = tuple(t.data_ptr() for t in (self.q, self.k, self.v, self.o, self.do, self.lse, self.dq, self.dk,
+                                                 self.dv))
+
+    def run(self, sh, ev=None):
+        w = self.w
+        if ev:
+            ev[0].record()
+        st = self.attn.lib().attn_bwd(*self.ptrs, w.B, w.H, w.N, w.d, int(w.causal), float(w.scale),
+                                      self.ws.data_ptr(), self.ws_bytes, sh)
+        if ev:
+            ev[1].record()
+        if st != 0:
+            raise self.attn.AttnError(st, "attn_bwd")
+
+    def input_bytes(self):
+        return 5 * self.q.numel() * 2
+
+    def e2e(self, dev, n_steps, world):
+        w = self.w
+        src = [t.pin_memory() for t in (self.q_h, self.k_h, self.v_h, self.o_h, self.do_h, self.lse_h)]
+        dst = [self.q, self.k, self.v, self.o, self.do, self.lse]
+        outs = [torch.empty(self.dq.shape, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+        sh = torch.cuda.current_stream(dev).cuda_stream
+
+        def call():
+            for d_, h_ in zip(dst, src):
+                d_.copy_(h_, non_blocking=True)
+            self.run(sh)
+            for h_, d_ in zip(outs, (self.dq, self.dk, self.dv)):
+                h_.copy_(d_, non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+        for _ in range(2):
+            call()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(n_steps):
+            call()
+        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+        return {"value": w.flops * n_steps * world / dt / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in src),
+                "d2h_bytes_per_step": sum(h.numel() * 2 for h in outs), "steps": n_steps}
+
+
 def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
     import online_softmax_fwd_gb300 as attn
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     attn.lib()
-    step = (Mxfp8Step if w.dtype == "mxfp8" else Bf16Step)(attn, w, dev, args)
+    step = (BwdStep if w.direction == "bwd" else Mxfp8Step if w.dtype == "mxfp8" else Bf16Step)(attn, w, dev, args)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     for _ in range(args.warmup):
@@ -436,10 +556,16 @@ def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
     achieved = w.flops / avg_launch_s / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": profiled_traffic(w.name), "peak_source": src, "flop_per_launch": w.flops,
-                "kernel": "attn_fwd_mxfp8_kernel" if w.dtype == "mxfp8" else "attn_fwd_bf16_kernel"}
+                "kernel": ("attn_bwd (bwd_prep + attn_bwd_bf16_kernel + bwd_post)" if w.direction == "bwd" else
+                           "attn_fwd_mxfp8_kernel" if w.dtype == "mxfp8" else "attn_fwd_bf16_kernel")}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and w.direction == "bwd":
+        s = oracle_bwd_sample(w, step.q_h, step.k_h, step.v_h, step.o_h, step.do_h, step.lse_h, args.cpu_seconds)
+        cpu = {"value": s["value"], "unit": UNIT, "cores": torch.get_num_threads(), "kind": "oracle",
+               "sample": f"float64 backward oracle on the workload's first {s['heads_touched']} whole head(s) "
+                         f"(O and LSE from the forward kernel), {s['seconds']:.1f} s"}
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline:
         s = oracle_sample(w, *cpu_inputs(step, w), args.cpu_seconds)
         cpu = {"value": s["value"], "unit": UNIT, "cores": torch.get_num_threads(), "kind": "oracle",
                "sample": f"float64 one-shot oracle on {s['rows']} query rows of the workload's first "
@@ -447,7 +573,7 @@ def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
                          + (" (inputs: the oracle's own MXFP8 quantisation, dequantised)" if w.dtype == "mxfp8" else "")}
     clocks = sampler.summary(t_wall0, t_wall1)
     if rank == 0:
-        out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        out = {"metric": METRIC_BWD if w.direction == "bwd" else METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                "warmup": args.warmup, "ms_per_step": region_ms_max / args.steps, "higher_is_better": True,
                "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8" if w.dtype == "mxfp8" else "bf16",
                "data": "synthetic",
@@ -477,7 +603,7 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
     ap.add_argument("--shape", default=None,
-                    help="B,H,N,d[,causal[,mxfp8]] instead of a named workload (profiling a smaller case)")
+                    help="B,H,N,d[,causal[,mxfp8[,bwd]]] instead of a named workload (profiling a smaller case)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--exp2-emu16", type=int, default=0)
     ap.add_argument("--tau", type=float, default=None,
@@ -500,8 +626,10 @@ def main() -> None:
         f = [int(x) for x in args.shape.split(",")]
         causal = bool(f[4]) if len(f) > 4 else False
         dt = "mxfp8" if len(f) > 5 and f[5] else "bf16"
-        w = I.Workload(f"custom_b{f[0]}h{f[1]}n{f[2]}d{f[3]}{'_causal' if causal else ''}{'_mxfp8' if dt == 'mxfp8' else ''}",
-                       f[0], f[1], f[2], f[3], causal, dtype=dt)
+        direction = "bwd" if len(f) > 6 and f[6] else "fwd"
+        w = I.Workload(f"custom_b{f[0]}h{f[1]}n{f[2]}d{f[3]}{'_causal' if causal else ''}{'_mxfp8' if dt == 'mxfp8' else ''}"
+                       f"{'_bwd' if direction == 'bwd' else ''}", f[0], f[1], f[2], f[3], causal, dtype=dt,
+                       direction=direction)
     world, rank, local = dist_setup(args.gpus)
     try:
         if args.impl == "reference":

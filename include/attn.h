@@ -242,6 +242,34 @@ attn_status_t attn_get_device_status(void* stream);
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* attn_status_string(attn_status_t status);
 
+/*
+ * attn_bwd -- the backward pass: dQ, dK, dV of O = softmax(s Q K^T [causal
+ * mask]) V for an upstream gradient dO, with P rebuilt from the forward's LSE
+ * ("Lecture 2 - Online Softmax and Numerical Correctness", section "Use it in
+ * the real stack": the LSE side output makes the backward cheap) and the five
+ * products S, dP, dV, dK, dQ of "PyTorch FlashAttention-4 adds MXFP8
+ * block-scaled forward and backward for Blackwell", section "TMEM allocation
+ * and scale factor placement" (dK and dV accumulated per key tile):
+ *   P = exp(s Q K^T - LSE), dV = P^T dO, dP = dO V^T, D = rowsum(dO * O),
+ *   dS = P * (dP - D), dQ = s dS K, dK = s dS^T Q.
+ *
+ *   q, k, v, o, dout  bf16 [B, H, N, d] contiguous, device memory, 16-byte
+ *                     aligned: the forward's inputs, its output O and dL/dO.
+ *   lse               fp32 [B, H, N], the forward's LSE (4-byte aligned).
+ *   dq, dk, dv        bf16 [B, H, N, d] outputs, 16-byte aligned.
+ *   B, H, N, d, causal, scale   as attn_fwd (d 64 or 128).
+ *   workspace         device memory of at least attn_bwd_workspace_bytes(B,
+ *                     H, N, d) bytes, 256-byte aligned, owned by the caller:
+ *                     an fp32 dQ accumulator, D and LSE log2(e).
+ * Asynchronous on `stream` (three kernels: preparation, the main kernel, dQ
+ * conversion); nothing is allocated. Errors as attn_fwd, plus
+ * ATTN_ERR_INVALID_ARG for a null or too small workspace.
+ */
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                       const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+                       float scale, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int attn_version(void);
 

@@ -61,6 +61,10 @@ _SIGNATURES = {
     # q, k, v, o, lse (host), B, H, N, d, causal, scale, stream
     "attn_fwd_host_noalloc": ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_void_p],
                               ctypes.c_int),
+    "attn_bwd_workspace_bytes": ([ctypes.c_int] * 4, ctypes.c_size_t),
+    # q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, scale, workspace, workspace_bytes, stream
+    "attn_bwd": ([ctypes.c_void_p] * 9 + [ctypes.c_int] * 5
+                 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
     "attn_get_device_status": ([ctypes.c_void_p], ctypes.c_int),
     "attn_selftest_wait_timeout": ([ctypes.c_longlong, ctypes.c_void_p], ctypes.c_int),
     "attn_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -190,6 +194,36 @@ def attn_fwd_from_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal
         torch.cuda.current_stream(dev).synchronize() if stream is None else torch.cuda.Stream(
             stream_ptr=h, device=dev).synchronize()
     return o_host, lse_host
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, dout: torch.Tensor,
+             lse: torch.Tensor, causal: bool = False, scale: float | None = None, workspace: dict | None = None,
+             stream=None) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """dQ, dK, dV (bf16 [B,H,N,d]) through the C ABI, from the forward's inputs,
+    its output O and LSE, and the upstream gradient dout (all contiguous CUDA;
+    bf16 except lse fp32 [B,H,N]). ``workspace`` (a dict) keeps the device
+    workspace between calls of the same shape."""
+    B, H, N, d = _check_qkv(q, k, v)
+    for name, t in (("o", o), ("dout", dout)):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q on q's device")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous() or lse.device != q.device:
+        raise ValueError("lse must be a contiguous float32 tensor [B,H,N] on q's device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    need = lib().attn_bwd_workspace_bytes(B, H, N, d)
+    ws = workspace if workspace is not None else {}
+    if ws.get("key") != (need, str(q.device)):
+        ws.clear()
+        ws["key"] = (need, str(q.device))
+        ws["buf"] = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    h = _stream_handle(stream)
+    with torch.cuda.device(q.device):
+        st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                            _ptr(dv), B, H, N, d, int(bool(causal)), float(scale), _ptr(ws["buf"]), need, h)
+    _check(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def mxfp8_scale_bytes(B: int, H: int, N: int, d: int) -> int:

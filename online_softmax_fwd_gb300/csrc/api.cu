@@ -13,6 +13,8 @@
 #include <mutex>
 
 #include "attn.h"
+#include "bwd_bf16.cuh"
+#include "bwd_dispatch.h"
 #include "exp2_fma.cuh"
 #include "fwd_bf16.cuh"
 #include "fwd_dispatch.h"
@@ -87,6 +89,21 @@ bool make_map_e4m3(CUtensorMap* m, const void* base, int n, long long bh) {
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 3-D map over a contiguous [B*H, N, d] fp32 tensor for reduce-adds: 32-column
+// boxes (128 bytes, the 128-byte swizzle span) of 128 rows; rows past N are
+// not written.
+bool make_map_f32(CUtensorMap* m, void* base, int d, int n, long long bh) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4u, static_cast<cuuint64_t>(d) * 4u * static_cast<cuuint64_t>(n)};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -188,6 +205,66 @@ attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, 
   else
     e = causal ? attn::launch_fwd_bf16_d128_c1(exp2_emu16, mq, mk, mv, a, wl, ctas, s)
                : attn::launch_fwd_bf16_d128_c0(exp2_emu16, mq, mk, mv, a, wl, ctas, s);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128) || N > kMaxN) return 0;
+  const size_t bh = static_cast<size_t>(B) * H;
+  const size_t np = (static_cast<size_t>(N) + 127) / 128 * 128;
+  const size_t acc = (bh * N * d * 4 + 255) / 256 * 256;
+  return acc + 2 * ((bh * np * 4 + 255) / 256 * 256);
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                       const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+                       float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || H < 0 || N < 0 || (causal != 0 && causal != 1)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return (d > 0) ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
+  if (N > kMaxN || static_cast<long long>(B) * H * ((N + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_bwd_workspace_bytes(B, H, N, d);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_ERR_MISALIGNED;
+  const long long bh = static_cast<long long>(B) * H;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_map(&mq, q, d, N, bh) || !make_map(&mk, k, d, N, bh) || !make_map(&mv, v, d, N, bh) ||
+      !make_map(&mdo, dout, d, N, bh))
+    return ATTN_ERR_CUDA;
+  unsigned int* status = status_word();
+  if (!status) return ATTN_ERR_CUDA;
+  const int np = (N + 127) / 128 * 128;
+  const size_t acc_bytes = (static_cast<size_t>(bh) * N * d * 4 + 255) / 256 * 256;
+  const size_t vec_bytes = (static_cast<size_t>(bh) * np * 4 + 255) / 256 * 256;
+  float* dq_acc = static_cast<float*>(workspace);
+  CUtensorMap mdq;
+  if (!make_map_f32(&mdq, dq_acc, d, N, bh)) return ATTN_ERR_CUDA;
+  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes);
+  float* dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes + vec_bytes);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (attn::launch_bwd_prep(o, dout, lse, lse2, dvec, dq_acc, bh, N, np, d, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  attn::BwdArgs a;
+  a.lse2 = lse2;
+  a.dvec = dvec;
+  a.dq_acc = dq_acc;
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.status = status;
+  a.n = N;
+  a.np = np;
+  a.n_tiles = (N + 127) / 128;
+  a.bh = static_cast<int>(bh);
+  a.scale = scale;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  cudaError_t e = d == 128 ? attn::launch_bwd_bf16_d128(causal, mq, mk, mv, mdo, mdq, a, st)
+                           : attn::launch_bwd_bf16_d64(causal, mq, mk, mv, mdo, mdq, a, st);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  e = attn::launch_bwd_post(dq_acc, dq, bh * N * static_cast<long long>(d), scale, st);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

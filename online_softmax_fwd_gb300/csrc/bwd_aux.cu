@@ -1,0 +1,104 @@
+// The backward pass's two small kernels around attn_bwd_bf16_kernel:
+//   bwd_prep: D_i = sum_c dO_ic O_ic (fp32 from bf16) and LSE_i log2(e) for
+//             every query row (rows N .. np-1 of a head get 0), and the fp32
+//             dQ accumulator zeroed;
+//   bwd_post: dQ = s * accumulator, rounded to bf16.
+// Both are bandwidth-bound elementwise passes.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "bwd_dispatch.h"
+
+namespace attn {
+
+namespace {
+
+// one warp per query row; lane l takes elements [D/32 l, D/32 (l+1))
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
+                                                       const __nv_bfloat16* __restrict__ dout,
+                                                       const float* __restrict__ lse, float* __restrict__ lse2,
+                                                       float* __restrict__ dvec, float* __restrict__ dq_acc, int n,
+                                                       int np) {
+  constexpr int kPer = D / 32;  // 2 or 4 bf16 per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + warp;
+  const long long bh = blockIdx.y;
+  if (row >= np) return;
+  const size_t prow = static_cast<size_t>(bh) * np + row;
+  if (row >= n) {
+    if (lane == 0) {
+      lse2[prow] = 0.f;
+      dvec[prow] = 0.f;
+    }
+    return;
+  }
+  const size_t grow = static_cast<size_t>(bh) * n + row;
+  float acc = 0.f;
+  if constexpr (kPer == 4) {
+    const uint2 a = reinterpret_cast<const uint2*>(o + grow * D)[lane];
+    const uint2 b = reinterpret_cast<const uint2*>(dout + grow * D)[lane];
+    const uint32_t aw[2] = {a.x, a.y}, bw[2] = {b.x, b.y};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      acc = __fmaf_rn(__uint_as_float(aw[e] << 16), __uint_as_float(bw[e] << 16), acc);
+      acc = __fmaf_rn(__uint_as_float(aw[e] & 0xFFFF0000u), __uint_as_float(bw[e] & 0xFFFF0000u), acc);
+    }
+  } else {
+    const uint32_t a = reinterpret_cast<const uint32_t*>(o + grow * D)[lane];
+    const uint32_t b = reinterpret_cast<const uint32_t*>(dout + grow * D)[lane];
+    acc = __fmaf_rn(__uint_as_float(a << 16), __uint_as_float(b << 16), acc);
+    acc = __fmaf_rn(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(b & 0xFFFF0000u), acc);
+  }
+#pragma unroll
+  for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+  if (lane == 0) {
+    dvec[prow] = acc;
+    lse2[prow] = lse[grow] * 1.4426950408889634f;
+  }
+  float4* z = reinterpret_cast<float4*>(dq_acc + grow * D);
+#pragma unroll
+  for (int e = lane; e < D / 4; e += 32) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// four elements per thread
+__global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
+                                                       long long n4, float scale) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const float4 a = reinterpret_cast<const float4*>(dq_acc)[i];
+  __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * scale, a.y * scale);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * scale, a.w * scale);
+  uint2 w;
+  w.x = *reinterpret_cast<uint32_t*>(&lo);
+  w.y = *reinterpret_cast<uint32_t*>(&hi);
+  reinterpret_cast<uint2*>(dq)[i] = w;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* lse2, float* dvec,
+                            float* dq_acc, long long bh, int n, int np, int d, cudaStream_t stream) {
+  dim3 grid(static_cast<unsigned>(np / 8), static_cast<unsigned>(bh));
+  if (d == 128)
+    bwd_prep_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
+                                                   static_cast<const __nv_bfloat16*>(dout), lse, lse2, dvec, dq_acc,
+                                                   n, np);
+  else
+    bwd_prep_kernel<64><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
+                                                  static_cast<const __nv_bfloat16*>(dout), lse, lse2, dvec, dq_acc,
+                                                  n, np);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long elems, float scale, cudaStream_t stream) {
+  const long long n4 = elems / 4;
+  const long long blocks = (n4 + 255) / 256;
+  bwd_post_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n4,
+                                                                     scale);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,20 @@
+// Host-side launchers of the backward pass's kernels (bwd_*.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+struct BwdArgs;
+
+cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, float* lse2, float* dvec,
+                            float* dq_acc, long long bh, int n, int np, int d, cudaStream_t stream);
+cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long elems, float scale, cudaStream_t stream);
+// dq: 3-D map over the fp32 dQ accumulator [B*H, N, d], 32-column boxes of 128 rows, 128-byte swizzle
+cudaError_t launch_bwd_bf16_d64(int causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                const CUtensorMap& dout, const CUtensorMap& dq, const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_bf16_d128(int causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                 const CUtensorMap& dout, const CUtensorMap& dq, const BwdArgs& a, cudaStream_t s);
+
+}  // namespace attn

@@ -28,10 +28,15 @@ import numpy as np
 
 
 def attention_bwd_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarray, do: np.ndarray,
-                       lse: np.ndarray, causal: bool, scale: float,
-                       row_chunk: int = 512) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+                       lse: np.ndarray, causal: bool, scale: float, row_chunk: int = 512,
+                       p_cast=None, ds_cast=None) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
     """dQ, dK, dV (float64) of one (batch, head): q [N, d], k [N, d], v [N, dv],
-    o and do [N, dv], lse [N] (natural log of the scaled scores' row sums)."""
+    o and do [N, dv], lse [N] (natural log of the scaled scores' row sums).
+
+    ``p_cast`` / ``ds_cast`` (optional) round P before it enters dV and dS,
+    and dS before it enters dQ and dK, to a matrix-multiply input type: the
+    same method in the precision a kernel feeds its tensor cores, for tight
+    parity checks (the forward's reading: P takes the MMA input type)."""
     q, k, v, o, do, lse = (np.asarray(x, dtype=np.float64) for x in (q, k, v, o, do, lse))
     n = q.shape[0]
     dq = np.zeros_like(q)
@@ -45,9 +50,13 @@ def attention_bwd_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarra
         if causal:
             j = np.arange(k.shape[0])[None, :]
             p = np.where(j <= np.arange(i0, i1)[:, None], p, 0.0)
+        if p_cast is not None:
+            p = np.asarray(p_cast(p), dtype=np.float64)
         dv += p.T @ do[i0:i1]
         dp = do[i0:i1] @ v.T
         ds = p * (dp - d_row[i0:i1, None])
+        if ds_cast is not None:
+            ds = np.asarray(ds_cast(ds), dtype=np.float64)
         dq[i0:i1] = scale * (ds @ k)
         dk += scale * (ds.T @ q[i0:i1])
     return dq, dk, dv
@@ -65,3 +74,30 @@ def attention_bwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarray, do
             for dst, src in zip(out, g):
                 dst[b, h] = src
     return out[0], out[1], out[2]
+
+
+def attention_bwd_abs_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarray, do: np.ndarray,
+                           lse: np.ndarray, causal: bool, scale: float,
+                           row_chunk: int = 512) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """The same three products with every factor replaced by its absolute
+    value: s |dS| |K|, s |dS|^T |Q|, |P|^T |dO| (float64). They bound how far
+    a rounding of P or dS by a relative epsilon can move each output element,
+    which is how the GPU tests size their tolerances."""
+    q, k, v, o, do, lse = (np.asarray(x, dtype=np.float64) for x in (q, k, v, o, do, lse))
+    n = q.shape[0]
+    aq = np.zeros_like(q)
+    ak = np.zeros_like(k)
+    av = np.zeros_like(v)
+    d_row = (do * o).sum(axis=1)
+    for i0 in range(0, n, row_chunk):
+        i1 = min(n, i0 + row_chunk)
+        p = np.exp(scale * (q[i0:i1] @ k.T) - lse[i0:i1, None])
+        if causal:
+            j = np.arange(k.shape[0])[None, :]
+            p = np.where(j <= np.arange(i0, i1)[:, None], p, 0.0)
+        av += p.T @ np.abs(do[i0:i1])
+        ds = np.abs(p * (do[i0:i1] @ v.T - d_row[i0:i1, None]))
+        aq[i0:i1] = scale * (ds @ np.abs(k))
+        ak += scale * (ds.T @ np.abs(q[i0:i1]))
+    return aq, ak, av
+

@@ -147,3 +147,29 @@ def test_host_noalloc_limits_and_validation(lib):
     assert call(1, 2, 256, 96) == 2         # unsupported head dim, as attn_fwd_host
     assert call(1, -2, 256, 64) == 1
     assert call(0, 2, 256, 64) == 0         # nothing to do
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    A = 1 << 20  # fake, 256-byte aligned addresses: rejected calls never dereference them
+    B, H, N, d = 1, 2, 300, 128
+    need = lib.attn_bwd_workspace_bytes(B, H, N, d)
+    # fp32 dQ accumulator + two padded fp32 row vectors (LSE log2 e, D)
+    assert need == (B * H * N * d * 4 + 255) // 256 * 256 + 2 * ((B * H * 384 * 4 + 255) // 256 * 256)
+    assert lib.attn_bwd_workspace_bytes(B, H, N, 96) == 0
+    assert lib.attn_bwd_workspace_bytes(0, H, N, d) == 0
+
+    def args(ws=A * 9, ws_bytes=need, d_=d, causal=1, scale=0.1, b=B, q=A, lse=A * 6):
+        return (q, A * 2, A * 3, A * 4, A * 5, lse, A * 7, A * 8, A * 10, b, H, N, d_, causal, scale, ws, ws_bytes,
+                None)
+
+    assert lib.attn_bwd(*args(d_=96)) == 2
+    assert lib.attn_bwd(*args(d_=0)) == 1
+    assert lib.attn_bwd(*args(causal=2)) == 1
+    assert lib.attn_bwd(*args(scale=0.0)) == 1
+    assert lib.attn_bwd(*args(scale=float("nan"))) == 1
+    assert lib.attn_bwd(*args(ws_bytes=need - 1)) == 1
+    assert lib.attn_bwd(*args(ws=0)) == 1
+    assert lib.attn_bwd(*args(q=A + 8)) == 3
+    assert lib.attn_bwd(*args(lse=A * 6 + 2)) == 3
+    assert lib.attn_bwd(*args(ws=A * 9 + 16)) == 3
+    assert lib.attn_bwd(*args(b=0)) == 0     # nothing to do
