@@ -17,9 +17,9 @@
 //   dQ_i (+)= dS K_j                               (fp32 reduction in global)
 //
 //   warps 0-3   thread = key row: P^T and dS^T, then the dK, dV epilogue
-//   warps 4-7   thread = query row: dQ_i out of TMEM, through the dS buffer
-//               (free again once the dQ product has read it) into TMA
-//               reduce-adds onto the fp32 dQ
+//   warps 4-7   thread = query row: dQ_i out of TMEM, through the stage's dO_i
+//               buffer (free once the dV product has read it; handed back to
+//               the TMA warp afterwards) into TMA reduce-adds onto the fp32 dQ
 //   warp 8      TMA: K_j, V_j once; Q_i, dO_i into a ring of stages
 //   warp 9      MMA issuer (one elected lane)
 //
@@ -71,8 +71,9 @@ struct BwdCfg {
   static constexpr uint32_t kDsOff = kStageOff + kStages * kStageBytes;
   static constexpr uint32_t kDsBytes = 2 * kBoxBytes;          // 128 keys x 128 queries bf16
   static constexpr uint32_t kBarOff = kDsOff + kDsBytes;
-  // kv, full[kStages], empty[kStages], s, dp, p, ds, dv_done, k_done, dq, ds_free, dq_read, fin, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 11;
+  // kv, q_full[kStages], q_free[kStages], do_full[kStages], do_free[kStages], s, dp, p, ds, dv_done, k_done,
+  // dq, ds_free, dq_read, fin, drain
+  static constexpr int kNumBars = 1 + 4 * kStages + 11;
   static constexpr uint32_t kHolderOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kAbortOff = kHolderOff + 4;
   // the 1024-byte alignment of the tiles takes up to 1008 bytes of slack; at
@@ -166,9 +167,13 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sbase = smem_addr(smem);
   const uint32_t bar0 = sbase + C::kBarOff;
   const uint32_t bar_kv = bar0;
-  auto bar_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto bar_empty = [&](int s) { return bar0 + 8u * (1 + C::kStages + s); };
-  const uint32_t bar_s = bar0 + 8u * (1 + 2 * C::kStages);
+  // a stage's Q_i (with LSE_i log2 e and D_i) and dO_i are loaded and freed separately:
+  // Q_i is free after the dK product, dO_i after dQ_i has gone out through its buffer
+  auto bar_qfull = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_qfree = [&](int s) { return bar0 + 8u * (1 + C::kStages + s); };
+  auto bar_dofull = [&](int s) { return bar0 + 8u * (1 + 2 * C::kStages + s); };
+  auto bar_dofree = [&](int s) { return bar0 + 8u * (1 + 3 * C::kStages + s); };
+  const uint32_t bar_s = bar0 + 8u * (1 + 4 * C::kStages);
   const uint32_t bar_dp = bar_s + 8u;
   const uint32_t bar_p = bar_s + 16u;
   const uint32_t bar_ds = bar_s + 24u;
@@ -194,8 +199,10 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar_kv, 1);
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 1);
+      mbar_init(bar_qfull(s), 1);
+      mbar_init(bar_qfree(s), 1);
+      mbar_init(bar_dofull(s), 1);
+      mbar_init(bar_dofree(s), 1);  // arrived by the dQ warpgroup once its reduce-adds have read the buffer
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
@@ -204,7 +211,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(bar_dvdone, 1);
     mbar_init(bar_kdone, 1);
     mbar_init(bar_dq, 1);
-    mbar_init(bar_dsfree, 1);  // arrived by the dQ warpgroup once its reduce-adds have read the buffer
+    mbar_init(bar_dsfree, 1);
     mbar_init(bar_dqread, 128);
     mbar_init(bar_fin, 1);
     mbar_init(bar_drain, 1);
@@ -239,29 +246,52 @@ __global__ void __launch_bounds__(384, 1)
         tma_load_3d_hint(sbase + C::kVOff + b * C::kBoxBytes, &tm_v, bar_kv, b * 64, j * 128, bh, pol_stream);
       }
     }
-    for (; it < n_it; ++it) {
-      const int st = it % C::kStages;
-      const uint32_t ph = static_cast<uint32_t>(it / C::kStages) & 1u;
-      ok = __all_sync(0xffffffffu, wait_bar(bar_empty(st), ph ^ 1u, abort_flag, args.status, 30));
-      if (!ok) break;
+    // Q_i (and its vectors) one iteration ahead of dO_i: the S^T product needs
+    // Q_{i+1} before the dP^T product needs dO_{i+1}
+    int nq = 0, ndo = 0;  // loads issued
+    auto load_q = [&](int i) {
+      const int st = i % C::kStages;
+      const uint32_t ph = static_cast<uint32_t>(i / C::kStages) & 1u;
+      if (!__all_sync(0xffffffffu, wait_bar(bar_qfree(st), ph ^ 1u, abort_flag, args.status, 30))) return false;
       if (leader) {
-        const int row = (i0 + it) * 128;
+        const int row = (i0 + i) * 128;
         const uint32_t dst = sbase + C::kStageOff + st * C::kStageBytes;
-        mbar_arrive_expect_tx(bar_full(st), 2 * C::kTileBytes + 1024);
+        mbar_arrive_expect_tx(bar_qfull(st), C::kTileBytes + 1024);
 #pragma unroll
-        for (int b = 0; b < C::kBoxes; ++b) {
-          tma_load_3d_hint(dst + b * C::kBoxBytes, &tm_q, bar_full(st), b * 64, row, bh, pol_keep);
-          tma_load_3d_hint(dst + C::kTileBytes + b * C::kBoxBytes, &tm_do, bar_full(st), b * 64, row, bh, pol_keep);
-        }
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_3d_hint(dst + b * C::kBoxBytes, &tm_q, bar_qfull(st), b * 64, row, bh, pol_keep);
         const size_t vrow = static_cast<size_t>(bh) * args.np + row;
-        bulk_g2s(dst + C::kVecOff, args.lse2 + vrow, 512, bar_full(st));
-        bulk_g2s(dst + C::kVecOff + 512, args.dvec + vrow, 512, bar_full(st));
+        bulk_g2s(dst + C::kVecOff, args.lse2 + vrow, 512, bar_qfull(st));
+        bulk_g2s(dst + C::kVecOff + 512, args.dvec + vrow, 512, bar_qfull(st));
       }
+      ++nq;
+      return true;
+    };
+    auto load_do = [&](int i) {
+      const int st = i % C::kStages;
+      const uint32_t ph = static_cast<uint32_t>(i / C::kStages) & 1u;
+      if (!__all_sync(0xffffffffu, wait_bar(bar_dofree(st), ph ^ 1u, abort_flag, args.status, 29))) return false;
+      if (leader) {
+        const uint32_t dst = sbase + C::kStageOff + st * C::kStageBytes + C::kTileBytes;
+        mbar_arrive_expect_tx(bar_dofull(st), C::kTileBytes);
+#pragma unroll
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_3d_hint(dst + b * C::kBoxBytes, &tm_do, bar_dofull(st), b * 64, (i0 + i) * 128, bh, pol_keep);
+      }
+      ++ndo;
+      return true;
+    };
+    ok = load_q(0);
+    for (; ok && it < n_it; ++it) {
+      if (it + 1 < n_it) ok = load_q(it + 1);
+      if (ok) ok = load_do(it);
     }
     if (!ok) {
       drain_bar(bar_kv, 0);
-      for (int s = it - C::kStages < 0 ? 0 : it - C::kStages; s < it; ++s)
-        drain_bar(bar_full(s % C::kStages), (s / C::kStages) & 1);
+      for (int s = nq - C::kStages < 0 ? 0 : nq - C::kStages; s < nq; ++s)
+        drain_bar(bar_qfull(s % C::kStages), (s / C::kStages) & 1);
+      for (int s = ndo - C::kStages < 0 ? 0 : ndo - C::kStages; s < ndo; ++s)
+        drain_bar(bar_dofull(s % C::kStages), (s / C::kStages) & 1);
     }
     __syncwarp();
   } else if (warp == 9) {
@@ -328,11 +358,15 @@ __global__ void __launch_bounds__(384, 1)
           mma_ss_lo(tmem + C::kColDq, a + kk * 128, b + kk * 128, desc_hi, kIdDq, kk > 0 ? 1u : 0u);
       }
     };
-    bool ok = wait(bar_kv, 0, 31) && wait(bar_full(0), 0, 32);
+    bool ok = wait(bar_kv, 0, 31) && wait(bar_qfull(0), 0, 32);
     if (ok) {
       tc_fence_after();
       issue_sq(k_km, st_km, C::kColS);
       commit(bar_s);
+      ok = wait(bar_dofull(0), 0, 39);
+    }
+    if (ok) {
+      tc_fence_after();
       issue_sq(v_km, st_km + kTileStep, C::kColDp);
       commit(bar_dp);
     }
@@ -349,12 +383,12 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       issue_acc(C::kColDp, st_mn + st * kStageStep, C::kColDk, it == 0);  // B = Q_i
       commit(bar_kdone);
-      commit(bar_empty(st));
+      commit(bar_qfree(st));
       const bool more = it + 1 < n_it;
       const int st1 = (it + 1) % C::kStages;
       if (more) {
         // S^T(i+1) overwrites P^T(i) once the dV product has read it
-        ok = wait(bar_full(st1), static_cast<uint32_t>((it + 1) / C::kStages) & 1u, 35) &&
+        ok = wait(bar_qfull(st1), static_cast<uint32_t>((it + 1) / C::kStages) & 1u, 35) &&
              wait(bar_dvdone, par, 36);
         if (!ok) break;
         tc_fence_after();
@@ -367,9 +401,11 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       issue_dq();
       commit(bar_dq);
+      commit(bar_dsfree);
       if (more) {
         // dP^T(i+1) overwrites dQ_i once the dQ warps have loaded it
-        ok = wait(bar_dqread, par, 38);
+        ok = wait(bar_dqread, par, 38) &&
+             wait(bar_dofull(st1), static_cast<uint32_t>((it + 1) / C::kStages) & 1u, 46);
         if (!ok) break;
         tc_fence_after();
         issue_sq(v_km, st_km + st1 * kStageStep + kTileStep, C::kColDp);
@@ -404,7 +440,7 @@ __global__ void __launch_bounds__(384, 1)
       // S^T(i) is complete, and the stage's vectors have landed (the stage is
       // refilled only after this warpgroup's dS^T(i) has been consumed)
       ok = __all_sync(0xffffffffu, wait_bar(bar_s, par, abort_flag, args.status, 40) &&
-                                       wait_bar(bar_full(it % C::kStages),
+                                       wait_bar(bar_qfull(it % C::kStages),
                                                 static_cast<uint32_t>(it / C::kStages) & 1u, abort_flag,
                                                 args.status, 45));
       if (!ok) break;
@@ -440,8 +476,7 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(bar_p);
       // dS^T = P^T (dP^T - D); the dS buffer in shared memory is free once the
-      // previous dQ product has read it and the dQ warpgroup has moved that
-      // dQ through it
+      // previous dQ product has read it
       ok = __all_sync(0xffffffffu, wait_bar(bar_dp, par, abort_flag, args.status, 41));
       if (ok && it > 0) ok = __all_sync(0xffffffffu, wait_bar(bar_dsfree, par ^ 1u, abort_flag, args.status, 42));
       if (!ok) break;
@@ -512,14 +547,14 @@ __global__ void __launch_bounds__(384, 1)
   } else {
     // ------------------------------------------------------------ dQ (thread = query row)
     // dQ_i leaves TMEM at once (the next dP^T may then take its columns) and
-    // goes out in 64-column halves through the dS buffer: two 32-column fp32
-    // boxes (128-byte rows, 128-byte swizzle) per half, each reduce-added onto
-    // the fp32 dQ by one TMA operation; the buffer is handed back to the P/dS
-    // warpgroup once the last operation has read it.
+    // goes out through dO_i's buffer (the dV product that read dO_i is
+    // complete before dQ_i is computed) in two rounds of half its columns, as
+    // 32-column fp32 boxes (128-byte rows, 128-byte swizzle), each
+    // reduce-added onto the fp32 dQ by one TMA operation; the buffer goes
+    // back to the TMA warp once they have read it.
     const int q = (warp - 4) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
     const bool issuer = q == 0;
-    const uint32_t stage_row = sbase + C::kDsOff + q * 128;
     bool ok = true;
     for (int it = 0; ok && it < n_it; ++it) {
       ok = dq_group_all(wait_bar(bar_dq, static_cast<uint32_t>(it) & 1u, abort_flag, args.status, 44));
@@ -531,35 +566,38 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(bar_dqread);
-      const int row0 = (i0 + it) * 128;
+      const int st = it % C::kStages;
+      const uint32_t buf = sbase + C::kStageOff + st * C::kStageBytes + C::kTileBytes;  // dO_i's buffer
+      const uint32_t buf_row = buf + q * 128;
+      constexpr int kPer = D / 64;  // 32-column boxes per round (the buffer holds half of dQ_i)
 #pragma unroll
-      for (int h = 0; h < D / 64; ++h) {
+      for (int h = 0; h < 2; ++h) {
         if (h > 0) {
-          // the previous half's reduce-adds have read the buffer
+          // the first round's reduce-adds have read the buffer
           if (issuer) bulk_wait_read();
           dq_group_sync();
         }
 #pragma unroll
-        for (int bb = 0; bb < 2; ++bb) {
-          reg_fence32(u[2 * h + bb]);
+        for (int b = 0; b < kPer; ++b) {
+          reg_fence32(u[h * kPer + b]);
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4)
-            st_shared_v4(stage_row + bb * C::kBoxBytes + ((static_cast<uint32_t>(c4) ^ static_cast<uint32_t>(q & 7)) << 4),
-                         u[2 * h + bb][4 * c4], u[2 * h + bb][4 * c4 + 1], u[2 * h + bb][4 * c4 + 2],
-                         u[2 * h + bb][4 * c4 + 3]);
+            st_shared_v4(buf_row + b * C::kBoxBytes + ((static_cast<uint32_t>(c4) ^ static_cast<uint32_t>(q & 7)) << 4),
+                         u[h * kPer + b][4 * c4], u[h * kPer + b][4 * c4 + 1], u[h * kPer + b][4 * c4 + 2],
+                         u[h * kPer + b][4 * c4 + 3]);
         }
         fence_async_shared();
         dq_group_sync();
         if (issuer) {
 #pragma unroll
-          for (int bb = 0; bb < 2; ++bb)
-            tma_reduce_add_3d(&tm_dq, sbase + C::kDsOff + bb * C::kBoxBytes, 64 * h + 32 * bb, row0, bh);
+          for (int b = 0; b < kPer; ++b)
+            tma_reduce_add_3d(&tm_dq, buf + b * C::kBoxBytes, 32 * (h * kPer + b), (i0 + it) * 128, bh);
           bulk_commit();
         }
       }
       if (issuer) {
         bulk_wait_read();
-        mbar_arrive(bar_dsfree);
+        mbar_arrive(bar_dofree(st));
       }
       __syncwarp();
     }
