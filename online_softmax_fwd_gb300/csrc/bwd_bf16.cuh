@@ -70,7 +70,11 @@ struct BwdCfg {
   static constexpr uint32_t kStageBytes = 2 * kTileBytes + 1024;
   static constexpr uint32_t kDsOff = kStageOff + kStages * kStageBytes;
   static constexpr uint32_t kDsBytes = 2 * kBoxBytes;          // 128 keys x 128 queries bf16
-  static constexpr uint32_t kBarOff = kDsOff + kDsBytes;
+  // d = 64 has room for a buffer of its own for dQ on its way out (two fp32
+  // 32-column boxes); d = 128 sends dQ through dO's buffer instead
+  static constexpr bool kOwnDqBuf = D == 64;
+  static constexpr uint32_t kDqBufOff = kDsOff + kDsBytes;
+  static constexpr uint32_t kBarOff = kDqBufOff + (kOwnDqBuf ? 2 * kBoxBytes : 0);
   // kv, q_full[kStages], q_free[kStages], do_full[kStages], do_free[kStages], s, dp, p, ds, dv_done, k_done,
   // dq, ds_free, dq_read, fin, drain
   static constexpr int kNumBars = 1 + 4 * kStages + 11;
@@ -202,7 +206,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar_qfull(s), 1);
       mbar_init(bar_qfree(s), 1);
       mbar_init(bar_dofull(s), 1);
-      mbar_init(bar_dofree(s), 1);  // arrived by the dQ warpgroup once its reduce-adds have read the buffer
+      // d = 128: arrived by the dQ warpgroup once its reduce-adds have read the buffer; d = 64: by the dV product
+      mbar_init(bar_dofree(s), 1);
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
@@ -378,16 +383,12 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       issue_acc(C::kColS, st_mn + st * kStageStep + kTileStep, C::kColDv, it == 0);  // B = dO_i
       commit(bar_dvdone);
-      ok = wait(bar_ds, par, 34);
-      if (!ok) break;
-      tc_fence_after();
-      issue_acc(C::kColDp, st_mn + st * kStageStep, C::kColDk, it == 0);  // B = Q_i
-      commit(bar_kdone);
-      commit(bar_qfree(st));
+      if constexpr (C::kOwnDqBuf) commit(bar_dofree(st));  // dO_i is read by this product alone
       const bool more = it + 1 < n_it;
       const int st1 = (it + 1) % C::kStages;
       if (more) {
-        // S^T(i+1) overwrites P^T(i) once the dV product has read it
+        // S^T(i+1) overwrites P^T(i) once the dV product has read it; issued
+        // before dK(i) so the P/dS warpgroup finds it ready after dS^T(i)
         ok = wait(bar_qfull(st1), static_cast<uint32_t>((it + 1) / C::kStages) & 1u, 35) &&
              wait(bar_dvdone, par, 36);
         if (!ok) break;
@@ -395,6 +396,12 @@ __global__ void __launch_bounds__(384, 1)
         issue_sq(k_km, st_km + st1 * kStageStep, C::kColS);
         commit(bar_s);
       }
+      ok = wait(bar_ds, par, 34);
+      if (!ok) break;
+      tc_fence_after();
+      issue_acc(C::kColDp, st_mn + st * kStageStep, C::kColDk, it == 0);  // B = Q_i
+      commit(bar_kdone);
+      commit(bar_qfree(st));
       // dQ_i overwrites dS^T(i) once the dK product has read it
       ok = wait(bar_kdone, par, 37);
       if (!ok) break;
@@ -548,10 +555,9 @@ __global__ void __launch_bounds__(384, 1)
     // ------------------------------------------------------------ dQ (thread = query row)
     // dQ_i leaves TMEM at once (the next dP^T may then take its columns) and
     // goes out through dO_i's buffer (the dV product that read dO_i is
-    // complete before dQ_i is computed) in two rounds of half its columns, as
-    // 32-column fp32 boxes (128-byte rows, 128-byte swizzle), each
-    // reduce-added onto the fp32 dQ by one TMA operation; the buffer goes
-    // back to the TMA warp once they have read it.
+    // complete before dQ_i is computed) as 32-column fp32 boxes (128-byte
+    // rows, 128-byte swizzle), each reduce-added onto the fp32 dQ by one TMA
+    // operation; the buffer goes back to the TMA warp once they have read it.
     const int q = (warp - 4) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
     const bool issuer = q == 0;
@@ -567,35 +573,44 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(bar_dqread);
       const int st = it % C::kStages;
-      const uint32_t buf = sbase + C::kStageOff + st * C::kStageBytes + C::kTileBytes;  // dO_i's buffer
-      const uint32_t buf_row = buf + q * 128;
-      constexpr int kPer = D / 64;  // 32-column boxes per round (the buffer holds half of dQ_i)
+      // dO_i's buffer, or at d = 64 the dQ buffer
+      const uint32_t buf = C::kOwnDqBuf ? sbase + C::kDqBufOff
+                                        : sbase + C::kStageOff + st * C::kStageBytes + C::kTileBytes;
+      // one 32-column box at a time through the buffer's box slots, each box
+      // its own bulk group, so writing the next box overlaps the reduce-add
+      // of the previous ones
+      constexpr int kSlots = C::kOwnDqBuf ? 2 : C::kBoxes;
+      if (C::kOwnDqBuf && it > 0) {
+        // the previous dQ's reduce-adds have read the buffer
+        if (issuer) bulk_wait_read();
+        dq_group_sync();
+      }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (h > 0) {
-          // the first round's reduce-adds have read the buffer
-          if (issuer) bulk_wait_read();
+      for (int bb = 0; bb < D / 32; ++bb) {
+        const uint32_t slot = buf + (bb % kSlots) * C::kBoxBytes;
+        if (bb >= kSlots) {
+          // the reduce-add that last used this slot has read it
+          if (issuer) {
+            if constexpr (kSlots == 2)
+              asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+            else
+              bulk_wait_read();
+          }
           dq_group_sync();
         }
+        reg_fence32(u[bb]);
 #pragma unroll
-        for (int b = 0; b < kPer; ++b) {
-          reg_fence32(u[h * kPer + b]);
-#pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4)
-            st_shared_v4(buf_row + b * C::kBoxBytes + ((static_cast<uint32_t>(c4) ^ static_cast<uint32_t>(q & 7)) << 4),
-                         u[h * kPer + b][4 * c4], u[h * kPer + b][4 * c4 + 1], u[h * kPer + b][4 * c4 + 2],
-                         u[h * kPer + b][4 * c4 + 3]);
-        }
+        for (int c4 = 0; c4 < 8; ++c4)
+          st_shared_v4(slot + q * 128 + ((static_cast<uint32_t>(c4) ^ static_cast<uint32_t>(q & 7)) << 4),
+                       u[bb][4 * c4], u[bb][4 * c4 + 1], u[bb][4 * c4 + 2], u[bb][4 * c4 + 3]);
         fence_async_shared();
         dq_group_sync();
         if (issuer) {
-#pragma unroll
-          for (int b = 0; b < kPer; ++b)
-            tma_reduce_add_3d(&tm_dq, buf + b * C::kBoxBytes, 32 * (h * kPer + b), (i0 + it) * 128, bh);
+          tma_reduce_add_3d(&tm_dq, slot, 32 * bb, (i0 + it) * 128, bh);
           bulk_commit();
         }
       }
-      if (issuer) {
+      if (!C::kOwnDqBuf && issuer) {
         bulk_wait_read();
         mbar_arrive(bar_dofree(st));
       }
