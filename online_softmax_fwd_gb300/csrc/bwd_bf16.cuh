@@ -16,17 +16,18 @@
 //   dV_j += P^T dO_i,   dK_j += dS^T Q_i           (A operands from TMEM)
 //   dQ_i (+)= dS K_j                               (fp32 reduction in global)
 //
-//   warps 0-3   thread = key row: P^T and dS^T, then the dK, dV epilogue
-//   warps 4-7   thread = query row: dQ_i out of TMEM, through the stage's dO_i
+//   warps 0-7   thread = key row (warps w and w + 4 share rows and split the
+//               128 queries): P^T and dS^T, then the dK, dV epilogue
+//   warps 8-11  thread = query row: dQ_i out of TMEM, through the stage's dO_i
 //               buffer (free once the dV product has read it; handed back to
 //               the TMA warp afterwards) into TMA reduce-adds onto the fp32 dQ
-//   warp 8      TMA: K_j, V_j once; Q_i, dO_i into a ring of stages
-//   warp 9      MMA issuer (one elected lane)
+//   warp 12     TMA: K_j, V_j once; Q_i, dO_i into a ring of stages
+//   warp 13     MMA issuer (one elected lane)
 //
 // TMEM: S^T (P^T as bf16 pairs over its first 64 columns) at 0, dP^T (dS^T
-// over its first 64) at 128, dV at 256, dK at 256 + d. dQ_i reuses the dP^T
-// columns once the dK product has read dS^T; the next dP^T waits until the
-// dQ warps have loaded dQ_i. dS also goes to shared memory, keys x queries
+// over its first 64) at 128, dV at 256, dK at 256 + d, and at d = 64 dQ_i at
+// 384. At d = 128 dQ_i reuses the dP^T columns once the dK product has read
+// dS^T, and the next dP^T waits until the dQ warps have loaded dQ_i. dS also goes to shared memory, keys x queries
 // with queries contiguous, as the MN-major A operand of the dQ product.
 #pragma once
 
@@ -87,16 +88,19 @@ struct BwdCfg {
   static constexpr uint32_t kSmemBytes = kUsed + 1024 <= 232448u ? kUsed + 1024 : 232448u;
   static constexpr uint32_t kSlack = kSmemBytes - kUsed;
   static_assert(kUsed + 256 <= 232448u, "shared memory");
-  static constexpr int kThreads = 384;
-  // setmaxnreg: the P/dS warpgroup grows, the producer warpgroup shrinks, the
-  // dQ warpgroup keeps the launch count; 4 warps x 32 x (232 + 168 + 104) =
-  // 384 threads x 168 at launch
-  static constexpr uint32_t kRegsDs = 232;
-  static constexpr uint32_t kRegsProducer = 104;
-  static constexpr int kLaunchRegs = 168;
-  static_assert(kRegsDs + kLaunchRegs + kRegsProducer <= 3 * kLaunchRegs, "register split");
+  static constexpr int kThreads = 512;
+  static constexpr int kDqWarp0 = 8, kTmaWarp = 12, kMmaWarp = 13;
+  // setmaxnreg: 4 warps x 32 x (2 x 136 + 152 + 88) = 512 threads x 128 at launch
+  static constexpr uint32_t kRegsDs = 136;
+  static constexpr uint32_t kRegsDq = 152;
+  static constexpr uint32_t kRegsProducer = 88;
+  static constexpr int kLaunchRegs = 128;
+  static_assert(2 * kRegsDs + kRegsDq + kRegsProducer <= 4 * kLaunchRegs, "register split");
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 256 + D, kColDq = 128;
+  // dQ_i has columns of its own at d = 64; at d = 128 it reuses dP^T's
+  static constexpr bool kDqAlias = D == 128;
+  static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 256 + D,
+                            kColDq = kDqAlias ? 128 : 256 + 2 * D;
 };
 
 // tcgen05 instruction descriptor, kind::f16, bf16 A and B, fp32 D, with the
@@ -135,6 +139,22 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // this thread's bulk groups are complete
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// barrier among the 64 threads of P/dS warps w and w + 4 (ids 2 .. 5)
+__device__ __forceinline__ void pair_sync(int quad) {
+  asm volatile("bar.sync %0, 64;" ::"r"(2 + quad) : "memory");
+}
+__device__ __forceinline__ bool pair_all(int quad, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %2, 0;\n\t"
+      "bar.red.and.pred p, %1, 64, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(2 + quad), "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
 // barrier among the 128 threads of the dQ warpgroup
 __device__ __forceinline__ void dq_group_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 // the same barrier, returning whether `v` holds in all 128 threads (so the
@@ -156,7 +176,7 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     attn_bwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                          const __grid_constant__ CUtensorMap tm_dq, const BwdArgs args) {
@@ -211,8 +231,8 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
-    mbar_init(bar_p, 128);
-    mbar_init(bar_ds, 128);
+    mbar_init(bar_p, 256);
+    mbar_init(bar_ds, 256);
     mbar_init(bar_dvdone, 1);
     mbar_init(bar_kdone, 1);
     mbar_init(bar_dq, 1);
@@ -223,7 +243,7 @@ __global__ void __launch_bounds__(384, 1)
     *abort_flag = 0u;
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == C::kMmaWarp) {
     tmem_alloc(smem_addr(holder), C::kTmemCols);
     tmem_relinquish();
   }
@@ -234,9 +254,9 @@ __global__ void __launch_bounds__(384, 1)
 
   // (each register-count change sits inside its role's branch: ptxas sizes a
   // region by the setmaxnreg that dominates it)
-  if (warp >= 8) {
+  if (warp >= C::kTmaWarp) {
   regs_decrease<C::kRegsProducer>();
-  if (warp == 8) {
+  if (warp == C::kTmaWarp) {
     // ------------------------------------------------------------ TMA
     const uint32_t leader = elect_one();
     const uint64_t pol_stream = policy_evict_first();  // K_j, V_j: read by this CTA alone
@@ -299,7 +319,7 @@ __global__ void __launch_bounds__(384, 1)
         drain_bar(bar_dofull(s % C::kStages), (s / C::kStages) & 1);
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t leader = elect_one();
     auto commit = [&](uint32_t bar) {
@@ -402,21 +422,42 @@ __global__ void __launch_bounds__(384, 1)
       issue_acc(C::kColDp, st_mn + st * kStageStep, C::kColDk, it == 0);  // B = Q_i
       commit(bar_kdone);
       commit(bar_qfree(st));
-      // dQ_i overwrites dS^T(i) once the dK product has read it
-      ok = wait(bar_kdone, par, 37);
-      if (!ok) break;
-      tc_fence_after();
-      issue_dq();
-      commit(bar_dq);
-      commit(bar_dsfree);
-      if (more) {
-        // dP^T(i+1) overwrites dQ_i once the dQ warps have loaded it
-        ok = wait(bar_dqread, par, 38) &&
-             wait(bar_dofull(st1), static_cast<uint32_t>((it + 1) / C::kStages) & 1u, 46);
+      if constexpr (C::kDqAlias) {
+        // dQ_i overwrites dS^T(i) once the dK product has read it
+        ok = wait(bar_kdone, par, 37);
         if (!ok) break;
         tc_fence_after();
-        issue_sq(v_km, st_km + st1 * kStageStep + kTileStep, C::kColDp);
-        commit(bar_dp);
+        issue_dq();
+        commit(bar_dq);
+        commit(bar_dsfree);
+        if (more) {
+          // dP^T(i+1) overwrites dQ_i once the dQ warps have loaded it
+          ok = wait(bar_dqread, par, 38) &&
+               wait(bar_dofull(st1), static_cast<uint32_t>((it + 1) / C::kStages) & 1u, 46);
+          if (!ok) break;
+          tc_fence_after();
+          issue_sq(v_km, st_km + st1 * kStageStep + kTileStep, C::kColDp);
+          commit(bar_dp);
+        }
+      } else {
+        // dQ_i in its own columns once the dQ warps have loaded dQ_{i-1}
+        if (it > 0) {
+          ok = wait(bar_dqread, par ^ 1u, 38);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        issue_dq();
+        commit(bar_dq);
+        commit(bar_dsfree);
+        if (more) {
+          // dP^T(i+1) overwrites dS^T(i) once the dK product has read it
+          ok = wait(bar_kdone, par, 37) &&
+               wait(bar_dofull(st1), static_cast<uint32_t>((it + 1) / C::kStages) & 1u, 46);
+          if (!ok) break;
+          tc_fence_after();
+          issue_sq(v_km, st_km + st1 * kStageStep + kTileStep, C::kColDp);
+          commit(bar_dp);
+        }
       }
     }
     commit(bar_fin);
@@ -425,12 +466,18 @@ __global__ void __launch_bounds__(384, 1)
     drain_bar(bar_drain, 0);
     __syncwarp();
   }
-  } else if (warp < 4) {
+  } else if (warp < C::kDqWarp0) {
     // ------------------------------------------------------------ P^T, dS^T (thread = key row)
+    // Warps w and w + 4 share key rows 32 (w % 4) .. and take queries
+    // 64 h .. 64 h + 63 (h = w / 4). P^T and dS^T are stored as bf16 pairs
+    // over the first half of the fp32 columns they come from, which the other
+    // warp of the pair may still have to read: the pair loads its columns,
+    // meets at a barrier, then stores.
     regs_increase<C::kRegsDs>();
-    const int r = warp * 32 + lane;
+    const int quad = warp & 3, h = warp >> 2;
+    const int r = quad * 32 + lane;
     const int kj = j * 128 + r;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_tm = tmem + lane_off + C::kColS;
     const uint32_t dp_tm = tmem + lane_off + C::kColDp;
     const float sl2 = args.scale_log2;
@@ -446,74 +493,85 @@ __global__ void __launch_bounds__(384, 1)
       int lim = args.n - 1 - q0;  // last valid query column
       // S^T(i) is complete, and the stage's vectors have landed (the stage is
       // refilled only after this warpgroup's dS^T(i) has been consumed)
-      ok = __all_sync(0xffffffffu, wait_bar(bar_s, par, abort_flag, args.status, 40) &&
-                                       wait_bar(bar_qfull(it % C::kStages),
-                                                static_cast<uint32_t>(it / C::kStages) & 1u, abort_flag,
-                                                args.status, 45));
+      ok = pair_all(quad, wait_bar(bar_s, par, abort_flag, args.status, 40) &&
+                              wait_bar(bar_qfull(it % C::kStages), static_cast<uint32_t>(it / C::kStages) & 1u,
+                                       abort_flag, args.status, 45));
       if (!ok) break;
       tc_fence_after();
-      uint32_t pk[64];  // P^T row as bf16 pairs
+      uint32_t pk[32];  // this warp's 64 queries of the P^T row, as bf16 pairs
+      {
+        uint32_t u[2][32];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t u[32];
-        tmem_ld32(s_tm + 32 * k, u);
+        for (int kk = 0; kk < 2; ++kk) tmem_ld32(s_tm + 32 * (2 * h + kk), u[kk]);
         tmem_ld_wait();
-        reg_fence32(u);
+        pair_sync(quad);
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 l4 = lds_f4(vec + 4u * (32 * k + 4 * c4));
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          float p[4];
+        for (int kk = 0; kk < 2; ++kk) {
+          const int k = 2 * h + kk;
+          reg_fence32(u[kk]);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 32 * k + 4 * c4 + e;
-            p[e] = ex2_mufu(__fmaf_rn(__uint_as_float(u[4 * c4 + e]), sl2, -lv[e]));
-            if (need_mask && (c > lim || (CAUSAL && kj > q0 + c))) p[e] = 0.f;
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 l4 = lds_f4(vec + 4u * (32 * k + 4 * c4));
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            float p[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = 32 * k + 4 * c4 + e;
+              p[e] = ex2_mufu(__fmaf_rn(__uint_as_float(u[kk][4 * c4 + e]), sl2, -lv[e]));
+              if (need_mask && (c > lim || (CAUSAL && kj > q0 + c))) p[e] = 0.f;
+            }
+            pk[16 * kk + 2 * c4] = pack_bf16x2(p[0], p[1]);
+            pk[16 * kk + 2 * c4 + 1] = pack_bf16x2(p[2], p[3]);
           }
-          pk[16 * k + 2 * c4] = pack_bf16x2(p[0], p[1]);
-          pk[16 * k + 2 * c4 + 1] = pack_bf16x2(p[2], p[3]);
-        }
-        uint32_t w[16];
+          uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = pk[16 * k + e];
-        // columns 16k .. 16k+15 held scores of chunks <= k, all loaded already
-        tmem_st16(s_tm + 16 * k, w);
+          for (int e = 0; e < 16; ++e) w[e] = pk[16 * kk + e];
+          tmem_st16(s_tm + 16 * k, w);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_p);
       // dS^T = P^T (dP^T - D); the dS buffer in shared memory is free once the
       // previous dQ product has read it
-      ok = __all_sync(0xffffffffu, wait_bar(bar_dp, par, abort_flag, args.status, 41));
-      if (ok && it > 0) ok = __all_sync(0xffffffffu, wait_bar(bar_dsfree, par ^ 1u, abort_flag, args.status, 42));
+      {
+        bool w_ok = wait_bar(bar_dp, par, abort_flag, args.status, 41);
+        if (w_ok && it > 0) w_ok = wait_bar(bar_dsfree, par ^ 1u, abort_flag, args.status, 42);
+        ok = pair_all(quad, w_ok);
+      }
       if (!ok) break;
       tc_fence_after();
+      {
+        uint32_t u[2][32];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t u[32];
-        tmem_ld32(dp_tm + 32 * k, u);
+        for (int kk = 0; kk < 2; ++kk) tmem_ld32(dp_tm + 32 * (2 * h + kk), u[kk]);
         tmem_ld_wait();
-        reg_fence32(u);
-        uint32_t w[16];
+        pair_sync(quad);
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 d4 = lds_f4(vec + 512u + 4u * (32 * k + 4 * c4));
-          const uint32_t a = pk[16 * k + 2 * c4], b = pk[16 * k + 2 * c4 + 1];
-          const float ds0 = bf16_lo(a) * (__uint_as_float(u[4 * c4]) - d4.x);
-          const float ds1 = bf16_hi(a) * (__uint_as_float(u[4 * c4 + 1]) - d4.y);
-          const float ds2 = bf16_lo(b) * (__uint_as_float(u[4 * c4 + 2]) - d4.z);
-          const float ds3 = bf16_hi(b) * (__uint_as_float(u[4 * c4 + 3]) - d4.w);
-          w[2 * c4] = pack_bf16x2(ds0, ds1);
-          w[2 * c4 + 1] = pack_bf16x2(ds2, ds3);
-        }
-        tmem_st16(dp_tm + 16 * k, w);
-        // shared memory: key row r, queries 32k .. 32k+31 = 16-byte chunks
-        // 4(k%2) .. 4(k%2)+3 of box k/2, 128-byte swizzled
+        for (int kk = 0; kk < 2; ++kk) {
+          const int k = 2 * h + kk;
+          reg_fence32(u[kk]);
+          uint32_t w[16];
 #pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4) {
-          const uint32_t chunk = static_cast<uint32_t>(4 * (k & 1) + v4);
-          st_shared_v4(ds_row + (k >> 1) * C::kBoxBytes + ((chunk ^ static_cast<uint32_t>(r & 7)) << 4),
-                       w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 d4 = lds_f4(vec + 512u + 4u * (32 * k + 4 * c4));
+            const uint32_t a = pk[16 * kk + 2 * c4], b = pk[16 * kk + 2 * c4 + 1];
+            const float ds0 = bf16_lo(a) * (__uint_as_float(u[kk][4 * c4]) - d4.x);
+            const float ds1 = bf16_hi(a) * (__uint_as_float(u[kk][4 * c4 + 1]) - d4.y);
+            const float ds2 = bf16_lo(b) * (__uint_as_float(u[kk][4 * c4 + 2]) - d4.z);
+            const float ds3 = bf16_hi(b) * (__uint_as_float(u[kk][4 * c4 + 3]) - d4.w);
+            w[2 * c4] = pack_bf16x2(ds0, ds1);
+            w[2 * c4 + 1] = pack_bf16x2(ds2, ds3);
+          }
+          tmem_st16(dp_tm + 16 * k, w);
+          // shared memory: key row r, queries 32k .. 32k+31 = 16-byte chunks
+          // 4(k%2) .. 4(k%2)+3 of box k/2, 128-byte swizzled
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const uint32_t chunk = static_cast<uint32_t>(4 * (k & 1) + v4);
+            st_shared_v4(ds_row + (k >> 1) * C::kBoxBytes + ((chunk ^ static_cast<uint32_t>(r & 7)) << 4),
+                         w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+          }
         }
       }
       tmem_st_wait();
@@ -533,7 +591,7 @@ __global__ void __launch_bounds__(384, 1)
         __nv_bfloat16* dst = (which ? args.dk : args.dv) + off;
         const uint32_t src = tmem + lane_off + (which ? C::kColDk : C::kColDv);
 #pragma unroll
-        for (int c = 0; c < D; c += 32) {
+        for (int c = h * (D / 2); c < (h + 1) * (D / 2); c += 32) {
           uint32_t u[32];
           tmem_ld32(src + c, u);
           tmem_ld_wait();
@@ -553,13 +611,14 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_before();
   } else {
     // ------------------------------------------------------------ dQ (thread = query row)
+    regs_increase<C::kRegsDq>();
     // dQ_i leaves TMEM at once (the next dP^T may then take its columns) and
     // goes out through dO_i's buffer (the dV product that read dO_i is
     // complete before dQ_i is computed) as 32-column fp32 boxes (128-byte
     // rows, 128-byte swizzle), each reduce-added onto the fp32 dQ by one TMA
     // operation; the buffer goes back to the TMA warp once they have read it.
-    const int q = (warp - 4) * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    const int q = (warp - C::kDqWarp0) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp - C::kDqWarp0) * 32) << 16;
     const bool issuer = q == 0;
     bool ok = true;
     for (int it = 0; ok && it < n_it; ++it) {
@@ -620,7 +679,7 @@ __global__ void __launch_bounds__(384, 1)
   }
 
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
