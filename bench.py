@@ -76,10 +76,16 @@ def profiled_traffic(workload: str) -> float | None:
     """DRAM bytes per launch from the committed ncu summary of this workload,
     if it was taken on the current kernel sources (else None)."""
     prof = os.path.join(ROOT, "profiles")
-    names = [f for f in (os.listdir(prof) if os.path.isdir(prof) else []) if f.endswith(f"_{workload}.md")]
-    if not names:
+    text = None
+    for f in sorted(os.listdir(prof) if os.path.isdir(prof) else []):
+        if f.endswith(".md"):
+            t = open(os.path.join(prof, f)).read()
+            m = re.search(r"^workload:\s*(\S+)\s*$", t, flags=re.M)
+            if m and m.group(1) == workload:
+                text = t
+                break
+    if text is None:
         return None
-    text = open(os.path.join(prof, sorted(names)[0])).read()
     sha = re.search(r"kernel_sources_sha:\s*([0-9a-f]+)", text)
     kind = re.search(r"kernel_kind:\s*(\w+)", text)
     val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)

@@ -46,8 +46,11 @@ def test_traffic_gated_by_kernel_fingerprint(tmp_path, monkeypatch):
     prof.mkdir()
     sha = bench.kernel_sources_sha("bf16")
     assert sha != bench.kernel_sources_sha("mxfp8")
-    (prof / "fwd_bf16_w.md").write_text(f"kernel_kind: bf16\nkernel_sources_sha: {sha}\n"
+    (prof / "fwd_bf16_w.md").write_text(f"workload: w\nkernel_kind: bf16\nkernel_sources_sha: {sha}\n"
                                         "dram_bytes_per_launch: 1.5e8\n")
+    # a summary of another workload whose name ends the same way is not taken
+    (prof / "bwd_bf16_bwd_w.md").write_text(f"workload: bwd_w\nkernel_kind: bf16\nkernel_sources_sha: {sha}\n"
+                                            "dram_bytes_per_launch: 9.9e8\n")
     monkeypatch.setattr(bench, "kernel_sources_sha", lambda kind="bf16": sha)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.profiled_traffic("w") == 1.5e8
