@@ -18,17 +18,20 @@
 //
 //   warps 0-7   thread = key row (warps w and w + 4 share rows and split the
 //               128 queries): P^T and dS^T, then the dK, dV epilogue
-//   warps 8-11  thread = query row: dQ_i out of TMEM, through the stage's dO_i
-//               buffer (free once the dV product has read it; handed back to
-//               the TMA warp afterwards) into TMA reduce-adds onto the fp32 dQ
-//   warp 12     TMA: K_j, V_j once; Q_i, dO_i into a ring of stages
+//   warps 8-11  thread = query row: dQ_i out of TMEM, through shared memory
+//               (at d = 128 the stage's dO_i buffer, free once the dV product
+//               has read it and handed back to the TMA warp afterwards; at
+//               d = 64 a buffer of its own) into TMA reduce-adds onto the fp32 dQ
+//   warp 12     TMA: K_j, V_j once; Q_i (with LSE_i log2 e and D_i) and dO_i
+//               into a ring of stages, loaded and released separately
 //   warp 13     MMA issuer (one elected lane)
 //
 // TMEM: S^T (P^T as bf16 pairs over its first 64 columns) at 0, dP^T (dS^T
 // over its first 64) at 128, dV at 256, dK at 256 + d, and at d = 64 dQ_i at
 // 384. At d = 128 dQ_i reuses the dP^T columns once the dK product has read
-// dS^T, and the next dP^T waits until the dQ warps have loaded dQ_i. dS also goes to shared memory, keys x queries
-// with queries contiguous, as the MN-major A operand of the dQ product.
+// dS^T, and the next dP^T waits until the dQ warps have loaded dQ_i. dS also
+// goes to shared memory, keys x queries with queries contiguous, as the
+// MN-major A operand of the dQ product.
 #pragma once
 
 #include <cuda_bf16.h>

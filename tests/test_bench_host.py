@@ -68,3 +68,16 @@ def test_reference_arm_json_line():
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_json_line_backward():
+    # the backward workload's reference arm times the float64 backward oracle on one head
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--shape",
+                        "1,1,512,64,1,0,1", "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"].startswith("attention bwd") and line["value"] > 0
+    assert line["config"]["pass"] == "bwd" and line["config"]["causal"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and "backward" in line["cpu_baseline"]["sample"]
+
