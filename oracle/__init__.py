@@ -16,7 +16,8 @@ Modules
   rescale_stats  the lagging-max (tau) rescale simulator and its statistics.
   mxfp8          the E4M3 / E8M0 32x32 block quantiser and its dequantisation.
   backward       the gradient of the forward (dQ, dK, dV) with P rebuilt from
-                 the LSE: the five products of the backward pass.
+                 the LSE: the five products of the backward pass, in float64
+                 and with MXFP8 inputs (32 x 32 blocks for Q, K, V, dO, dS).
 
 Parity pins (tests/test_oracle_*.py, marked "not gpu") tie every function here
 to something other than itself: brute force, closed forms, and the numbers the

@@ -21,22 +21,43 @@ O = softmax(s Q K^T [causal mask]) V for an upstream gradient dO:
 (the five products: S, dP, dV, dK, dQ). Masked scores have P = 0, so they
 contribute nothing. Everything is float64, one (batch, head) at a time, rows
 in chunks only to bound memory.
+
+The MXFP8 backward (``attention_bwd_mxfp8``) is the same method with every
+product's inputs in MXFP8. The page on the MXFP8 extension, section
+"Quantization along both axes and jagged tensors", quantises Q, K and dO in
+square 32 x 32 blocks, so that one E4M3 payload serves both products that read
+a tensor (along d for S and dP, along the sequence for dV, dK and dQ), and
+quantises dS the same way so that dK and dQ read one representation. Its
+section "Softmax conversion and unroll-KV" converts P online and notes that a
+constant scale for P is robust, P being in [0, 1]. The readings taken here:
+  * V is quantised in the same square blocks (it enters only dP, along d);
+  * P enters dV as E4M3 with the constant scale 2^-8 (``p_to_mxfp8_constant``);
+    dS = P (dP - D) takes the unrounded P;
+  * dS is rounded in 32 x 32 blocks of (queries, keys) by the block rule of
+    ``quantize_blocks``, the blocks starting at query 0 and key 0, entries
+    outside the sequence or masked being zero;
+  * D = rowsum(dO * O) takes the dequantised dO, the one dP is built from.
 """
 from __future__ import annotations
 
 import numpy as np
 
+from oracle.mxfp8 import p_to_mxfp8_constant, quantize_blocks
+
 
 def attention_bwd_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarray, do: np.ndarray,
                        lse: np.ndarray, causal: bool, scale: float, row_chunk: int = 512,
-                       p_cast=None, ds_cast=None) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+                       p_cast=None, ds_cast=None, dv_p_cast=None) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
     """dQ, dK, dV (float64) of one (batch, head): q [N, d], k [N, d], v [N, dv],
     o and do [N, dv], lse [N] (natural log of the scaled scores' row sums).
 
     ``p_cast`` / ``ds_cast`` (optional) round P before it enters dV and dS,
     and dS before it enters dQ and dK, to a matrix-multiply input type: the
     same method in the precision a kernel feeds its tensor cores, for tight
-    parity checks (the forward's reading: P takes the MMA input type)."""
+    parity checks (the forward's reading: P takes the MMA input type).
+    ``dv_p_cast`` (optional) rounds only the P that enters dV; dS then takes
+    P as it was. ``row_chunk`` must be a multiple of 32 when ``ds_cast``
+    rounds in 32-row blocks."""
     q, k, v, o, do, lse = (np.asarray(x, dtype=np.float64) for x in (q, k, v, o, do, lse))
     n = q.shape[0]
     dq = np.zeros_like(q)
@@ -52,7 +73,8 @@ def attention_bwd_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarra
             p = np.where(j <= np.arange(i0, i1)[:, None], p, 0.0)
         if p_cast is not None:
             p = np.asarray(p_cast(p), dtype=np.float64)
-        dv += p.T @ do[i0:i1]
+        p_dv = p if dv_p_cast is None else np.asarray(dv_p_cast(p), dtype=np.float64)
+        dv += p_dv.T @ do[i0:i1]
         dp = do[i0:i1] @ v.T
         ds = p * (dp - d_row[i0:i1, None])
         if ds_cast is not None:
@@ -101,3 +123,27 @@ def attention_bwd_abs_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.nd
         ak += scale * (ds.T @ np.abs(q[i0:i1]))
     return aq, ak, av
 
+
+
+def attention_bwd_mxfp8_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarray, do: np.ndarray,
+                             lse: np.ndarray, causal: bool, scale: float) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """dQ, dK, dV (float64) of one (batch, head) in MXFP8: q, k, v, do [N, d]
+    are the unquantised inputs (rounded here in 32 x 32 blocks), o [N, d] the
+    forward's output and lse [N] its LSE, both taken as given."""
+    qd, kd, vd, dod = (quantize_blocks(np.asarray(x, dtype=np.float64))[2] for x in (q, k, v, do))
+    return attention_bwd_head(qd, kd, vd, o, dod, lse, causal, scale, row_chunk=512,
+                              ds_cast=lambda ds: quantize_blocks(ds)[2], dv_p_cast=p_to_mxfp8_constant)
+
+
+def attention_bwd_mxfp8(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarray, do: np.ndarray,
+                        lse: np.ndarray, causal: bool, scale: float) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """``attention_bwd_mxfp8_head`` over [B, H, N, d] inputs and lse [B, H, N]."""
+    q = np.asarray(q)
+    B, H = q.shape[:2]
+    out = [np.empty(np.shape(x), dtype=np.float64) for x in (q, k, v)]
+    for b in range(B):
+        for h in range(H):
+            g = attention_bwd_mxfp8_head(q[b, h], k[b, h], v[b, h], o[b, h], do[b, h], lse[b, h], causal, scale)
+            for dst, src in zip(out, g):
+                dst[b, h] = src
+    return out[0], out[1], out[2]
