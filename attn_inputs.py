@@ -81,8 +81,14 @@ BWD_D128 = Workload("bwd_bf16_b4h16n4096d128", 4, 16, 4096, 128, False, directio
 BWD_CAUSAL_D128 = Workload("bwd_bf16_causal_b2h16n8192d128_qk2", 2, 16, 8192, 128, True, qk_std=2.0,
                            direction="bwd")
 
+# The MXFP8 backward (fp32 Q, K, V, dO quantised inside the step) on the bf16
+# backward's non-causal shape and on the MXFP8 forward's causal one.
+BWD_MXFP8 = Workload("bwd_mxfp8_b4h16n4096d128", 4, 16, 4096, 128, False, dtype="mxfp8", direction="bwd")
+BWD_MXFP8_CAUSAL = Workload("bwd_mxfp8_causal_b2h16n16384d128", 2, 16, 16384, 128, True, dtype="mxfp8",
+                            direction="bwd")
+
 WORKLOADS = {w.name: w for w in (TINY, NONCAUSAL_D128, CAUSAL_D128_WIDE, CAUSAL_D64, MXFP8_CAUSAL, BWD_D128,
-                                 BWD_CAUSAL_D128)}
+                                 BWD_CAUSAL_D128, BWD_MXFP8, BWD_MXFP8_CAUSAL)}
 
 
 def draw_fp32(B: int, H: int, N: int, d: int, qk_std: float = 1.0, v_std: float = 1.0,

@@ -36,7 +36,7 @@ if ROOT not in sys.path:
 import attn_inputs as I  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s on 1xGB300 and fraction of dense BF16/FP8 peak"
-METRIC_BWD = "attention bwd TFLOP/s on 1xGB300 and fraction of dense BF16 peak"
+METRIC_BWD = "attention bwd TFLOP/s on 1xGB300 and fraction of dense BF16/FP8 peak"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = I.NONCAUSAL_D128.name
 L2_BYTES = 129 * 1024 * 1024
@@ -53,7 +53,17 @@ KERNEL_SOURCES = {
     "bwd": ["online_softmax_fwd_gb300/csrc/bwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/bwd_aux.cu",
             "online_softmax_fwd_gb300/csrc/fwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/ptx.cuh",
             "online_softmax_fwd_gb300/csrc/exp2_fma.cuh", "online_softmax_fwd_gb300/csrc/schedule.h"],
+    "bwd_mxfp8": ["online_softmax_fwd_gb300/csrc/bwd_mxfp8.cuh", "online_softmax_fwd_gb300/csrc/bwd_bf16.cuh",
+                  "online_softmax_fwd_gb300/csrc/bwd_aux.cu", "online_softmax_fwd_gb300/csrc/mxfp8_common.cuh",
+                  "online_softmax_fwd_gb300/csrc/quant_mxfp8.cu", "online_softmax_fwd_gb300/csrc/fwd_bf16.cuh",
+                  "online_softmax_fwd_gb300/csrc/ptx.cuh"],
 }
+
+
+# what the roofline's achieved figure times (CUDA events around that call)
+KERNEL_NAMES = {("fwd", "bf16"): "attn_fwd_bf16_kernel", ("fwd", "mxfp8"): "attn_fwd_mxfp8_kernel",
+                ("bwd", "bf16"): "attn_bwd (bwd_prep + attn_bwd_bf16_kernel + bwd_post)",
+                ("bwd", "mxfp8"): "attn_bwd_mxfp8 (bwd_prep_mxfp8 + attn_bwd_mxfp8_kernel + bwd_post)"}
 
 
 def kernel_sources_sha(kind: str = "bf16") -> str:
@@ -259,14 +269,16 @@ def oracle_sample(w: I.Workload, q, k, v, seconds: float, rows_per_call: int = 5
 def oracle_bwd_sample(w: I.Workload, q, k, v, o, do, lse, seconds: float) -> dict:
     """Time the float64 backward oracle on whole heads of the workload (at
     least one) until `seconds` have passed; useful FLOP as the metric counts
-    them (10 N^2 d per head, halved for causal)."""
-    from oracle.backward import attention_bwd_head
+    them (10 N^2 d per head, halved for causal). MXFP8 workloads time the
+    MXFP8 backward oracle on the fp32 inputs (it quantises them itself)."""
+    from oracle.backward import attention_bwd_head, attention_bwd_mxfp8_head
+    bwd = attention_bwd_mxfp8_head if w.dtype == "mxfp8" else attention_bwd_head
     t0 = time.perf_counter()
     heads = 0
     for b in range(w.B):
         for h in range(w.H):
-            attention_bwd_head(I.as_f64(q[b, h]), I.as_f64(k[b, h]), I.as_f64(v[b, h]), I.as_f64(o[b, h]),
-                               I.as_f64(do[b, h]), lse[b, h].double().numpy(), w.causal, w.scale)
+            bwd(I.as_f64(q[b, h]), I.as_f64(k[b, h]), I.as_f64(v[b, h]), I.as_f64(o[b, h]),
+                I.as_f64(do[b, h]), lse[b, h].double().numpy(), w.causal, w.scale)
             heads += 1
             if time.perf_counter() - t0 >= seconds:
                 break
@@ -282,25 +294,38 @@ def bench_reference_bwd(args, w: I.Workload) -> None:
     the workload's first head, its O and LSE from the float64 forward oracle
     (computed once, outside the timed steps)."""
     from oracle.attention import attention_fwd
-    from oracle.backward import attention_bwd_head
-    q, k, v = (t[:1, :1] for t in I.bf16_qkv(w))
-    do = I.to_bf16(I.draw_grad(w.B, w.H, w.N, w.d, seed=w.seed + 1)[:1, :1])
-    qq, kk, vv, dd = (I.as_f64(t)[0, 0] for t in (q, k, v, do))
-    o, lse = attention_fwd(qq[None, None], kk[None, None], vv[None, None], w.causal, w.scale)
+    from oracle.backward import attention_bwd_head, attention_bwd_mxfp8_head
+    if w.dtype == "mxfp8":
+        # fp32 draws of the first head; O and LSE from the float64 forward of
+        # their dequantised MXFP8 form
+        from oracle.mxfp8 import quantize_blocks
+        xs = I.draw_fp32(w.B, w.H, w.N, w.d, w.qk_std, w.v_std, w.seed)
+        qq, kk, vv = (x[0, 0].astype(np.float64) for x in xs)
+        dd = I.draw_grad(w.B, w.H, w.N, w.d, seed=w.seed + 1)[0, 0].astype(np.float64)
+        qf, kf, vf = (quantize_blocks(x)[2] for x in (qq, kk, vv))
+        bwd = attention_bwd_mxfp8_head
+    else:
+        q, k, v = (t[:1, :1] for t in I.bf16_qkv(w))
+        do = I.to_bf16(I.draw_grad(w.B, w.H, w.N, w.d, seed=w.seed + 1)[:1, :1])
+        qq, kk, vv, dd = (I.as_f64(t)[0, 0] for t in (q, k, v, do))
+        qf, kf, vf = qq, kk, vv
+        bwd = attention_bwd_head
+    o, lse = attention_fwd(qf[None, None], kf[None, None], vf[None, None], w.causal, w.scale)
     o = I.as_f64(torch.from_numpy(o).to(torch.bfloat16))[0, 0]
     lse = lse.astype(np.float32).astype(np.float64)[0, 0]
     head_flop = w.flops / (w.B * w.H)
 
     def one_step():
         t0 = time.perf_counter()
-        attention_bwd_head(qq, kk, vv, o, dd, lse, w.causal, w.scale)
+        bwd(qq, kk, vv, o, dd, lse, w.causal, w.scale)
         return time.perf_counter() - t0
     for _ in range(args.warmup):
         one_step()
     secs = [one_step() for _ in range(args.steps)]
     value = head_flop / float(np.mean(secs)) / 1e12
     cores = torch.get_num_threads()
-    sample = f"float64 backward oracle on one whole head (N = {w.N}, d = {w.d}) of the workload per step"
+    sample = (f"float64 {'MXFP8 ' if w.dtype == 'mxfp8' else ''}backward oracle on one whole head "
+              f"(N = {w.N}, d = {w.d}) of the workload per step")
     out = {"impl": "reference", "metric": METRIC_BWD, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(secs)), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -514,12 +539,96 @@ class BwdStep:
                 "d2h_bytes_per_step": sum(h.numel() * 2 for h in outs), "steps": n_steps}
 
 
+class BwdMxfp8Step:
+    """One MXFP8 backward pass: quantise Q, K, dO (both scale layouts) and V
+    (fp32, resident in HBM) to E4M3 + E8M0, then attn_bwd_mxfp8 (preparation,
+    main kernel, dQ conversion). O and LSE come from the MXFP8 forward once,
+    before the timed region."""
+
+    launches = 7
+
+    def __init__(self, attn, w, dev, args):
+        self.attn, self.w, self.args = attn, w, args
+        self.tau = 0.0
+        L = attn.lib()
+        self.xq_h, self.xk_h, self.xv_h = (torch.from_numpy(x) for x in I.draw_fp32(
+            w.B, w.H, w.N, w.d, w.qk_std, w.v_std, w.seed))
+        self.do_h = torch.from_numpy(I.draw_grad(w.B, w.H, w.N, w.d, seed=w.seed + 1))
+        self.x = [t.to(dev) for t in (self.xq_h, self.xk_h, self.xv_h, self.do_h)]
+        nsf = attn.mxfp8_scale_bytes(w.B, w.H, w.N, w.d)
+        self.roles = (2, 2, 0, 2)
+        self.codes = [torch.empty(t.shape, dtype=torch.uint8, device=dev) for t in self.x]
+        self.sf = [torch.empty((2 if r == 2 else 1) * nsf, dtype=torch.uint8, device=dev) for r in self.roles]
+        # the forward's O and LSE (its own quantisation: Q, K role 0, V role 1)
+        q8, q_sf = attn.mxfp8_quantize(self.x[0], role=0)
+        k8, k_sf = attn.mxfp8_quantize(self.x[1], role=0)
+        v8, v_sf = attn.mxfp8_quantize(self.x[2], role=1)
+        self.o, self.lse = attn.attn_fwd_mxfp8(q8, q_sf, k8, k_sf, v8, v_sf, causal=w.causal, scale=w.scale)
+        torch.cuda.synchronize(dev)
+        del q8, q_sf, k8, k_sf, v8, v_sf
+        self.o_h, self.lse_h = self.o.cpu(), self.lse.cpu()
+        self.dq, self.dk, self.dv = (torch.empty(self.o.shape, dtype=torch.bfloat16, device=dev) for _ in range(3))
+        self.ws_bytes = L.attn_bwd_workspace_bytes(w.B, w.H, w.N, w.d)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        c, f = self.codes, self.sf
+        self.ptrs = tuple(t.data_ptr() for t in (c[0], f[0], c[1], f[1], c[2], f[2], self.o, c[3], f[3], self.lse,
+                                                 self.dq, self.dk, self.dv))
+
+    def run(self, sh, ev=None):
+        w, L = self.w, self.attn.lib()
+        for i, role in enumerate(self.roles):
+            st = L.attn_mxfp8_quantize(self.x[i].data_ptr(), self.codes[i].data_ptr(), self.sf[i].data_ptr(),
+                                       w.B, w.H, w.N, w.d, role, sh)
+            if st != 0:
+                raise self.attn.AttnError(st, "attn_mxfp8_quantize")
+        if ev:
+            ev[0].record()
+        st = L.attn_bwd_mxfp8(*self.ptrs, w.B, w.H, w.N, w.d, int(w.causal), float(w.scale), self.ws.data_ptr(),
+                              self.ws_bytes, sh)
+        if ev:
+            ev[1].record()
+        if st != 0:
+            raise self.attn.AttnError(st, "attn_bwd_mxfp8")
+
+    def input_bytes(self):
+        return 4 * self.x[0].numel() * 4 + self.o.numel() * 2
+
+    def e2e(self, dev, n_steps, world):
+        w = self.w
+        src = [t.pin_memory() for t in (self.xq_h, self.xk_h, self.xv_h, self.do_h, self.o_h, self.lse_h)]
+        dst = [*self.x, self.o, self.lse]
+        outs = [torch.empty(self.dq.shape, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+        sh = torch.cuda.current_stream(dev).cuda_stream
+
+        def call():
+            for d_, h_ in zip(dst, src):
+                d_.copy_(h_, non_blocking=True)
+            self.run(sh)
+            for h_, d_ in zip(outs, (self.dq, self.dk, self.dv)):
+                h_.copy_(d_, non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+        for _ in range(2):
+            call()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(n_steps):
+            call()
+        dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+        return {"value": w.flops * n_steps * world / dt / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in src),
+                "d2h_bytes_per_step": sum(h.numel() * 2 for h in outs), "steps": n_steps}
+
+
 def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
     import online_softmax_fwd_gb300 as attn
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     attn.lib()
-    step = (BwdStep if w.direction == "bwd" else Mxfp8Step if w.dtype == "mxfp8" else Bf16Step)(attn, w, dev, args)
+    if w.direction == "bwd":
+        step_cls = BwdMxfp8Step if w.dtype == "mxfp8" else BwdStep
+    else:
+        step_cls = Mxfp8Step if w.dtype == "mxfp8" else Bf16Step
+    step = step_cls(attn, w, dev, args)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     for _ in range(args.warmup):
@@ -565,15 +674,16 @@ def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
     achieved = w.flops / avg_launch_s / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": profiled_traffic(w.name), "peak_source": src, "flop_per_launch": w.flops,
-                "kernel": ("attn_bwd (bwd_prep + attn_bwd_bf16_kernel + bwd_post)" if w.direction == "bwd" else
-                           "attn_fwd_mxfp8_kernel" if w.dtype == "mxfp8" else "attn_fwd_bf16_kernel")}
+                "kernel": KERNEL_NAMES[(w.direction, w.dtype)]}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and w.direction == "bwd":
-        s = oracle_bwd_sample(w, step.q_h, step.k_h, step.v_h, step.o_h, step.do_h, step.lse_h, args.cpu_seconds)
+        ins = ((step.xq_h, step.xk_h, step.xv_h) if w.dtype == "mxfp8" else (step.q_h, step.k_h, step.v_h))
+        s = oracle_bwd_sample(w, *ins, step.o_h, step.do_h, step.lse_h, args.cpu_seconds)
         cpu = {"value": s["value"], "unit": UNIT, "cores": torch.get_num_threads(), "kind": "oracle",
-               "sample": f"float64 backward oracle on the workload's first {s['heads_touched']} whole head(s) "
-                         f"(O and LSE from the forward kernel), {s['seconds']:.1f} s"}
+               "sample": f"float64 {'MXFP8 ' if w.dtype == 'mxfp8' else ''}backward oracle on the workload's first "
+                         f"{s['heads_touched']} whole head(s) (O and LSE from the forward kernel), "
+                         f"{s['seconds']:.1f} s"}
     elif rank == 0 and world == 1 and not args.no_cpu_baseline:
         s = oracle_sample(w, *cpu_inputs(step, w), args.cpu_seconds)
         cpu = {"value": s["value"], "unit": UNIT, "cores": torch.get_num_threads(), "kind": "oracle",
@@ -590,7 +700,8 @@ def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
                           "l2": f"inputs larger than L2 ({step.input_bytes() / 2**20:.0f} MiB > 129 MB)",
                           "tau": step.tau if w.dtype == "mxfp8" else args.tau, "exp2_emu16": args.exp2_emu16,
                           **({"p_scaling": ["block_amax", "constant_2^-8", "constant_2^-8_e5m2"][args.p_scaling]}
-                             if w.dtype == "mxfp8" else {})},
+                             if w.dtype == "mxfp8" and w.direction == "fwd" else
+                             {"p_scaling": "constant_2^-8", "ds_blocks": "32x32"} if w.dtype == "mxfp8" else {})},
                "e2e": e2e, "gpu_launches": args.steps * step.launches, "roofline": roofline, "cpu_baseline": cpu,
                "clocks": clocks, "kernel_ms": {"mean": float(np.mean(launch_ms)), "min": float(np.min(launch_ms)),
                                                "max": float(np.max(launch_ms))}}

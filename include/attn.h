@@ -157,7 +157,11 @@ size_t attn_mxfp8_scale_bytes(int B, int H, int N, int d);
  * codes [B,H,N,d] (x_e4m3, one byte each) and the scale array (x_scales).
  * Each 32 x 32 block (rows past N count as zero) takes the smallest power of
  * two 2^e with amax / 2^e <= 448; elements are multiplied by 2^-e and rounded
- * to E4M3, nearest even, saturating at +-448. role 0: Q or K; role 1: V.
+ * to E4M3, nearest even, saturating at +-448. role 0: the atom layout of a
+ * product along d (Q, K of the forward); role 1: along the sequence (V of the
+ * forward); role 2: both (the blocks are square, so the codes are the same),
+ * x_scales then holding 2 * attn_mxfp8_scale_bytes bytes, role 0's array
+ * first and role 1's right after it (Q, K, dO of attn_bwd_mxfp8).
  * d must be 128 (else ATTN_ERR_UNSUPPORTED); B*H <= 65535. Asynchronous on
  * stream; allocates nothing.
  */
@@ -269,6 +273,36 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                        const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
                        float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_bwd_mxfp8 -- the backward pass with all five products on the
+ * block-scaled tensor cores ("PyTorch FlashAttention-4 adds MXFP8
+ * block-scaled forward and backward for Blackwell", section "Quantization
+ * along both axes and jagged tensors": square 32 x 32 blocks for Q, K and dO,
+ * whose one E4M3 payload serves the products along d and along the sequence,
+ * and for dS, which the dK and dQ products both read). The same gradient as
+ * attn_bwd, computed from the quantised inputs, with
+ *   P entering dV as E4M3 with the constant scale 2^-8 (P = 1 held as 256);
+ *   dS = P (dP - D) from the unrounded P, rounded to E4M3 in 32 x 32 blocks
+ *   of (queries, keys) with the quantiser's scale rule;
+ *   D = rowsum(dO * O) from the dequantised dO and O.
+ *
+ *   q8, k8, do8       E4M3 [B, H, N, 128] from attn_mxfp8_quantize with
+ *   q_sf, k_sf, do_sf role 2 (their scale arrays hold both layouts);
+ *   v8, v_sf          V from attn_mxfp8_quantize with role 0;
+ *   o                 bf16 [B, H, N, 128], the forward's output;
+ *   lse               fp32 [B, H, N], the forward's LSE (4-byte aligned);
+ *   dq, dk, dv        bf16 [B, H, N, 128] outputs;
+ *   workspace         as attn_bwd: attn_bwd_workspace_bytes(B, H, N, 128)
+ *                     bytes, 256-byte aligned, owned by the caller.
+ * d must be 128 (else ATTN_ERR_UNSUPPORTED), B*H <= 65535. All other
+ * pointers device memory, 16-byte aligned. Asynchronous on `stream` (three
+ * kernels); nothing is allocated. Errors as attn_bwd.
+ */
+attn_status_t attn_bwd_mxfp8(const void* q8, const void* q_sf, const void* k8, const void* k_sf, const void* v8,
+                             const void* v_sf, const void* o, const void* do8, const void* do_sf, const float* lse,
+                             void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
+                             void* workspace, size_t workspace_bytes, void* stream);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int attn_version(void);

@@ -65,6 +65,10 @@ _SIGNATURES = {
     # q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, causal, scale, workspace, workspace_bytes, stream
     "attn_bwd": ([ctypes.c_void_p] * 9 + [ctypes.c_int] * 5
                  + [ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
+    # q8, q_sf, k8, k_sf, v8, v_sf, o, do8, do_sf, lse, dq, dk, dv, B, H, N, d, causal, scale, workspace,
+    # workspace_bytes, stream
+    "attn_bwd_mxfp8": ([ctypes.c_void_p] * 13 + [ctypes.c_int] * 5
+                       + [ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
     "attn_get_device_status": ([ctypes.c_void_p], ctypes.c_int),
     "attn_selftest_wait_timeout": ([ctypes.c_longlong, ctypes.c_void_p], ctypes.c_int),
     "attn_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -232,16 +236,56 @@ def mxfp8_scale_bytes(B: int, H: int, N: int, d: int) -> int:
 
 def mxfp8_quantize(x: torch.Tensor, role: int, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
     """fp32 CUDA [B,H,N,128] -> (E4M3 codes uint8 [B,H,N,128], scale atoms uint8
-    [B*H*ceil(N/128)*512]). role 0: Q or K; role 1: V."""
+    [B*H*ceil(N/128)*512]). role 0: Q or K of the forward (atom rows = sequence
+    positions); role 1: V of the forward (rows = d columns); role 2: both
+    layouts, one array after the other (Q, K and dO of attn_bwd_mxfp8)."""
     if not x.is_cuda or x.dtype != torch.float32 or x.dim() != 4 or not x.is_contiguous():
         raise ValueError("x must be a contiguous CUDA float32 tensor [B,H,N,d]")
     B, H, N, d = x.shape
     codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
-    scales = torch.empty(max(1, mxfp8_scale_bytes(B, H, N, d)), dtype=torch.uint8, device=x.device)
+    copies = 2 if role == 2 else 1
+    scales = torch.empty(max(1, copies * mxfp8_scale_bytes(B, H, N, d)), dtype=torch.uint8, device=x.device)
     with torch.cuda.device(x.device):
         _check(lib().attn_mxfp8_quantize(_ptr(x), _ptr(codes), _ptr(scales), B, H, N, d, int(role),
                                          _stream_handle(stream)), "attn_mxfp8_quantize")
     return codes, scales
+
+
+def attn_bwd_mxfp8(q8: torch.Tensor, q_sf: torch.Tensor, k8: torch.Tensor, k_sf: torch.Tensor, v8: torch.Tensor,
+                   v_sf: torch.Tensor, o: torch.Tensor, do8: torch.Tensor, do_sf: torch.Tensor, lse: torch.Tensor,
+                   causal: bool = False, scale: float | None = None, workspace: dict | None = None,
+                   stream=None) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """dQ, dK, dV (bf16 [B,H,N,128]) through the C ABI from MXFP8 inputs: q8/q_sf,
+    k8/k_sf and do8/do_sf from mxfp8_quantize(role=2), v8/v_sf from role 0, the
+    forward's output o (bf16) and LSE (fp32 [B,H,N]). ``workspace`` (a dict)
+    keeps the device workspace between calls of the same shape."""
+    for name, t in (("q8", q8), ("k8", k8), ("v8", v8), ("do8", do8)):
+        if not t.is_cuda or t.dtype != torch.uint8 or t.dim() != 4 or not t.is_contiguous() or t.shape != q8.shape:
+            raise ValueError(f"{name} must be contiguous CUDA uint8 (E4M3 codes) shaped like q8")
+    B, H, N, d = q8.shape
+    need_sf = mxfp8_scale_bytes(B, H, N, d)
+    for name, t, copies in (("q_sf", q_sf, 2), ("k_sf", k_sf, 2), ("v_sf", v_sf, 1), ("do_sf", do_sf, 2)):
+        if not t.is_cuda or t.dtype != torch.uint8 or t.numel() < copies * need_sf:
+            raise ValueError(f"{name} must be a CUDA uint8 scale array of >= {copies * need_sf} bytes")
+    if o.shape != q8.shape or o.dtype != torch.bfloat16 or not o.is_contiguous() or o.device != q8.device:
+        raise ValueError("o must be a contiguous bf16 tensor shaped like q8 on its device")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous() or lse.device != q8.device:
+        raise ValueError("lse must be a contiguous float32 tensor [B,H,N] on q8's device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = (torch.empty(q8.shape, dtype=torch.bfloat16, device=q8.device) for _ in range(3))
+    need = lib().attn_bwd_workspace_bytes(B, H, N, d)
+    ws = workspace if workspace is not None else {}
+    if ws.get("key") != (need, str(q8.device)):
+        ws.clear()
+        ws["key"] = (need, str(q8.device))
+        ws["buf"] = torch.empty(max(need, 1), dtype=torch.uint8, device=q8.device)
+    h = _stream_handle(stream)
+    with torch.cuda.device(q8.device):
+        st = lib().attn_bwd_mxfp8(*(_ptr(t) for t in (q8, q_sf, k8, k_sf, v8, v_sf, o, do8, do_sf, lse, dq, dk, dv)),
+                                  B, H, N, d, int(bool(causal)), float(scale), _ptr(ws["buf"]), need, h)
+    _check(st, "attn_bwd_mxfp8")
+    return dq, dk, dv
 
 
 P_SCALE_BLOCK_AMAX = 0

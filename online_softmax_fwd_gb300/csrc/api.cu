@@ -15,6 +15,7 @@
 #include "attn.h"
 #include "bwd_bf16.cuh"
 #include "bwd_dispatch.h"
+#include "bwd_mxfp8.cuh"
 #include "exp2_fma.cuh"
 #include "fwd_bf16.cuh"
 #include "fwd_dispatch.h"
@@ -268,6 +269,72 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+attn_status_t attn_bwd_mxfp8(const void* q8, const void* q_sf, const void* k8, const void* k_sf, const void* v8,
+                             const void* v_sf, const void* o, const void* do8, const void* do_sf, const float* lse,
+                             void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || H < 0 || N < 0 || (causal != 0 && causal != 1)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (d != 128) return d > 0 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
+  if (N > kMaxN || static_cast<long long>(B) * H * ((N + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (!q8 || !q_sf || !k8 || !k_sf || !v8 || !v_sf || !o || !do8 || !do_sf || !lse || !dq || !dk || !dv)
+    return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_bwd_workspace_bytes(B, H, N, d);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(q_sf) || !aligned16(k8) || !aligned16(k_sf) || !aligned16(v8) ||
+      !aligned16(v_sf) || !aligned16(o) || !aligned16(do8) || !aligned16(do_sf) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTN_ERR_MISALIGNED;
+  const long long bh = static_cast<long long>(B) * H;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_map_e4m3(&mq, q8, N, bh) || !make_map_e4m3(&mk, k8, N, bh) || !make_map_e4m3(&mv, v8, N, bh) ||
+      !make_map_e4m3(&mdo, do8, N, bh))
+    return ATTN_ERR_CUDA;
+  unsigned int* status = status_word();
+  if (!status) return ATTN_ERR_CUDA;
+  const int np = (N + 127) / 128 * 128;
+  const size_t acc_bytes = (static_cast<size_t>(bh) * N * d * 4 + 255) / 256 * 256;
+  const size_t vec_bytes = (static_cast<size_t>(bh) * np * 4 + 255) / 256 * 256;
+  float* dq_acc = static_cast<float*>(workspace);
+  CUtensorMap mdq;
+  if (!make_map_f32(&mdq, dq_acc, d, N, bh)) return ATTN_ERR_CUDA;
+  float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes);
+  float* dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes + vec_bytes);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (attn::launch_bwd_prep_mxfp8(o, do8, do_sf, lse, lse2, dvec, dq_acc, bh, N, np, st) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  // role-2 scale arrays: the atoms whose rows are sequence positions, then
+  // those whose rows are d columns
+  const size_t sf_bytes = attn_mxfp8_scale_bytes(B, H, N, d);
+  auto u8 = [](const void* p) { return static_cast<const uint8_t*>(p); };
+  attn::BwdMxArgs a;
+  a.q_sf = u8(q_sf);
+  a.q_sf_t = u8(q_sf) + sf_bytes;
+  a.k_sf = u8(k_sf);
+  a.k_sf_t = u8(k_sf) + sf_bytes;
+  a.v_sf = u8(v_sf);
+  a.do_sf = u8(do_sf);
+  a.do_sf_t = u8(do_sf) + sf_bytes;
+  a.lse2 = lse2;
+  a.dvec = dvec;
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.status = status;
+  a.n = N;
+  a.np = np;
+  a.n_tiles = (N + 127) / 128;
+  a.bh = static_cast<int>(bh);
+  a.scale = scale;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  cudaError_t e = attn::launch_bwd_mxfp8_d128(causal, mq, mk, mv, mdo, mdq, a, st);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  e = attn::launch_bwd_post(dq_acc, dq, bh * N * static_cast<long long>(d), scale, st);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                        int causal, float scale, void* stream) {
   return attn_fwd_ex(q, k, v, o, lse, B, H, N, d, causal, scale, 8.0f, 0, stream);
@@ -280,7 +347,7 @@ size_t attn_mxfp8_scale_bytes(int B, int H, int N, int d) {
 
 attn_status_t attn_mxfp8_quantize(const float* x, void* x_e4m3, void* x_scales, int B, int H, int N, int d, int role,
                                   void* stream) {
-  if (B < 0 || H < 0 || N < 0 || (role != 0 && role != 1)) return ATTN_ERR_INVALID_ARG;
+  if (B < 0 || H < 0 || N < 0 || role < 0 || role > 2) return ATTN_ERR_INVALID_ARG;
   if (d != 128) return d > 0 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
   if (N > kMaxN || static_cast<long long>(B) * H > 65535) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;

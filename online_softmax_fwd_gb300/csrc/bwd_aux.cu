@@ -1,10 +1,14 @@
-// The backward pass's two small kernels around attn_bwd_bf16_kernel:
+// The backward pass's small kernels around its main kernels:
 //   bwd_prep: D_i = sum_c dO_ic O_ic (fp32 from bf16) and LSE_i log2(e) for
 //             every query row (rows N .. np-1 of a head get 0), and the fp32
 //             dQ accumulator zeroed;
+//   bwd_prep_mxfp8: the same with dO from its E4M3 codes times its blocks'
+//             E8M0 scales, and LSE_i log2(e) - 8 (the MXFP8 kernel's exp then
+//             gives P 2^8, the constant scale of P in E4M3);
 //   bwd_post: dQ = s * accumulator, rounded to bf16.
-// Both are bandwidth-bound elementwise passes.
+// All are bandwidth-bound elementwise passes.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -63,6 +67,54 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   for (int e = lane; e < D / 4; e += 32) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// one warp per query row (d = 128); lane l takes columns 4l .. 4l + 3, in dO's
+// 32-column block l / 8
+__global__ void __launch_bounds__(256) bwd_prep_mxfp8_kernel(const __nv_bfloat16* __restrict__ o,
+                                                             const uint8_t* __restrict__ do8,
+                                                             const uint8_t* __restrict__ do_sf,
+                                                             const float* __restrict__ lse, float* __restrict__ lse2,
+                                                             float* __restrict__ dvec, float* __restrict__ dq_acc,
+                                                             int n, int np) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + warp;
+  const long long bh = blockIdx.y;
+  if (row >= np) return;
+  const size_t prow = static_cast<size_t>(bh) * np + row;
+  if (row >= n) {
+    if (lane == 0) {
+      lse2[prow] = 0.f;
+      dvec[prow] = 0.f;
+    }
+    return;
+  }
+  const size_t grow = static_cast<size_t>(bh) * n + row;
+  const uint2 a = reinterpret_cast<const uint2*>(o + grow * 128)[lane];
+  const uint32_t c = reinterpret_cast<const uint32_t*>(do8 + grow * 128)[lane];
+  // the block's E8M0 byte: atom of tile row / 128, row r at byte (r % 32) * 16 + (r / 32) * 4 + block
+  const int r = row & 127;
+  const uint32_t byte =
+      do_sf[(static_cast<size_t>(bh) * (np / 128) + (row >> 7)) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (lane >> 3)];
+  const float sc = byte ? __uint_as_float(byte << 23) : __uint_as_float(0x400000u);  // 2^(byte - 127)
+  // E4M3 -> f16 is exact; the lower byte becomes the lower half
+  uint32_t h01, h23;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"(static_cast<uint16_t>(c & 0xFFFFu)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(static_cast<uint16_t>(c >> 16)));
+  const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+  const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+  float acc = 0.f;
+  acc = __fmaf_rn(f01.x * sc, __uint_as_float(a.x << 16), acc);
+  acc = __fmaf_rn(f01.y * sc, __uint_as_float(a.x & 0xFFFF0000u), acc);
+  acc = __fmaf_rn(f23.x * sc, __uint_as_float(a.y << 16), acc);
+  acc = __fmaf_rn(f23.y * sc, __uint_as_float(a.y & 0xFFFF0000u), acc);
+#pragma unroll
+  for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+  if (lane == 0) {
+    dvec[prow] = acc;
+    lse2[prow] = lse[grow] * 1.4426950408889634f - 8.0f;
+  }
+  reinterpret_cast<float4*>(dq_acc + grow * 128)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 // four elements per thread
 __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
                                                        long long n4, float scale) {
@@ -90,6 +142,15 @@ cudaError_t launch_bwd_prep(const void* o, const void* dout, const float* lse, f
     bwd_prep_kernel<64><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
                                                   static_cast<const __nv_bfloat16*>(dout), lse, lse2, dvec, dq_acc,
                                                   n, np);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_prep_mxfp8(const void* o, const void* do8, const void* do_sf, const float* lse, float* lse2,
+                                  float* dvec, float* dq_acc, long long bh, int n, int np, cudaStream_t stream) {
+  dim3 grid(static_cast<unsigned>(np / 8), static_cast<unsigned>(bh));
+  bwd_prep_mxfp8_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
+                                                  static_cast<const uint8_t*>(do8), static_cast<const uint8_t*>(do_sf),
+                                                  lse, lse2, dvec, dq_acc, n, np);
   return cudaGetLastError();
 }
 

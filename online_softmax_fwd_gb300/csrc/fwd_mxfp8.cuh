@@ -85,10 +85,6 @@ struct MxCfg {
   static constexpr uint32_t kPScale = 32, kVScale = 36, kQScale = 40, kKScale = 44;
 };
 
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
-}
-
 // PS, the scaling of P: 0 = one E8M0 scale per 32 keys from the block amax;
 // 1 = the constant 2^-8 (E8M0 byte 119) with P in E4M3 (same page, same
 // section: constant scaling of P stays robust because softmax keeps P in

@@ -78,9 +78,10 @@ __device__ __forceinline__ void sf_copy_to_tmem(uint32_t tmem_cols, uint32_t ato
 // Instruction descriptor, kind::mxf8f6f4 with E4M3 B, E4M3 or E5M2 A, E8M0
 // scales, fp32 accumulator; a_sf / b_sf pick the scale byte of this K=32 step.
 __host__ __device__ constexpr uint32_t idesc_mxf8(int m, int n, bool b_mn_major, uint32_t a_sf, uint32_t b_sf,
-                                                  bool a_e5m2 = false) {
+                                                  bool a_e5m2 = false, bool a_mn_major = false) {
   return ((b_sf & 3u) << 4)                         // B scale-factor id
          | ((a_e5m2 ? 1u : 0u) << 7)                 // A format: E4M3 0, E5M2 1 (B stays E4M3)
+         | ((a_mn_major ? 1u : 0u) << 15)            // A major-ness (shared-memory A only)
          | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
          | (static_cast<uint32_t>(n >> 3) << 17)     // N / 8
          | (1u << 23)                                // scale type E8M0

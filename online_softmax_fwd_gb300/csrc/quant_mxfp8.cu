@@ -6,10 +6,14 @@
 // "Quantization along both axes and jagged tensors"): each block's amax gives
 // its E8M0 exponent e (smallest power of two with amax / 2^e <= 448); elements
 // are multiplied by 2^-e (exact) and rounded to E4M3 (nearest even,
-// saturating). Role 0 lays the atom out for the S = Q K^T GEMM (atom row = the
-// tile's sequence row, block = d / 32); role 1 for the O = P V GEMM (atom row =
-// the d column, block = key block of the tile). Rows past N count as zeros for
-// the amax and are not written.
+// saturating). Role 0 lays the atom out for a GEMM that contracts over d (atom
+// row = the tile's sequence row, block = d / 32: Q and K in S = Q K^T); role 1
+// for one that contracts over the sequence (atom row = the d column, block =
+// 32-row block of the tile: V in O = P V). The blocks being square, the E4M3
+// payload is the same for both; role 2 writes both atom arrays in one pass,
+// role 0's first and role 1's right after it, for a tensor that enters
+// products along both axes (Q, K and dO in the backward pass). Rows past N
+// count as zeros for the amax and are not written.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -59,14 +63,18 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const float* __rest
       reinterpret_cast<uint32_t*>(q + (bh * n + row) * 128)[lane] =
           pack_e4m3x4(v[i].x * sc, v[i].y * sc, v[i].z * sc, v[i].w * sc);
   }
-  // the tile's atom: 512 bytes, two per thread
+  // the tile's atom(s): 512 bytes each, two bytes per thread
   uint8_t* atom = atoms + (bh * ntiles + tile) * 512;
+  uint8_t* atom_t = atoms + ((static_cast<long long>(gridDim.y) + bh) * ntiles + tile) * 512;
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const uint32_t p = 2 * tid + k;
     const uint32_t atom_row = (p >> 4) + 32 * ((p & 15) >> 2);
     const uint32_t kb = p & 3;
-    atom[p] = static_cast<uint8_t>(role == 0 ? eb[atom_row >> 5][kb] : eb[kb][atom_row >> 5]);
+    const uint8_t by_row = static_cast<uint8_t>(eb[atom_row >> 5][kb]);  // row = sequence position
+    const uint8_t by_col = static_cast<uint8_t>(eb[kb][atom_row >> 5]);  // row = d column
+    atom[p] = role == 1 ? by_col : by_row;
+    if (role == 2) atom_t[p] = by_col;
   }
 }
 

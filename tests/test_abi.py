@@ -173,3 +173,35 @@ def test_bwd_rejects_bad_arguments(lib):
     assert lib.attn_bwd(*args(lse=A * 6 + 2)) == 3
     assert lib.attn_bwd(*args(ws=A * 9 + 16)) == 3
     assert lib.attn_bwd(*args(b=0)) == 0     # nothing to do
+
+
+def test_bwd_mxfp8_rejects_bad_arguments(lib):
+    A = 1 << 20  # fake, 256-byte aligned addresses: rejected calls never dereference them
+    B, H, N, d = 1, 2, 300, 128
+    need = lib.attn_bwd_workspace_bytes(B, H, N, d)
+
+    def args(ws=A * 14, ws_bytes=need, d_=d, causal=0, scale=0.1, b=B, q_sf=A * 2, do8=A * 8, lse=A * 10, h=H):
+        # q8, q_sf, k8, k_sf, v8, v_sf, o, do8, do_sf, lse, dq, dk, dv
+        return (A, q_sf, A * 3, A * 4, A * 5, A * 6, A * 7, do8, A * 9, lse, A * 11, A * 12, A * 13, b, h, N, d_,
+                causal, scale, ws, ws_bytes, None)
+
+    assert lib.attn_bwd_mxfp8(*args(d_=64)) == 2     # MXFP8 is d = 128 only
+    assert lib.attn_bwd_mxfp8(*args(d_=0)) == 1
+    assert lib.attn_bwd_mxfp8(*args(causal=3)) == 1
+    assert lib.attn_bwd_mxfp8(*args(scale=-1.0)) == 1
+    assert lib.attn_bwd_mxfp8(*args(ws_bytes=need - 1)) == 1
+    assert lib.attn_bwd_mxfp8(*args(q_sf=0)) == 1
+    assert lib.attn_bwd_mxfp8(*args(q_sf=A * 2 + 4)) == 3
+    assert lib.attn_bwd_mxfp8(*args(do8=A * 8 + 8)) == 3
+    assert lib.attn_bwd_mxfp8(*args(lse=A * 10 + 1)) == 3
+    assert lib.attn_bwd_mxfp8(*args(ws=A * 14 + 64)) == 3
+    assert lib.attn_bwd_mxfp8(*args(b=300, h=300)) == 2   # B*H above the quantiser's grid limit
+    assert lib.attn_bwd_mxfp8(*args(b=0)) == 0            # nothing to do
+
+
+def test_quantize_roles(lib):
+    A = 1 << 20
+    q = lambda role, d=128: lib.attn_mxfp8_quantize(A, A * 2, A * 3, 1, 2, 256, d, role, None)
+    assert q(3) == 1 and q(-1) == 1
+    assert q(0, d=64) == 2
+    assert lib.attn_mxfp8_quantize(A, A * 2, A * 3, 0, 2, 256, 128, 2, None) == 0   # role 2 accepted; empty
