@@ -8,7 +8,6 @@
 //   bwd_post: dQ = s * accumulator, rounded to bf16.
 // All are bandwidth-bound elementwise passes.
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -67,6 +66,14 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   for (int e = lane; e < D / 4; e += 32) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// The value of an E4M3 code (OCP E4M3FN: sign, 4 exponent bits with bias 7, 3
+// mantissa bits; exponent 0 holds the subnormals m 2^-9), exact in fp32.
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  const uint32_t e = (code >> 3) & 0xFu, m = code & 7u;
+  const float mag = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : static_cast<float>(m) * 0.001953125f;
+  return (code & 0x80u) ? -mag : mag;
+}
+
 // one warp per query row (d = 128); lane l takes columns 4l .. 4l + 3, in dO's
 // 32-column block l / 8
 __global__ void __launch_bounds__(256) bwd_prep_mxfp8_kernel(const __nv_bfloat16* __restrict__ o,
@@ -95,17 +102,11 @@ __global__ void __launch_bounds__(256) bwd_prep_mxfp8_kernel(const __nv_bfloat16
   const uint32_t byte =
       do_sf[(static_cast<size_t>(bh) * (np / 128) + (row >> 7)) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (lane >> 3)];
   const float sc = byte ? __uint_as_float(byte << 23) : __uint_as_float(0x400000u);  // 2^(byte - 127)
-  // E4M3 -> f16 is exact; the lower byte becomes the lower half
-  uint32_t h01, h23;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"(static_cast<uint16_t>(c & 0xFFFFu)));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(static_cast<uint16_t>(c >> 16)));
-  const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-  const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
   float acc = 0.f;
-  acc = __fmaf_rn(f01.x * sc, __uint_as_float(a.x << 16), acc);
-  acc = __fmaf_rn(f01.y * sc, __uint_as_float(a.x & 0xFFFF0000u), acc);
-  acc = __fmaf_rn(f23.x * sc, __uint_as_float(a.y << 16), acc);
-  acc = __fmaf_rn(f23.y * sc, __uint_as_float(a.y & 0xFFFF0000u), acc);
+  acc = __fmaf_rn(e4m3_value(c & 0xFFu) * sc, __uint_as_float(a.x << 16), acc);
+  acc = __fmaf_rn(e4m3_value((c >> 8) & 0xFFu) * sc, __uint_as_float(a.x & 0xFFFF0000u), acc);
+  acc = __fmaf_rn(e4m3_value((c >> 16) & 0xFFu) * sc, __uint_as_float(a.y << 16), acc);
+  acc = __fmaf_rn(e4m3_value(c >> 24) * sc, __uint_as_float(a.y & 0xFFFF0000u), acc);
 #pragma unroll
   for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
   if (lane == 0) {

@@ -4,7 +4,7 @@
 // block-scaled tensor cores, as "PyTorch FlashAttention-4 adds MXFP8
 // block-scaled forward and backward for Blackwell" describes them: Q, K and dO
 // quantised in square 32 x 32 blocks, so that one E4M3 payload in shared
-// memory is read K-major by one product and MN-major by the other (section
+// memory serves the products along d and those along the sequence (section
 // "Quantization along both axes and jagged tensors"), with a scale-factor atom
 // per layout; dS quantised online in square 32 x 32 blocks, so that the dK and
 // dQ products read one representation; P converted online with the constant
@@ -13,36 +13,42 @@
 //
 // One CTA owns a 128-key tile j of one (batch, head) and streams the head's
 // query tiles i (causal: i >= j):
-//   S^T  = K_j Q_i^T           A = K_j, B = Q_i     (both K-major, along d)
-//   dP^T = V_j dO_i^T          A = V_j, B = dO_i    (both K-major, along d)
+//   S^T  = K_j Q_i^T           A = K_j, B = Q_i     (shared memory, K-major)
+//   dP^T = V_j dO_i^T          A = V_j, B = dO_i    (shared memory, K-major)
 //   P^T  = exp2(S^T s log2 e - LSE_i log2 e), to E4M3 x 2^8 in TMEM
 //   dS^T = P^T (dP^T - D_i),    to E4M3 in 32 x 32 blocks, in TMEM and smem
 //   dV_j += P^T dO_i           A = P^T (TMEM), B = dO_i (MN-major)
 //   dK_j += dS^T Q_i           A = dS^T (TMEM), B = Q_i (MN-major)
-//   dQ_i (+)= dS K_j           A = dS (smem, MN-major), B = K_j (MN-major)
+//   dQ_i^T = K_j^T dS^T        A = K_j^T, B = dS (shared memory, K-major)
+// Every product has the operand forms of the MXFP8 forward kernel's two: both
+// operands K-major in shared memory, or A in TMEM with an MN-major B; dQ is
+// therefore taken transposed, from a K-major copy of K_j^T the dQ warps make
+// once, and its rows (d) are turned back into query rows on the way out.
 //
 //   warps 0-7   thread = key row; warps w and w + 4 share key rows 32 (w % 4)
 //               .. and take queries 64 h .. 64 h + 63 (h = w / 4): P^T, dS^T
 //               and their scales, then the dK, dV epilogue
-//   warps 8-11  thread = query row: dQ_i out of TMEM into a shared-memory
-//               buffer of its own, then TMA reduce-adds onto the fp32 dQ
-//   warp 12     TMA: K_j, V_j and their atoms once; Q_i (+ LSE_i log2 e, D_i
-//               and Q's two atoms) and dO_i (+ its two atoms) into a ring
+//   warps 8-11  thread = d column: K_j^T once; then dQ_i^T out of TMEM into
+//               the query-row boxes of the dQ buffer (warp 8 + b fills box b,
+//               columns 32 b .. 32 b + 31) and a TMA reduce-add per box onto
+//               the fp32 dQ
+//   warp 12     TMA: K_j, V_j and their atoms once; Q_i (+ LSE_i log2 e - 8,
+//               D_i and Q's two atoms) and dO_i (+ its two atoms) into a ring
 //   warp 13     MMA issuer (one elected lane); tcgen05.cp of every atom
 //
-// TMEM (512 columns): S^T 0-127, dP^T 128-255, dV 256-383, dK 384-511; dQ_i
+// TMEM (512 columns): S^T 0-127, dP^T 128-255, dV 256-383, dK 384-511; dQ_i^T
 // takes the dP^T columns once the dK product has read dS^T, and the next dP^T
-// waits until the dQ warps have loaded dQ_i. P^T and dS^T as E4M3 take four
-// queries per column: warp h's 64 queries go to columns 64 h .. 64 h + 15 of
-// their region, which that warp alone has read. The scale factors sit in the
-// columns of the S^T and dP^T regions that are dead at the time (the same
-// page, section "TMEM allocation and scale factor placement"):
-//   S^T region  16-19 P^T's scales (the constant), 20-23 dO_i's (dV);
-//               24-31 dS's and K's (dQ_i), 32-39 V's and dO_{i+1}'s (dP_{i+1}):
-//               the last two once the P warps have loaded S^T_{i+1}
-//   dP^T region 16-19 and 80-83 dS^T's scales (per half), 20-23 Q_i's (dK);
-//               24-31 K's and Q_{i+1}'s (S_{i+1}), once the dS warps have
-//               loaded dP^T_i
+// waits until the dQ warps have loaded dQ_i^T. P^T and dS^T as E4M3 take the
+// first 32 columns of their region (four queries per column; warp h's 64
+// queries at 16 h .. 16 h + 15, stored once both warps of the pair have loaded
+// their scores). The scale factors sit in columns of the S^T and dP^T regions
+// that are dead at the time (the same page, section "TMEM allocation and
+// scale factor placement"):
+//   S^T region  32-35 P^T's (the constant), 36-39 dO_i's (dV); 40-47 K^T's and
+//               dS's (dQ_i), once the P warps have loaded S^T_{i+1}, then V's
+//               and dO_{i+1}'s (dP_{i+1}), once dQ_i is complete
+//   dP^T region 32-35 dS^T's, 36-39 Q_i's (dK); 40-47 K's and Q_{i+1}'s
+//               (S_{i+1}), once the dS warps have loaded dP^T_i
 // The first S and dP products read their scales from the dV and dK regions,
 // which no product has written yet. Each extra dependency is one barrier:
 // "dP^T loaded" before S_{i+1}, "S^T loaded" before dQ_i.
@@ -83,32 +89,36 @@ struct BwdMxArgs {
 struct BwdMxCfg {
   static constexpr uint32_t kTileBytes = 128u * 128u;  // 128 x 128 E4M3
   static constexpr uint32_t kAtomBytes = 512u;
-  static constexpr int kStages = 3;
+  static constexpr int kStages = 2;
   static constexpr uint32_t kKOff = 0;
   static constexpr uint32_t kVOff = kTileBytes;
   // K (rows = key), K (rows = d), V (rows = key)
   static constexpr uint32_t kKvAtomOff = 2 * kTileBytes;
-  // stage: Q_i, dO_i, LSE_i log2 e and D_i, Q_i's atoms (rows = query, rows =
-  // d), dO_i's atoms (the same two)
+  // stage: Q_i, dO_i, LSE_i log2 e - 8 and D_i, Q_i's atoms (rows = query,
+  // rows = d), dO_i's atoms (the same two)
   static constexpr uint32_t kStageOff = 34u * 1024u;
   static constexpr uint32_t kVecOff = 2 * kTileBytes;
   static constexpr uint32_t kQAtomOff = kVecOff + 1024;
   static constexpr uint32_t kDoAtomOff = kQAtomOff + 2 * kAtomBytes;
   static constexpr uint32_t kStageBytes = kDoAtomOff + 2 * kAtomBytes;  // 35 KiB
-  static constexpr uint32_t kDsOff = kStageOff + kStages * kStageBytes;  // dS, keys x queries, queries contiguous
+  static constexpr uint32_t kDsOff = kStageOff + kStages * kStageBytes;  // dS, queries x keys, keys contiguous
   static constexpr uint32_t kDsAtomOff = kDsOff + kTileBytes;            // dS's scales, rows = query (dQ product)
-  static constexpr uint32_t kDqBufOff = (kDsAtomOff + kAtomBytes + 1023u) / 1024u * 1024u;
+  static constexpr uint32_t kPairScOff = kDsAtomOff + kAtomBytes;        // dS^T's scale bytes, 4 per key
+  static constexpr uint32_t kKtOff = (kPairScOff + 512u + 1023u) / 1024u * 1024u;  // K^T, d x keys, keys contiguous
+  static constexpr uint32_t kDqBufOff = kKtOff + kTileBytes;
   static constexpr uint32_t kDqBufBytes = 4 * kTileBytes;                // four fp32 32-column boxes
   static constexpr uint32_t kBarOff = kDqBufOff + kDqBufBytes;
-  // kv, q_full[3], q_free[3], do_full[3], do_free[3], s, dp, p, ds, dv_done, k_done, dq, ds_free, dq_read, fin,
-  // drain, dp_loaded, s_loaded
-  static constexpr int kNumBars = 1 + 4 * kStages + 13;
+  // kv, q_full[2], q_free[2], do_full[2], do_free[2], s, dp, p, ds, dv_done, k_done, dq, ds_free, dq_read, fin,
+  // drain, dp_loaded, s_loaded, kt_ready
+  static constexpr int kNumBars = 1 + 4 * kStages + 14;
   static constexpr uint32_t kHolderOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kAbortOff = kHolderOff + 4;
   static constexpr uint32_t kUsed = kAbortOff + 4;
   static constexpr uint32_t kSmemBytes = kUsed + 1024;
   static_assert(kSmemBytes <= 232448u, "shared memory");
-  static_assert(kStageOff % 1024 == 0 && kStageBytes % 1024 == 0 && kDsOff % 1024 == 0, "1024-byte tiles");
+  static_assert(kStageOff % 1024 == 0 && kStageBytes % 1024 == 0 && kDsOff % 1024 == 0 && kKtOff % 1024 == 0 &&
+                    kDqBufOff % 1024 == 0,
+                "1024-byte tiles");
   static_assert(kKvAtomOff + 3 * kAtomBytes <= kStageOff, "K, V atoms");
   static constexpr int kThreads = 512;
   static constexpr int kDqWarp0 = 8, kTmaWarp = 12, kMmaWarp = 13;
@@ -120,9 +130,10 @@ struct BwdMxCfg {
   static_assert(2 * kRegsDs + kRegsDq + kRegsProducer <= 4 * kLaunchRegs, "register split");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 384, kColDq = 128;
-  // scale-factor columns (offsets inside the S^T and dP^T regions)
-  static constexpr uint32_t kSfP = 16, kSfDoT = 20, kSfDs = 24, kSfKT = 28, kSfV = 32, kSfDo = 36;  // S^T region
-  static constexpr uint32_t kSfDsT0 = 16, kSfDsT1 = 80, kSfQT = 20, kSfK = 24, kSfQ = 28;            // dP^T region
+  // scale-factor columns, offsets inside the S^T and dP^T regions: the A
+  // operand's at 32 or 40, the B operand's 4 further
+  static constexpr uint32_t kSfTs = 32;  // TMEM-A products: P^T / dS^T, then dO_i / Q_i
+  static constexpr uint32_t kSfSs = 40;  // shared-memory products: dQ_i and dP_{i+1} (S^T region), S_{i+1} (dP^T region)
   // the constant E8M0 byte of P^T: 2^-8 (P = 1 is held as 256)
   static constexpr uint32_t kPScaleByte = 119u;
 };
@@ -155,6 +166,7 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t bar_drain = bar_s + 80u;
   const uint32_t bar_dpld = bar_s + 88u;  // the dS warps have loaded dP^T_i
   const uint32_t bar_sld = bar_s + 96u;   // the P warps have loaded S^T_i
+  const uint32_t bar_ktr = bar_s + 104u;  // the dQ warps have written K^T
   uint32_t* holder = reinterpret_cast<uint32_t*>(smem + C::kHolderOff);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kAbortOff);
 
@@ -188,6 +200,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(bar_drain, 1);
     mbar_init(bar_dpld, 256);
     mbar_init(bar_sld, 256);
+    mbar_init(bar_ktr, 128);
     *abort_flag = 0u;
     fence_barrier_init();
   }
@@ -285,8 +298,8 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t desc_hi = static_cast<uint32_t>(k0 >> 32);
     const uint32_t k_km = static_cast<uint32_t>(k0);
     const uint32_t v_km = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kVOff, 16, 1024));
-    const uint32_t k_mn = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kKOff, C::kTileBytes, 1024));
-    const uint32_t ds_mn = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kDsOff, C::kTileBytes, 1024));
+    const uint32_t kt_km = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kKtOff, 16, 1024));
+    const uint32_t ds_km = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kDsOff, 16, 1024));
     const uint32_t st_km = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kStageOff, 16, 1024));
     const uint32_t st_mn = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kStageOff, C::kTileBytes, 1024));
     constexpr uint32_t kStageStep = C::kStageBytes >> 4;
@@ -298,9 +311,9 @@ __global__ void __launch_bounds__(512, 1)
       asm volatile("" : "+r"(x));
       return x;
     };
-    // S^T = K Q_i^T or dP^T = V dO_i^T (along d, both K-major): the A and B
-    // atoms are copied to TMEM columns sf and sf + 4 first
-    auto issue_sq = [&](uint32_t a_lo, uint32_t b_lo, uint32_t d_col, uint32_t sf, uint32_t atom_a, uint32_t atom_b) {
+    // D = A B^T with both operands K-major in shared memory (S^T, dP^T,
+    // dQ^T): the A and B atoms are copied to TMEM columns sf and sf + 4 first
+    auto issue_ss = [&](uint32_t a_lo, uint32_t b_lo, uint32_t d_col, uint32_t sf, uint32_t atom_a, uint32_t atom_b) {
       a_lo = opaque(a_lo);
       b_lo = opaque(b_lo);
       if (leader) {
@@ -312,56 +325,31 @@ __global__ void __launch_bounds__(512, 1)
                          kk > 0 ? 1u : 0u, tmem + sf, tmem + sf + 4);
       }
     };
-    // the TMEM column of k-step kk (32 queries) of P^T or dS^T in its region
-    auto a_col = [](uint32_t kk) { return kk < 2 ? 8 * kk : 64 + 8 * (kk - 2); };
-    // dV += P^T dO_i (A from TMEM, B = dO_i MN-major)
-    auto issue_dv = [&](int st, bool first) {
-      const uint32_t b = opaque(st_mn + st * kStageStep + kTileStep);
+    // D += A B with A (E4M3, 32 columns) in TMEM region a_reg, its scales at
+    // a_reg + 32 (written by the P/dS warps), B MN-major in shared memory with
+    // its atom copied to a_reg + 36 (dV = P^T dO_i, dK = dS^T Q_i)
+    auto issue_ts = [&](uint32_t a_reg, uint32_t b_lo, uint32_t d_col, uint32_t atom_b, bool first) {
+      b_lo = opaque(b_lo);
       if (leader) {
-        sf_copy_to_tmem(tmem + C::kColS + C::kSfDoT, stage_addr(st) + C::kDoAtomOff + C::kAtomBytes);
+        sf_copy_to_tmem(tmem + a_reg + C::kSfTs + 4, atom_b);
 #pragma unroll
         for (uint32_t kk = 0; kk < 4; ++kk)
-          mma_mxf8_ts_lo(tmem + C::kColDv, tmem + C::kColS + a_col(kk), b + 256 * kk, desc_hi,
+          mma_mxf8_ts_lo(tmem + d_col, tmem + a_reg + 8 * kk, b_lo + 256 * kk, desc_hi,
                          idesc_mxf8(128, 128, true, kk, kk), (!first || kk > 0) ? 1u : 0u,
-                         tmem + C::kColS + C::kSfP, tmem + C::kColS + C::kSfDoT);
-      }
-    };
-    // dK += dS^T Q_i (A from TMEM with a scale column per half, B = Q_i MN-major)
-    auto issue_dk = [&](int st, bool first) {
-      const uint32_t b = opaque(st_mn + st * kStageStep);
-      if (leader) {
-        sf_copy_to_tmem(tmem + C::kColDp + C::kSfQT, stage_addr(st) + C::kQAtomOff + C::kAtomBytes);
-#pragma unroll
-        for (uint32_t kk = 0; kk < 4; ++kk)
-          mma_mxf8_ts_lo(tmem + C::kColDk, tmem + C::kColDp + a_col(kk), b + 256 * kk, desc_hi,
-                         idesc_mxf8(128, 128, true, kk & 1u, kk), (!first || kk > 0) ? 1u : 0u,
-                         tmem + C::kColDp + (kk < 2 ? C::kSfDsT0 : C::kSfDsT1), tmem + C::kColDp + C::kSfQT);
-      }
-    };
-    // dQ_i = dS K (A = dS MN-major, B = K MN-major, along the keys)
-    auto issue_dq = [&]() {
-      const uint32_t a = opaque(ds_mn), b = opaque(k_mn);
-      if (leader) {
-        sf_copy_to_tmem(tmem + C::kColS + C::kSfDs, sbase + C::kDsAtomOff);
-        sf_copy_to_tmem(tmem + C::kColS + C::kSfKT, atom_kt);
-#pragma unroll
-        for (uint32_t kk = 0; kk < 4; ++kk)
-          mma_mxf8_ss_lo(tmem + C::kColDq, a + 256 * kk, b + 256 * kk, desc_hi,
-                         idesc_mxf8(128, 128, true, kk, kk, false, true), kk > 0 ? 1u : 0u,
-                         tmem + C::kColS + C::kSfDs, tmem + C::kColS + C::kSfKT);
+                         tmem + a_reg + C::kSfTs, tmem + a_reg + C::kSfTs + 4);
       }
     };
     // the first S^T and dP^T take their scales from the dV and dK regions
     bool ok = wait(bar_kv, 0, 52) && wait(bar_qfull(0), 0, 53);
     if (ok) {
       tc_fence_after();
-      issue_sq(k_km, st_km, C::kColS, C::kColDv, atom_k, stage_addr(0) + C::kQAtomOff);
+      issue_ss(k_km, st_km, C::kColS, C::kColDv, atom_k, stage_addr(0) + C::kQAtomOff);
       commit(bar_s);
       ok = wait(bar_dofull(0), 0, 54);
     }
     if (ok) {
       tc_fence_after();
-      issue_sq(v_km, st_km + kTileStep, C::kColDp, C::kColDk, atom_v, stage_addr(0) + C::kDoAtomOff);
+      issue_ss(v_km, st_km + kTileStep, C::kColDp, C::kColDk, atom_v, stage_addr(0) + C::kDoAtomOff);
       commit(bar_dp);
     }
     for (int it = 0; ok && it < n_it; ++it) {
@@ -373,7 +361,9 @@ __global__ void __launch_bounds__(512, 1)
       ok = wait(bar_p, par, 55);
       if (!ok) break;
       tc_fence_after();
-      issue_dv(st, it == 0);
+      // dV += P^T dO_i (B = dO_i MN-major, its atom whose rows are d columns)
+      issue_ts(C::kColS, st_mn + st * kStageStep + kTileStep, C::kColDv,
+               stage_addr(st) + C::kDoAtomOff + C::kAtomBytes, it == 0);
       commit(bar_dvdone);
       commit(bar_dofree(st));  // dO_i: read by dP^T_i (earlier) and this product
       if (more) {
@@ -382,31 +372,37 @@ __global__ void __launch_bounds__(512, 1)
         ok = wait(bar_qfull(st1), par1, 56) && wait(bar_dvdone, par, 57) && wait(bar_dpld, par, 58);
         if (!ok) break;
         tc_fence_after();
-        issue_sq(k_km, st_km + st1 * kStageStep, C::kColS, C::kColDp + C::kSfK, atom_k,
+        issue_ss(k_km, st_km + st1 * kStageStep, C::kColS, C::kColDp + C::kSfSs, atom_k,
                  stage_addr(st1) + C::kQAtomOff);
         commit(bar_s);
       }
       ok = wait(bar_ds, par, 59);
       if (!ok) break;
       tc_fence_after();
-      issue_dk(st, it == 0);
+      // dK += dS^T Q_i (B = Q_i MN-major, its atom whose rows are d columns)
+      issue_ts(C::kColDp, st_mn + st * kStageStep, C::kColDk, stage_addr(st) + C::kQAtomOff + C::kAtomBytes,
+               it == 0);
       commit(bar_kdone);
       commit(bar_qfree(st));  // Q_i: read by S^T_i and this product
-      // dQ_i overwrites dS^T_i (and S^T_{i+1}'s scales) once the dK product
-      // (and with it S^T_{i+1}) is complete; its own scales go into the S^T
-      // region once the P warps have loaded S^T_{i+1}
-      ok = wait(bar_kdone, par, 60) && (!more || wait(bar_sld, static_cast<uint32_t>(it + 1) & 1u, 61));
+      // dQ_i^T = K^T dS^T overwrites dS^T_i (and S^T_{i+1}'s scales) once the
+      // dK product (and with it S^T_{i+1}) is complete; its scales go into the
+      // S^T region once the P warps have loaded S^T_{i+1}; K^T is written once
+      ok = wait(bar_kdone, par, 60) && (!more || wait(bar_sld, static_cast<uint32_t>(it + 1) & 1u, 61)) &&
+           (it > 0 || wait(bar_ktr, 0, 70));
       if (!ok) break;
       tc_fence_after();
-      issue_dq();
+      // A = K^T (rows d, its atom whose rows are d columns), B = dS (rows
+      // queries, the atom the dS warps wrote)
+      issue_ss(kt_km, ds_km, C::kColDq, C::kColS + C::kSfSs, atom_kt, sbase + C::kDsAtomOff);
       commit(bar_dq);
       commit(bar_dsfree);
       if (more) {
-        // dP^T_{i+1} overwrites dQ_i once the dQ warps have loaded it
+        // dP^T_{i+1} overwrites dQ_i^T once the dQ warps have loaded it; its
+        // scales take dQ_i's columns, free once dQ_i is complete
         ok = wait(bar_dqread, par, 62) && wait(bar_dofull(st1), par1, 63);
         if (!ok) break;
         tc_fence_after();
-        issue_sq(v_km, st_km + st1 * kStageStep + kTileStep, C::kColDp, C::kColS + C::kSfV, atom_v,
+        issue_ss(v_km, st_km + st1 * kStageStep + kTileStep, C::kColDp, C::kColS + C::kSfSs, atom_v,
                  stage_addr(st1) + C::kDoAtomOff);
         commit(bar_dp);
       }
@@ -419,6 +415,10 @@ __global__ void __launch_bounds__(512, 1)
   }
   } else if (warp < C::kDqWarp0) {
     // ------------------------------------------------------------ P^T, dS^T (thread = key row)
+    // Warps w and w + 4 share key rows and split the queries; each stores its
+    // half of P^T (dS^T) into the first 32 columns of the region, which the
+    // other warp of the pair may still have to read: the pair loads, meets at
+    // a barrier, then stores (and leaves its loops together).
     regs_increase<C::kRegsDs>();
     const int quad = warp & 3, h = warp >> 2;
     const int r = quad * 32 + lane;
@@ -427,10 +427,14 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t s_tm = tmem + lane_off + C::kColS;
     const uint32_t dp_tm = tmem + lane_off + C::kColDp;
     const float sl2 = args.scale_log2;
-    const uint32_t ds_row = sbase + C::kDsOff + r * 128;
-    // dQ's A atom: row = query m, block = key block (this warp's quad); every
+    // this thread's key is byte r % 16 of chunk r / 16 in every query row of dS
+    const uint32_t ds_col = sbase + C::kDsOff + (r & 15);
+    // dQ's B atom: row = query m, block = key block (this warp's quad); every
     // lane l writes its replica row l
     const uint32_t ds_atom = sbase + C::kDsAtomOff + lane * 16 + quad;
+    // dS^T's scales of key r: one byte per query block, gathered from both
+    // warps of the pair
+    const uint32_t pair_sc = sbase + C::kPairScOff + r * 4;
     // keys past N take no part (their P is 0), so they do not enter the
     // 32 x 32 blocks' maxima
     const bool key_valid = kj < args.n;
@@ -443,9 +447,9 @@ __global__ void __launch_bounds__(512, 1)
       const uint32_t vec = sbase + C::kStageOff + st * C::kStageBytes + C::kVecOff;
       const bool need_mask = (q0 + 128 > args.n) || (CAUSAL && it == 0) || (j * 128 + 128 > args.n);
       const int lim = key_valid ? args.n - 1 - q0 : -1;  // last valid query column of this row
-      ok = __all_sync(0xffffffffu, wait_bar(bar_s, par, abort_flag, args.status, 64) &&
-                                       wait_bar(bar_qfull(st), static_cast<uint32_t>(it / C::kStages) & 1u,
-                                                abort_flag, args.status, 65));
+      ok = pair_all(quad, wait_bar(bar_s, par, abort_flag, args.status, 64) &&
+                              wait_bar(bar_qfull(st), static_cast<uint32_t>(it / C::kStages) & 1u, abort_flag,
+                                       args.status, 65));
       if (!ok) break;
       tc_fence_after();
       // P^T 2^8 = exp2(S^T s log2 e - (LSE log2 e - 8)) for this warp's 64 queries
@@ -478,9 +482,10 @@ __global__ void __launch_bounds__(512, 1)
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) w[e] = pack_e4m3x4(p8[4 * e], p8[4 * e + 1], p8[4 * e + 2], p8[4 * e + 3]);
-        tmem_st16(s_tm + 64 * h, w);
+        pair_sync(quad);  // both warps have loaded their scores
+        tmem_st16(s_tm + 16 * h, w);
         // P^T's scales: the constant 2^-8 for every row and k-step
-        if (h == 0) tmem_st1(s_tm + C::kSfP + quad, C::kPScaleByte * 0x01010101u);
+        if (h == 0) tmem_st1(s_tm + C::kSfTs + quad, C::kPScaleByte * 0x01010101u);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -490,7 +495,7 @@ __global__ void __launch_bounds__(512, 1)
       {
         bool w_ok = wait_bar(bar_dp, par, abort_flag, args.status, 66);
         if (w_ok && it > 0) w_ok = wait_bar(bar_dsfree, par ^ 1u, abort_flag, args.status, 67);
-        ok = __all_sync(0xffffffffu, w_ok);
+        ok = pair_all(quad, w_ok);
       }
       if (!ok) break;
       tc_fence_after();
@@ -502,7 +507,6 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_before();
         mbar_arrive(bar_dpld);
         uint32_t w[16];
-        uint32_t sfw = 0;
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           reg_fence32(u[kk]);
@@ -532,19 +536,33 @@ __global__ void __launch_bounds__(512, 1)
             const int i = 32 * kk + 4 * e;
             w[8 * kk + e] = pack_e4m3x4(p8[i] * inv, p8[i + 1] * inv, p8[i + 2] * inv, p8[i + 3] * inv);
           }
-          sfw |= b << (8 * kk);
-          asm volatile("st.shared.u8 [%0], %1;" ::"r"(ds_atom + (2 * h + kk) * 4), "r"(b) : "memory");
+          const uint32_t qb = static_cast<uint32_t>(2 * h + kk);
+          asm volatile("st.shared.u8 [%0], %1;" ::"r"(pair_sc + qb), "r"(b) : "memory");
+          asm volatile("st.shared.u8 [%0], %1;" ::"r"(ds_atom + qb * 4), "r"(b) : "memory");
         }
-        // dS^T for the dK product, with its scales (k-steps 2h, 2h + 1)
-        tmem_st16(dp_tm + 64 * h, w);
-        tmem_st1(dp_tm + (h ? C::kSfDsT1 : C::kSfDsT0) + quad, sfw);
-        // dS for the dQ product: key row r, queries 64h .. 64h + 63 = 16-byte
-        // chunks 4h .. 4h + 3 of the 128-byte swizzled row
+        // dS for the dQ product, K-major: a 128-byte row per query m (64h +
+        // 4e + b, byte b of word e), the keys' 16-byte chunks swizzled by m % 8
+        {
+          uint32_t off[8];
 #pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4) {
-          const uint32_t chunk = static_cast<uint32_t>(4 * h + v4);
-          st_shared_v4(ds_row + ((chunk ^ static_cast<uint32_t>(r & 7)) << 4), w[4 * v4], w[4 * v4 + 1],
-                       w[4 * v4 + 2], w[4 * v4 + 3]);
+          for (int x = 0; x < 8; ++x) off[x] = ((static_cast<uint32_t>(r >> 4) ^ static_cast<uint32_t>(x)) << 4);
+          const uint32_t base = ds_col + static_cast<uint32_t>(64 * h) * 128u;
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              const int m = 4 * e + b;
+              asm volatile("st.shared.u8 [%0], %1;" ::"r"(base + m * 128 + off[m & 7]), "r"(w[e] >> (8 * b))
+                           : "memory");
+            }
+        }
+        pair_sync(quad);  // both warps have loaded dP^T and written their scale bytes
+        // dS^T for the dK product, with its scales (one byte per query block)
+        tmem_st16(dp_tm + 16 * h, w);
+        if (h == 0) {
+          uint32_t sc;
+          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sc) : "r"(pair_sc) : "memory");
+          tmem_st1(dp_tm + C::kSfTs + quad, sc);
         }
       }
       tmem_st_wait();
@@ -582,21 +600,57 @@ __global__ void __launch_bounds__(512, 1)
     }
     tc_fence_before();
   } else {
-    // ------------------------------------------------------------ dQ (thread = query row)
-    // dQ_i leaves TMEM in two halves (the next dP^T may take the columns after
-    // the second) into the four 32-column fp32 boxes of the dQ buffer
-    // (128-byte rows, 128-byte swizzle), which four TMA reduce-adds, one bulk
-    // group, add onto the fp32 dQ.
+    // ------------------------------------------------------------ dQ (thread = d column)
+    // Warp 8 + b owns d columns 32 b .. 32 b + 31: it writes their rows of
+    // K^T once, then for every query tile loads their rows of dQ_i^T (two
+    // halves of 64 queries; the next dP^T may take the columns after the
+    // second) into box b of the dQ buffer -- 128 query rows of 32 fp32, 128-byte
+    // rows, 128-byte swizzle -- which its lane 0 reduce-adds onto the fp32 dQ.
     regs_increase<C::kRegsDq>();
-    const int q = (warp - C::kDqWarp0) * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>((warp - C::kDqWarp0) * 32) << 16;
-    const bool issuer = q == 0;
-    bool ok = true;
+    const int wq = warp - C::kDqWarp0;
+    const int dcol = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    bool ok = __all_sync(0xffffffffu, wait_bar(bar_kv, 0, abort_flag, args.status, 71));
+    if (ok) {
+      // K^T row dcol, K-major: key k is byte k % 16 of chunk k / 16, the chunks
+      // swizzled by dcol % 8; K_j holds (key k, column dcol) at byte dcol % 16
+      // of chunk (dcol / 16) ^ (k % 8) of row k
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t word = 0;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int k = 16 * c + 4 * q4 + e;
+            const uint32_t src = sbase + C::kKOff + k * 128 +
+                                 (((static_cast<uint32_t>(dcol >> 4)) ^ static_cast<uint32_t>(k & 7)) << 4) +
+                                 (dcol & 15);
+            uint32_t byte;
+            asm volatile("ld.shared.u8 %0, [%1];" : "=r"(byte) : "r"(src) : "memory");
+            word |= (byte & 0xFFu) << (8 * e);
+          }
+          wv[q4] = word;
+        }
+        st_shared_v4(sbase + C::kKtOff + dcol * 128 + ((static_cast<uint32_t>(c) ^ static_cast<uint32_t>(dcol & 7)) << 4),
+                     wv[0], wv[1], wv[2], wv[3]);
+      }
+      fence_async_shared();  // K^T, before the tensor core reads it
+      mbar_arrive(bar_ktr);
+    }
+    // this lane's column of box wq: float lane % 4 of 16-byte chunk lane / 4,
+    // the chunks swizzled by the row's query % 8
+    uint32_t off[8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x)
+      off[x] = (((static_cast<uint32_t>(lane) >> 2) ^ static_cast<uint32_t>(x)) << 4) + (static_cast<uint32_t>(lane) & 3u) * 4u;
+    const uint32_t box = sbase + C::kDqBufOff + static_cast<uint32_t>(wq) * C::kTileBytes;
     for (int it = 0; ok && it < n_it; ++it) {
-      // the previous dQ's reduce-adds have read the buffer (the issuer waits
-      // before the group barrier)
-      if (issuer && it > 0) bulk_wait_read();
-      ok = dq_group_all(wait_bar(bar_dq, static_cast<uint32_t>(it) & 1u, abort_flag, args.status, 69));
+      // this warp's previous reduce-add has read the box
+      if (lane == 0 && it > 0) bulk_wait_read();
+      __syncwarp();
+      ok = __all_sync(0xffffffffu, wait_bar(bar_dq, static_cast<uint32_t>(it) & 1u, abort_flag, args.status, 69));
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
@@ -611,25 +665,23 @@ __global__ void __launch_bounds__(512, 1)
         }
 #pragma unroll
         for (int b2 = 0; b2 < 2; ++b2) {
-          const uint32_t slot = sbase + C::kDqBufOff + (2 * half + b2) * C::kTileBytes;
           reg_fence32(u[b2]);
 #pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4)
-            st_shared_v4(slot + q * 128 + ((static_cast<uint32_t>(c4) ^ static_cast<uint32_t>(q & 7)) << 4),
-                         u[b2][4 * c4], u[b2][4 * c4 + 1], u[b2][4 * c4 + 2], u[b2][4 * c4 + 3]);
+          for (int i = 0; i < 32; ++i) {
+            const int q = 64 * half + 32 * b2 + i;
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(box + q * 128 + off[q & 7]), "r"(u[b2][i]) : "memory");
+          }
         }
       }
       fence_async_shared();
-      dq_group_sync();
-      if (issuer) {
-#pragma unroll
-        for (int bb = 0; bb < 4; ++bb)
-          tma_reduce_add_3d(&tm_dq, sbase + C::kDqBufOff + bb * C::kTileBytes, 32 * bb, (i0 + it) * 128, bh);
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_3d(&tm_dq, box, 32 * wq, (i0 + it) * 128, bh);
         bulk_commit();
       }
       __syncwarp();
     }
-    if (issuer) bulk_wait_all();
+    if (lane == 0) bulk_wait_all();
   }
 
   __syncthreads();
