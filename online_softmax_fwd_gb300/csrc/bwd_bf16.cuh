@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(512, 1)
   // (each register-count change sits inside its role's branch: ptxas sizes a
   // region by the setmaxnreg that dominates it)
   if (warp >= C::kTmaWarp) {
-  regs_decrease<C::kRegsProducer>();
+  regs_to<C::kRegsProducer, C::kLaunchRegs>();
   if (warp == C::kTmaWarp) {
     // ------------------------------------------------------------ TMA
     const uint32_t leader = elect_one();
@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(512, 1)
     // over the first half of the fp32 columns they come from, which the other
     // warp of the pair may still have to read: the pair loads its columns,
     // meets at a barrier, then stores.
-    regs_increase<C::kRegsDs>();
+    regs_to<C::kRegsDs, C::kLaunchRegs>();
     const int quad = warp & 3, h = warp >> 2;
     const int r = quad * 32 + lane;
     const int kj = j * 128 + r;
@@ -614,7 +614,7 @@ __global__ void __launch_bounds__(512, 1)
     tc_fence_before();
   } else {
     // ------------------------------------------------------------ dQ (thread = query row)
-    regs_increase<C::kRegsDq>();
+    regs_to<C::kRegsDq, C::kLaunchRegs>();
     // dQ_i leaves TMEM at once (the next dP^T may then take its columns) and
     // goes out through dO_i's buffer (the dV product that read dO_i is
     // complete before dQ_i is computed) as 32-column fp32 boxes (128-byte
@@ -700,7 +700,9 @@ cudaError_t launch_bwd_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, co
   cudaFuncAttributes fa;
   e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;
-  if (fa.numRegs < C::kLaunchRegs) return cudaErrorInvalidConfiguration;
+  // (each warpgroup moves from exactly this count: setmaxnreg.inc only raises
+  // it, setmaxnreg.dec only lowers it)
+  if (fa.numRegs != C::kLaunchRegs) return cudaErrorInvalidConfiguration;
   const long long ctas = static_cast<long long>(args.bh) * args.n_tiles;
   kernel<<<static_cast<unsigned>(ctas), C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_do, tm_dq, args);
   return cudaGetLastError();

@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(512, 1)
 
   // (each register-count change sits inside its role's branch)
   if (warp >= C::kTmaWarp) {
-  regs_decrease<C::kRegsProducer>();
+  regs_to<C::kRegsProducer, C::kLaunchRegs>();
   if (warp == C::kTmaWarp) {
     // ------------------------------------------------------------ TMA
     const uint32_t leader = elect_one();
@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(512, 1)
     // half of P^T (dS^T) into the first 32 columns of the region, which the
     // other warp of the pair may still have to read: the pair loads, meets at
     // a barrier, then stores (and leaves its loops together).
-    regs_increase<C::kRegsDs>();
+    regs_to<C::kRegsDs, C::kLaunchRegs>();
     const int quad = warp & 3, h = warp >> 2;
     const int r = quad * 32 + lane;
     const int kj = j * 128 + r;
@@ -606,7 +606,7 @@ __global__ void __launch_bounds__(512, 1)
     // halves of 64 queries; the next dP^T may take the columns after the
     // second) into box b of the dQ buffer -- 128 query rows of 32 fp32, 128-byte
     // rows, 128-byte swizzle -- which its lane 0 reduce-adds onto the fp32 dQ.
-    regs_increase<C::kRegsDq>();
+    regs_to<C::kRegsDq, C::kLaunchRegs>();
     const int wq = warp - C::kDqWarp0;
     const int dcol = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
@@ -703,7 +703,9 @@ cudaError_t launch_bwd_mxfp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, c
   cudaFuncAttributes fa;
   e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;
-  if (fa.numRegs < C::kLaunchRegs) return cudaErrorInvalidConfiguration;
+  // (each warpgroup moves from exactly this count: setmaxnreg.inc only raises
+  // it, setmaxnreg.dec only lowers it)
+  if (fa.numRegs != C::kLaunchRegs) return cudaErrorInvalidConfiguration;
   const long long ctas = static_cast<long long>(args.bh) * args.n_tiles;
   kernel<<<static_cast<unsigned>(ctas), C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_do, tm_dq, args);
   return cudaGetLastError();

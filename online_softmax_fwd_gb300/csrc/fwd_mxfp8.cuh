@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp >= 8) {
     // ============================================================ producer warpgroup
-    regs_decrease<C::kRegsOther>();
+    regs_to<C::kRegsOther, C::kLaunchRegs>();
     if (warp == 8) {
       // ---------------------------------------------------------- TMA: Q0, Q1 (+ atoms), then K_j, V_j
       const uint32_t leader = elect_one();
@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else {
     // ============================================================ softmax warpgroups
-    regs_increase<C::kRegsSoftmax>();
+    regs_to<C::kRegsSoftmax, C::kLaunchRegs>();
     const int t = warp >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
@@ -556,7 +556,9 @@ cudaError_t launch_fwd_mxfp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, c
   cudaFuncAttributes fa;
   e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;
-  if (fa.numRegs < MxCfg::kLaunchRegs) return cudaErrorInvalidConfiguration;
+  // (each warpgroup moves from exactly this count: setmaxnreg.inc only raises
+  // it, setmaxnreg.dec only lowers it)
+  if (fa.numRegs != MxCfg::kLaunchRegs) return cudaErrorInvalidConfiguration;
   kernel<<<static_cast<unsigned>(ctas), MxCfg::kThreads, MxCfg::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, args, wl);
   return cudaGetLastError();
 }

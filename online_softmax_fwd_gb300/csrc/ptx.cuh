@@ -285,5 +285,16 @@ template <uint32_t N>
 __device__ __forceinline__ void regs_decrease() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
+// Move a warpgroup from the FROM registers per thread it was launched with to
+// N: setmaxnreg.inc may only raise the count and setmaxnreg.dec only lower it,
+// so the direction is chosen here, at compile time.
+template <uint32_t N, uint32_t FROM>
+__device__ __forceinline__ void regs_to() {
+  static_assert(N >= 24 && N <= 256 && N % 8 == 0, "setmaxnreg takes 24 .. 256 in steps of 8");
+  if constexpr (N > FROM)
+    regs_increase<N>();
+  else if constexpr (N < FROM)
+    regs_decrease<N>();
+}
 
 }  // namespace attn
