@@ -108,6 +108,21 @@ bool make_map_f32(CUtensorMap* m, void* base, int d, int n, long long bh) {
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over a transposed fp32 accumulator [B*H, d, np] for reduce-adds:
+// x = the sequence (N valid of a row stride of np), 32 x 32 boxes (128-byte
+// rows, 128-byte swizzle); columns past N are not written.
+bool make_map_f32_t(CUtensorMap* m, void* base, int d, int n, int np, long long bh) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(np) * 4u, static_cast<cuuint64_t>(np) * 4u * static_cast<cuuint64_t>(d)};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // SMs of the current device, queried once per device (the persistent grid size)
 int sm_count() {
   static std::atomic<int> cache[kMaxDevices];
@@ -213,7 +228,7 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128) || N > kMaxN) return 0;
   const size_t bh = static_cast<size_t>(B) * H;
   const size_t np = (static_cast<size_t>(N) + 127) / 128 * 128;
-  const size_t acc = (bh * N * d * 4 + 255) / 256 * 256;
+  const size_t acc = (bh * np * d * 4 + 255) / 256 * 256;
   return acc + 2 * ((bh * np * 4 + 255) / 256 * 256);
 }
 
@@ -240,7 +255,7 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
   unsigned int* status = status_word();
   if (!status) return ATTN_ERR_CUDA;
   const int np = (N + 127) / 128 * 128;
-  const size_t acc_bytes = (static_cast<size_t>(bh) * N * d * 4 + 255) / 256 * 256;
+  const size_t acc_bytes = (static_cast<size_t>(bh) * np * d * 4 + 255) / 256 * 256;
   const size_t vec_bytes = (static_cast<size_t>(bh) * np * 4 + 255) / 256 * 256;
   float* dq_acc = static_cast<float*>(workspace);
   CUtensorMap mdq;
@@ -296,11 +311,11 @@ attn_status_t attn_bwd_mxfp8(const void* q8, const void* q_sf, const void* k8, c
   unsigned int* status = status_word();
   if (!status) return ATTN_ERR_CUDA;
   const int np = (N + 127) / 128 * 128;
-  const size_t acc_bytes = (static_cast<size_t>(bh) * N * d * 4 + 255) / 256 * 256;
+  const size_t acc_bytes = (static_cast<size_t>(bh) * np * d * 4 + 255) / 256 * 256;
   const size_t vec_bytes = (static_cast<size_t>(bh) * np * 4 + 255) / 256 * 256;
-  float* dq_acc = static_cast<float*>(workspace);
+  float* dq_acc = static_cast<float*>(workspace);  // transposed: [B*H, d, np]
   CUtensorMap mdq;
-  if (!make_map_f32(&mdq, dq_acc, d, N, bh)) return ATTN_ERR_CUDA;
+  if (!make_map_f32_t(&mdq, dq_acc, d, N, np, bh)) return ATTN_ERR_CUDA;
   float* lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes);
   float* dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes + vec_bytes);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -331,7 +346,7 @@ attn_status_t attn_bwd_mxfp8(const void* q8, const void* q_sf, const void* k8, c
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   cudaError_t e = attn::launch_bwd_mxfp8_d128(causal, mq, mk, mv, mdo, mdq, a, st);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
-  e = attn::launch_bwd_post(dq_acc, dq, bh * N * static_cast<long long>(d), scale, st);
+  e = attn::launch_bwd_post_t(dq_acc, dq, bh, N, np, scale, st);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -4,8 +4,10 @@
 //             dQ accumulator zeroed;
 //   bwd_prep_mxfp8: the same with dO from its E4M3 codes times its blocks'
 //             E8M0 scales, and LSE_i log2(e) - 8 (the MXFP8 kernel's exp then
-//             gives P 2^8, the constant scale of P in E4M3);
-//   bwd_post: dQ = s * accumulator, rounded to bf16.
+//             gives P 2^8, the constant scale of P in E4M3); its accumulator
+//             is transposed, [B*H, d, np];
+//   bwd_post: dQ = s * accumulator, rounded to bf16 (bwd_post_t: from the
+//             transposed accumulator).
 // All are bandwidth-bound elementwise passes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -87,6 +89,9 @@ __global__ void __launch_bounds__(256) bwd_prep_mxfp8_kernel(const __nv_bfloat16
   const long long bh = blockIdx.y;
   if (row >= np) return;
   const size_t prow = static_cast<size_t>(bh) * np + row;
+  // the head's transposed accumulator [128, np] holds 128 np floats: row
+  // index r zeroes floats 128 r .. 128 r + 127 of it
+  reinterpret_cast<float4*>(dq_acc + prow * 128)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (row >= n) {
     if (lane == 0) {
       lse2[prow] = 0.f;
@@ -113,7 +118,27 @@ __global__ void __launch_bounds__(256) bwd_prep_mxfp8_kernel(const __nv_bfloat16
     dvec[prow] = acc;
     lse2[prow] = lse[grow] * 1.4426950408889634f - 8.0f;
   }
-  reinterpret_cast<float4*>(dq_acc + grow * 128)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// dQ[bh, q, c] = bf16(s acc[bh, c, q]) through a 32 x 32 shared-memory tile:
+// reads along q, writes along c, both coalesced
+__global__ void __launch_bounds__(256) bwd_post_t_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
+                                                         int n, int np, float scale) {
+  __shared__ float tile[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int q0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  const long long bh = blockIdx.z;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int c = c0 + ty + 8 * k, q = q0 + tx;
+    tile[ty + 8 * k][tx] = q < n ? acc[(static_cast<size_t>(bh) * 128 + c) * np + q] : 0.f;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int q = q0 + ty + 8 * k, c = c0 + tx;
+    if (q < n) dq[(static_cast<size_t>(bh) * n + q) * 128 + c] = __float2bfloat16_rn(tile[tx][ty + 8 * k] * scale);
+  }
 }
 
 // four elements per thread
@@ -152,6 +177,13 @@ cudaError_t launch_bwd_prep_mxfp8(const void* o, const void* do8, const void* do
   bwd_prep_mxfp8_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
                                                   static_cast<const uint8_t*>(do8), static_cast<const uint8_t*>(do_sf),
                                                   lse, lse2, dvec, dq_acc, n, np);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_post_t(const float* dq_acc, void* dq, long long bh, int n, int np, float scale,
+                              cudaStream_t stream) {
+  dim3 grid(static_cast<unsigned>((n + 31) / 32), 4, static_cast<unsigned>(bh));
+  bwd_post_t_kernel<<<grid, 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n, np, scale);
   return cudaGetLastError();
 }
 

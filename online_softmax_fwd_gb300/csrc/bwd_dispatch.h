@@ -21,7 +21,11 @@ cudaError_t launch_bwd_bf16_d128(int causal, const CUtensorMap& q, const CUtenso
 // and LSE log2 e - 8 (P comes out of the exp already scaled by 2^8)
 cudaError_t launch_bwd_prep_mxfp8(const void* o, const void* do8, const void* do_sf, const float* lse, float* lse2,
                                   float* dvec, float* dq_acc, long long bh, int n, int np, cudaStream_t stream);
-// q, k, v, dout: 3-D maps over the E4M3 payloads (128 x 128 boxes)
+// dQ from the transposed accumulator [B*H, 128, np] (MXFP8)
+cudaError_t launch_bwd_post_t(const float* dq_acc, void* dq, long long bh, int n, int np, float scale,
+                              cudaStream_t stream);
+// q, k, v, dout: 3-D maps over the E4M3 payloads (128 x 128 boxes); dq: over
+// the transposed fp32 accumulator, 32 x 32 boxes
 cudaError_t launch_bwd_mxfp8_d128(int causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                   const CUtensorMap& dout, const CUtensorMap& dq, const BwdMxArgs& a,
                                   cudaStream_t s);

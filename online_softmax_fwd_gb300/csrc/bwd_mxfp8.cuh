@@ -19,19 +19,19 @@
 //   dS^T = P^T (dP^T - D_i),    to E4M3 in 32 x 32 blocks, in TMEM and smem
 //   dV_j += P^T dO_i           A = P^T (TMEM), B = dO_i (MN-major)
 //   dK_j += dS^T Q_i           A = dS^T (TMEM), B = Q_i (MN-major)
-//   dQ_i^T = K_j^T dS^T        A = K_j^T, B = dS (shared memory, K-major)
-// Every product has the operand forms of the MXFP8 forward kernel's two: both
-// operands K-major in shared memory, or A in TMEM with an MN-major B; dQ is
-// therefore taken transposed, from a K-major copy of K_j^T the dQ warps make
-// once, and its rows (d) are turned back into query rows on the way out.
+//   dQ_i^T = K_j^T dS^T        A = K_j^T (K-major), B = dS (MN-major)
+// dQ is taken transposed (A then comes from a K-major copy of K_j^T the dQ
+// warps make once), so that every product has its A operand K-major or in
+// TMEM; the fp32 dQ accumulator is kept transposed too, [B*H, d, N], and the
+// last kernel turns it back while rounding to bf16.
 //
 //   warps 0-7   thread = key row; warps w and w + 4 share key rows 32 (w % 4)
 //               .. and take queries 64 h .. 64 h + 63 (h = w / 4): P^T, dS^T
 //               and their scales, then the dK, dV epilogue
 //   warps 8-11  thread = d column: K_j^T once; then dQ_i^T out of TMEM into
-//               the query-row boxes of the dQ buffer (warp 8 + b fills box b,
-//               columns 32 b .. 32 b + 31) and a TMA reduce-add per box onto
-//               the fp32 dQ
+//               the dQ buffer (warp 8 + b: d rows 32 b .. 32 b + 31, four
+//               boxes of 32 queries) and TMA reduce-adds onto the transposed
+//               fp32 dQ
 //   warp 12     TMA: K_j, V_j and their atoms once; Q_i (+ LSE_i log2 e - 8,
 //               D_i and Q's two atoms) and dO_i (+ its two atoms) into a ring
 //   warp 13     MMA issuer (one elected lane); tcgen05.cp of every atom
@@ -101,12 +101,13 @@ struct BwdMxCfg {
   static constexpr uint32_t kQAtomOff = kVecOff + 1024;
   static constexpr uint32_t kDoAtomOff = kQAtomOff + 2 * kAtomBytes;
   static constexpr uint32_t kStageBytes = kDoAtomOff + 2 * kAtomBytes;  // 35 KiB
-  static constexpr uint32_t kDsOff = kStageOff + kStages * kStageBytes;  // dS, queries x keys, keys contiguous
+  static constexpr uint32_t kDsOff = kStageOff + kStages * kStageBytes;  // dS, keys x queries, queries contiguous
   static constexpr uint32_t kDsAtomOff = kDsOff + kTileBytes;            // dS's scales, rows = query (dQ product)
   static constexpr uint32_t kPairScOff = kDsAtomOff + kAtomBytes;        // dS^T's scale bytes, 4 per key
   static constexpr uint32_t kKtOff = (kPairScOff + 512u + 1023u) / 1024u * 1024u;  // K^T, d x keys, keys contiguous
   static constexpr uint32_t kDqBufOff = kKtOff + kTileBytes;
-  static constexpr uint32_t kDqBufBytes = 4 * kTileBytes;                // four fp32 32-column boxes
+  static constexpr uint32_t kDqBufBytes = 4 * kTileBytes;                // per dQ warp 4 boxes of 32 d x 32 fp32
+  static constexpr uint32_t kDqBoxBytes = 32u * 128u;
   static constexpr uint32_t kBarOff = kDqBufOff + kDqBufBytes;
   // kv, q_full[2], q_free[2], do_full[2], do_free[2], s, dp, p, ds, dv_done, k_done, dq, ds_free, dq_read, fin,
   // drain, dp_loaded, s_loaded, kt_ready
@@ -299,7 +300,7 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t k_km = static_cast<uint32_t>(k0);
     const uint32_t v_km = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kVOff, 16, 1024));
     const uint32_t kt_km = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kKtOff, 16, 1024));
-    const uint32_t ds_km = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kDsOff, 16, 1024));
+    const uint32_t ds_mn = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kDsOff, C::kTileBytes, 1024));
     const uint32_t st_km = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kStageOff, 16, 1024));
     const uint32_t st_mn = static_cast<uint32_t>(smem_desc_sw128(sbase + C::kStageOff, C::kTileBytes, 1024));
     constexpr uint32_t kStageStep = C::kStageBytes >> 4;
@@ -311,9 +312,11 @@ __global__ void __launch_bounds__(512, 1)
       asm volatile("" : "+r"(x));
       return x;
     };
-    // D = A B^T with both operands K-major in shared memory (S^T, dP^T,
-    // dQ^T): the A and B atoms are copied to TMEM columns sf and sf + 4 first
-    auto issue_ss = [&](uint32_t a_lo, uint32_t b_lo, uint32_t d_col, uint32_t sf, uint32_t atom_a, uint32_t atom_b) {
+    // D = A B^T with both operands in shared memory, A K-major, B K-major
+    // (S^T, dP^T) or MN-major (dQ^T): the A and B atoms are copied to TMEM
+    // columns sf and sf + 4 first
+    auto issue_ss = [&](uint32_t a_lo, uint32_t b_lo, uint32_t d_col, uint32_t sf, uint32_t atom_a, uint32_t atom_b,
+                        bool b_mn) {
       a_lo = opaque(a_lo);
       b_lo = opaque(b_lo);
       if (leader) {
@@ -321,8 +324,8 @@ __global__ void __launch_bounds__(512, 1)
         sf_copy_to_tmem(tmem + sf + 4, atom_b);
 #pragma unroll
         for (uint32_t kk = 0; kk < 4; ++kk)
-          mma_mxf8_ss_lo(tmem + d_col, a_lo + 2 * kk, b_lo + 2 * kk, desc_hi, idesc_mxf8(128, 128, false, kk, kk),
-                         kk > 0 ? 1u : 0u, tmem + sf, tmem + sf + 4);
+          mma_mxf8_ss_lo(tmem + d_col, a_lo + 2 * kk, b_lo + (b_mn ? 256 : 2) * kk, desc_hi,
+                         idesc_mxf8(128, 128, b_mn, kk, kk), kk > 0 ? 1u : 0u, tmem + sf, tmem + sf + 4);
       }
     };
     // D += A B with A (E4M3, 32 columns) in TMEM region a_reg, its scales at
@@ -343,13 +346,13 @@ __global__ void __launch_bounds__(512, 1)
     bool ok = wait(bar_kv, 0, 52) && wait(bar_qfull(0), 0, 53);
     if (ok) {
       tc_fence_after();
-      issue_ss(k_km, st_km, C::kColS, C::kColDv, atom_k, stage_addr(0) + C::kQAtomOff);
+      issue_ss(k_km, st_km, C::kColS, C::kColDv, atom_k, stage_addr(0) + C::kQAtomOff, false);
       commit(bar_s);
       ok = wait(bar_dofull(0), 0, 54);
     }
     if (ok) {
       tc_fence_after();
-      issue_ss(v_km, st_km + kTileStep, C::kColDp, C::kColDk, atom_v, stage_addr(0) + C::kDoAtomOff);
+      issue_ss(v_km, st_km + kTileStep, C::kColDp, C::kColDk, atom_v, stage_addr(0) + C::kDoAtomOff, false);
       commit(bar_dp);
     }
     for (int it = 0; ok && it < n_it; ++it) {
@@ -373,7 +376,7 @@ __global__ void __launch_bounds__(512, 1)
         if (!ok) break;
         tc_fence_after();
         issue_ss(k_km, st_km + st1 * kStageStep, C::kColS, C::kColDp + C::kSfSs, atom_k,
-                 stage_addr(st1) + C::kQAtomOff);
+                 stage_addr(st1) + C::kQAtomOff, false);
         commit(bar_s);
       }
       ok = wait(bar_ds, par, 59);
@@ -392,8 +395,8 @@ __global__ void __launch_bounds__(512, 1)
       if (!ok) break;
       tc_fence_after();
       // A = K^T (rows d, its atom whose rows are d columns), B = dS (rows
-      // queries, the atom the dS warps wrote)
-      issue_ss(kt_km, ds_km, C::kColDq, C::kColS + C::kSfSs, atom_kt, sbase + C::kDsAtomOff);
+      // queries, MN-major; the atom the dS warps wrote)
+      issue_ss(kt_km, ds_mn, C::kColDq, C::kColS + C::kSfSs, atom_kt, sbase + C::kDsAtomOff, true);
       commit(bar_dq);
       commit(bar_dsfree);
       if (more) {
@@ -403,7 +406,7 @@ __global__ void __launch_bounds__(512, 1)
         if (!ok) break;
         tc_fence_after();
         issue_ss(v_km, st_km + st1 * kStageStep + kTileStep, C::kColDp, C::kColS + C::kSfSs, atom_v,
-                 stage_addr(st1) + C::kDoAtomOff);
+                 stage_addr(st1) + C::kDoAtomOff, false);
         commit(bar_dp);
       }
     }
@@ -427,8 +430,8 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t s_tm = tmem + lane_off + C::kColS;
     const uint32_t dp_tm = tmem + lane_off + C::kColDp;
     const float sl2 = args.scale_log2;
-    // this thread's key is byte r % 16 of chunk r / 16 in every query row of dS
-    const uint32_t ds_col = sbase + C::kDsOff + (r & 15);
+    // this thread's row of dS (keys x queries, 128-byte swizzled rows)
+    const uint32_t ds_row = sbase + C::kDsOff + r * 128;
     // dQ's B atom: row = query m, block = key block (this warp's quad); every
     // lane l writes its replica row l
     const uint32_t ds_atom = sbase + C::kDsAtomOff + lane * 16 + quad;
@@ -540,21 +543,13 @@ __global__ void __launch_bounds__(512, 1)
           asm volatile("st.shared.u8 [%0], %1;" ::"r"(pair_sc + qb), "r"(b) : "memory");
           asm volatile("st.shared.u8 [%0], %1;" ::"r"(ds_atom + qb * 4), "r"(b) : "memory");
         }
-        // dS for the dQ product, K-major: a 128-byte row per query m (64h +
-        // 4e + b, byte b of word e), the keys' 16-byte chunks swizzled by m % 8
-        {
-          uint32_t off[8];
+        // dS for the dQ product: key row r, queries 64h .. 64h + 63 = 16-byte
+        // chunks 4h .. 4h + 3 of the 128-byte swizzled row
 #pragma unroll
-          for (int x = 0; x < 8; ++x) off[x] = ((static_cast<uint32_t>(r >> 4) ^ static_cast<uint32_t>(x)) << 4);
-          const uint32_t base = ds_col + static_cast<uint32_t>(64 * h) * 128u;
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-              const int m = 4 * e + b;
-              asm volatile("st.shared.u8 [%0], %1;" ::"r"(base + m * 128 + off[m & 7]), "r"(w[e] >> (8 * b))
-                           : "memory");
-            }
+        for (int v4 = 0; v4 < 4; ++v4) {
+          const uint32_t chunk = static_cast<uint32_t>(4 * h + v4);
+          st_shared_v4(ds_row + ((chunk ^ static_cast<uint32_t>(r & 7)) << 4), w[4 * v4], w[4 * v4 + 1],
+                       w[4 * v4 + 2], w[4 * v4 + 3]);
         }
         pair_sync(quad);  // both warps have loaded dP^T and written their scale bytes
         // dS^T for the dK product, with its scales (one byte per query block)
@@ -601,11 +596,12 @@ __global__ void __launch_bounds__(512, 1)
     tc_fence_before();
   } else {
     // ------------------------------------------------------------ dQ (thread = d column)
-    // Warp 8 + b owns d columns 32 b .. 32 b + 31: it writes their rows of
+    // Warp 8 + b owns d rows 32 b .. 32 b + 31 of dQ^T: it writes their rows of
     // K^T once, then for every query tile loads their rows of dQ_i^T (two
     // halves of 64 queries; the next dP^T may take the columns after the
-    // second) into box b of the dQ buffer -- 128 query rows of 32 fp32, 128-byte
-    // rows, 128-byte swizzle -- which its lane 0 reduce-adds onto the fp32 dQ.
+    // second) into four boxes of 32 queries -- 32 rows of 32 fp32, 128-byte
+    // rows, 128-byte swizzle -- which its lane 0 reduce-adds onto the
+    // transposed fp32 dQ.
     regs_to<C::kRegsDq, C::kLaunchRegs>();
     const int wq = warp - C::kDqWarp0;
     const int dcol = wq * 32 + lane;
@@ -639,15 +635,11 @@ __global__ void __launch_bounds__(512, 1)
       fence_async_shared();  // K^T, before the tensor core reads it
       mbar_arrive(bar_ktr);
     }
-    // this lane's column of box wq: float lane % 4 of 16-byte chunk lane / 4,
-    // the chunks swizzled by the row's query % 8
-    uint32_t off[8];
-#pragma unroll
-    for (int x = 0; x < 8; ++x)
-      off[x] = (((static_cast<uint32_t>(lane) >> 2) ^ static_cast<uint32_t>(x)) << 4) + (static_cast<uint32_t>(lane) & 3u) * 4u;
-    const uint32_t box = sbase + C::kDqBufOff + static_cast<uint32_t>(wq) * C::kTileBytes;
+    // this lane's row in each box: 16-byte chunk c at ((c ^ lane % 8) << 4)
+    const uint32_t boxes = sbase + C::kDqBufOff + static_cast<uint32_t>(wq) * 4u * C::kDqBoxBytes;
+    const uint32_t row = boxes + static_cast<uint32_t>(lane) * 128u;
     for (int it = 0; ok && it < n_it; ++it) {
-      // this warp's previous reduce-add has read the box
+      // this warp's previous reduce-adds have read the boxes
       if (lane == 0 && it > 0) bulk_wait_read();
       __syncwarp();
       ok = __all_sync(0xffffffffu, wait_bar(bar_dq, static_cast<uint32_t>(it) & 1u, abort_flag, args.status, 69));
@@ -666,17 +658,19 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int b2 = 0; b2 < 2; ++b2) {
           reg_fence32(u[b2]);
+          const uint32_t box_row = row + static_cast<uint32_t>(2 * half + b2) * C::kDqBoxBytes;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int q = 64 * half + 32 * b2 + i;
-            asm volatile("st.shared.b32 [%0], %1;" ::"r"(box + q * 128 + off[q & 7]), "r"(u[b2][i]) : "memory");
-          }
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(box_row + ((static_cast<uint32_t>(c) ^ static_cast<uint32_t>(lane & 7)) << 4),
+                         u[b2][4 * c], u[b2][4 * c + 1], u[b2][4 * c + 2], u[b2][4 * c + 3]);
         }
       }
       fence_async_shared();
       __syncwarp();
       if (lane == 0) {
-        tma_reduce_add_3d(&tm_dq, box, 32 * wq, (i0 + it) * 128, bh);
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb)
+          tma_reduce_add_3d(&tm_dq, boxes + bb * C::kDqBoxBytes, (i0 + it) * 128 + 32 * bb, 32 * wq, bh);
         bulk_commit();
       }
       __syncwarp();

@@ -153,8 +153,8 @@ def test_bwd_rejects_bad_arguments(lib):
     A = 1 << 20  # fake, 256-byte aligned addresses: rejected calls never dereference them
     B, H, N, d = 1, 2, 300, 128
     need = lib.attn_bwd_workspace_bytes(B, H, N, d)
-    # fp32 dQ accumulator + two padded fp32 row vectors (LSE log2 e, D)
-    assert need == (B * H * N * d * 4 + 255) // 256 * 256 + 2 * ((B * H * 384 * 4 + 255) // 256 * 256)
+    # fp32 dQ accumulator and two fp32 row vectors (LSE log2 e, D), N padded to 128
+    assert need == (B * H * 384 * d * 4 + 255) // 256 * 256 + 2 * ((B * H * 384 * 4 + 255) // 256 * 256)
     assert lib.attn_bwd_workspace_bytes(B, H, N, 96) == 0
     assert lib.attn_bwd_workspace_bytes(0, H, N, d) == 0
 
