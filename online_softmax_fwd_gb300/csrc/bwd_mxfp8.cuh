@@ -38,17 +38,18 @@
 //
 // TMEM (512 columns): S^T 0-127, dP^T 128-255, dV 256-383, dK 384-511; dQ_i^T
 // takes the dP^T columns once the dK product has read dS^T, and the next dP^T
-// waits until the dQ warps have loaded dQ_i^T. P^T and dS^T as E4M3 take the
-// first 32 columns of their region (four queries per column; warp h's 64
-// queries at 16 h .. 16 h + 15, stored once both warps of the pair have loaded
-// their scores). The scale factors sit in columns of the S^T and dP^T regions
-// that are dead at the time (the same page, section "TMEM allocation and
-// scale factor placement"):
+// waits until the dQ warps have loaded dQ_i^T. P^T and dS^T as E4M3 (four
+// queries per column) take columns 0-15 (queries 0-63, warp h = 0) and 64-79
+// (queries 64-127, h = 1) of their region, among the columns each warp loaded
+// itself. The scale factors sit in columns of the S^T and dP^T regions that
+// are dead at the time (the same page, section "TMEM allocation and scale
+// factor placement"):
 //   S^T region  32-35 P^T's (the constant), 36-39 dO_i's (dV); 40-47 K^T's and
 //               dS's (dQ_i), once the P warps have loaded S^T_{i+1}, then V's
 //               and dO_{i+1}'s (dP_{i+1}), once dQ_i is complete
-//   dP^T region 32-35 dS^T's, 36-39 Q_i's (dK); 40-47 K's and Q_{i+1}'s
-//               (S_{i+1}), once the dS warps have loaded dP^T_i
+//   dP^T region 32-35 and 96-99 dS^T's (query blocks 0-1 and 2-3), 36-39
+//               Q_i's (dK); 40-47 K's and Q_{i+1}'s (S_{i+1}), once the dS
+//               warps have loaded dP^T_i
 // The first S and dP products read their scales from the dV and dK regions,
 // which no product has written yet. Each extra dependency is one barrier:
 // "dP^T loaded" before S_{i+1}, "S^T loaded" before dQ_i.
@@ -103,8 +104,7 @@ struct BwdMxCfg {
   static constexpr uint32_t kStageBytes = kDoAtomOff + 2 * kAtomBytes;  // 35 KiB
   static constexpr uint32_t kDsOff = kStageOff + kStages * kStageBytes;  // dS, keys x queries, queries contiguous
   static constexpr uint32_t kDsAtomOff = kDsOff + kTileBytes;            // dS's scales, rows = query (dQ product)
-  static constexpr uint32_t kPairScOff = kDsAtomOff + kAtomBytes;        // dS^T's scale bytes, 4 per key
-  static constexpr uint32_t kKtOff = (kPairScOff + 512u + 1023u) / 1024u * 1024u;  // K^T, d x keys, keys contiguous
+  static constexpr uint32_t kKtOff = (kDsAtomOff + kAtomBytes + 1023u) / 1024u * 1024u;  // K^T, d x keys, keys contiguous
   static constexpr uint32_t kDqBufOff = kKtOff + kTileBytes;
   static constexpr uint32_t kDqBufBytes = 4 * kTileBytes;                // per dQ warp 4 boxes of 32 d x 32 fp32
   static constexpr uint32_t kDqBoxBytes = 32u * 128u;
@@ -123,17 +123,18 @@ struct BwdMxCfg {
   static_assert(kKvAtomOff + 3 * kAtomBytes <= kStageOff, "K, V atoms");
   static constexpr int kThreads = 512;
   static constexpr int kDqWarp0 = 8, kTmaWarp = 12, kMmaWarp = 13;
-  // setmaxnreg: 4 warps x 32 x (2 x 152 + 112 + 96) = 512 threads x 128 at launch
+  // setmaxnreg: 4 warps x 32 x (2 x 152 + 120 + 88) = 512 threads x 128 at launch
   static constexpr uint32_t kRegsDs = 152;
-  static constexpr uint32_t kRegsDq = 112;
-  static constexpr uint32_t kRegsProducer = 96;
+  static constexpr uint32_t kRegsDq = 120;
+  static constexpr uint32_t kRegsProducer = 88;
   static constexpr int kLaunchRegs = 128;
   static_assert(2 * kRegsDs + kRegsDq + kRegsProducer <= 4 * kLaunchRegs, "register split");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 384, kColDq = 128;
   // scale-factor columns, offsets inside the S^T and dP^T regions: the A
   // operand's at 32 or 40, the B operand's 4 further
-  static constexpr uint32_t kSfTs = 32;  // TMEM-A products: P^T / dS^T, then dO_i / Q_i
+  static constexpr uint32_t kSfTs = 32;  // TMEM-A products: P^T / dS^T (queries 0-63), then dO_i / Q_i
+  static constexpr uint32_t kSfTsHi = 96;  // dS^T's scales for queries 64-127
   static constexpr uint32_t kSfSs = 40;  // shared-memory products: dQ_i and dP_{i+1} (S^T region), S_{i+1} (dP^T region)
   // the constant E8M0 byte of P^T: 2^-8 (P = 1 is held as 256)
   static constexpr uint32_t kPScaleByte = 119u;
@@ -328,18 +329,21 @@ __global__ void __launch_bounds__(512, 1)
                          idesc_mxf8(128, 128, b_mn, kk, kk), kk > 0 ? 1u : 0u, tmem + sf, tmem + sf + 4);
       }
     };
-    // D += A B with A (E4M3, 32 columns) in TMEM region a_reg, its scales at
-    // a_reg + 32 (written by the P/dS warps), B MN-major in shared memory with
-    // its atom copied to a_reg + 36 (dV = P^T dO_i, dK = dS^T Q_i)
-    auto issue_ts = [&](uint32_t a_reg, uint32_t b_lo, uint32_t d_col, uint32_t atom_b, bool first) {
+    // D += A B with A (E4M3) in TMEM region a_reg -- k-steps 0, 1 (queries
+    // 0-63) at columns 0-15, k-steps 2, 3 at 64-79 -- its scales at a_reg + 32
+    // (P^T: one constant column; dS^T: bytes of query blocks 0, 1 there and of
+    // 2, 3 at a_reg + 96), B MN-major in shared memory with its atom copied to
+    // a_reg + 36 (dV = P^T dO_i, dK = dS^T Q_i)
+    auto issue_ts = [&](uint32_t a_reg, uint32_t b_lo, uint32_t d_col, uint32_t atom_b, bool first, bool split_sf) {
       b_lo = opaque(b_lo);
       if (leader) {
         sf_copy_to_tmem(tmem + a_reg + C::kSfTs + 4, atom_b);
 #pragma unroll
         for (uint32_t kk = 0; kk < 4; ++kk)
-          mma_mxf8_ts_lo(tmem + d_col, tmem + a_reg + 8 * kk, b_lo + 256 * kk, desc_hi,
-                         idesc_mxf8(128, 128, true, kk, kk), (!first || kk > 0) ? 1u : 0u,
-                         tmem + a_reg + C::kSfTs, tmem + a_reg + C::kSfTs + 4);
+          mma_mxf8_ts_lo(tmem + d_col, tmem + a_reg + (kk < 2 ? 8 * kk : 64 + 8 * (kk - 2)), b_lo + 256 * kk,
+                         desc_hi, idesc_mxf8(128, 128, true, split_sf ? (kk & 1u) : kk, kk),
+                         (!first || kk > 0) ? 1u : 0u,
+                         tmem + a_reg + (split_sf && kk >= 2 ? C::kSfTsHi : C::kSfTs), tmem + a_reg + C::kSfTs + 4);
       }
     };
     // the first S^T and dP^T take their scales from the dV and dK regions
@@ -366,7 +370,7 @@ __global__ void __launch_bounds__(512, 1)
       tc_fence_after();
       // dV += P^T dO_i (B = dO_i MN-major, its atom whose rows are d columns)
       issue_ts(C::kColS, st_mn + st * kStageStep + kTileStep, C::kColDv,
-               stage_addr(st) + C::kDoAtomOff + C::kAtomBytes, it == 0);
+               stage_addr(st) + C::kDoAtomOff + C::kAtomBytes, it == 0, false);
       commit(bar_dvdone);
       commit(bar_dofree(st));  // dO_i: read by dP^T_i (earlier) and this product
       if (more) {
@@ -384,7 +388,7 @@ __global__ void __launch_bounds__(512, 1)
       tc_fence_after();
       // dK += dS^T Q_i (B = Q_i MN-major, its atom whose rows are d columns)
       issue_ts(C::kColDp, st_mn + st * kStageStep, C::kColDk, stage_addr(st) + C::kQAtomOff + C::kAtomBytes,
-               it == 0);
+               it == 0, true);
       commit(bar_kdone);
       commit(bar_qfree(st));  // Q_i: read by S^T_i and this product
       // dQ_i^T = K^T dS^T overwrites dS^T_i (and S^T_{i+1}'s scales) once the
@@ -419,9 +423,7 @@ __global__ void __launch_bounds__(512, 1)
   } else if (warp < C::kDqWarp0) {
     // ------------------------------------------------------------ P^T, dS^T (thread = key row)
     // Warps w and w + 4 share key rows and split the queries; each stores its
-    // half of P^T (dS^T) into the first 32 columns of the region, which the
-    // other warp of the pair may still have to read: the pair loads, meets at
-    // a barrier, then stores (and leaves its loops together).
+    // half of P^T (dS^T) and its scales over the 64 columns it loaded itself.
     regs_to<C::kRegsDs, C::kLaunchRegs>();
     const int quad = warp & 3, h = warp >> 2;
     const int r = quad * 32 + lane;
@@ -435,9 +437,6 @@ __global__ void __launch_bounds__(512, 1)
     // dQ's B atom: row = query m, block = key block (this warp's quad); every
     // lane l writes its replica row l
     const uint32_t ds_atom = sbase + C::kDsAtomOff + lane * 16 + quad;
-    // dS^T's scales of key r: one byte per query block, gathered from both
-    // warps of the pair
-    const uint32_t pair_sc = sbase + C::kPairScOff + r * 4;
     // keys past N take no part (their P is 0), so they do not enter the
     // 32 x 32 blocks' maxima
     const bool key_valid = kj < args.n;
@@ -450,9 +449,9 @@ __global__ void __launch_bounds__(512, 1)
       const uint32_t vec = sbase + C::kStageOff + st * C::kStageBytes + C::kVecOff;
       const bool need_mask = (q0 + 128 > args.n) || (CAUSAL && it == 0) || (j * 128 + 128 > args.n);
       const int lim = key_valid ? args.n - 1 - q0 : -1;  // last valid query column of this row
-      ok = pair_all(quad, wait_bar(bar_s, par, abort_flag, args.status, 64) &&
-                              wait_bar(bar_qfull(st), static_cast<uint32_t>(it / C::kStages) & 1u, abort_flag,
-                                       args.status, 65));
+      ok = __all_sync(0xffffffffu, wait_bar(bar_s, par, abort_flag, args.status, 64) &&
+                                       wait_bar(bar_qfull(st), static_cast<uint32_t>(it / C::kStages) & 1u,
+                                                abort_flag, args.status, 65));
       if (!ok) break;
       tc_fence_after();
       // P^T 2^8 = exp2(S^T s log2 e - (LSE log2 e - 8)) for this warp's 64 queries
@@ -485,8 +484,7 @@ __global__ void __launch_bounds__(512, 1)
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) w[e] = pack_e4m3x4(p8[4 * e], p8[4 * e + 1], p8[4 * e + 2], p8[4 * e + 3]);
-        pair_sync(quad);  // both warps have loaded their scores
-        tmem_st16(s_tm + 16 * h, w);
+        tmem_st16(s_tm + 64 * h, w);
         // P^T's scales: the constant 2^-8 for every row and k-step
         if (h == 0) tmem_st1(s_tm + C::kSfTs + quad, C::kPScaleByte * 0x01010101u);
       }
@@ -498,7 +496,7 @@ __global__ void __launch_bounds__(512, 1)
       {
         bool w_ok = wait_bar(bar_dp, par, abort_flag, args.status, 66);
         if (w_ok && it > 0) w_ok = wait_bar(bar_dsfree, par ^ 1u, abort_flag, args.status, 67);
-        ok = pair_all(quad, w_ok);
+        ok = __all_sync(0xffffffffu, w_ok);
       }
       if (!ok) break;
       tc_fence_after();
@@ -510,6 +508,7 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_before();
         mbar_arrive(bar_dpld);
         uint32_t w[16];
+        uint32_t sfw = 0;
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           reg_fence32(u[kk]);
@@ -540,7 +539,7 @@ __global__ void __launch_bounds__(512, 1)
             w[8 * kk + e] = pack_e4m3x4(p8[i] * inv, p8[i + 1] * inv, p8[i + 2] * inv, p8[i + 3] * inv);
           }
           const uint32_t qb = static_cast<uint32_t>(2 * h + kk);
-          asm volatile("st.shared.u8 [%0], %1;" ::"r"(pair_sc + qb), "r"(b) : "memory");
+          sfw |= b << (8 * kk);
           asm volatile("st.shared.u8 [%0], %1;" ::"r"(ds_atom + qb * 4), "r"(b) : "memory");
         }
         // dS for the dQ product: key row r, queries 64h .. 64h + 63 = 16-byte
@@ -551,14 +550,10 @@ __global__ void __launch_bounds__(512, 1)
           st_shared_v4(ds_row + ((chunk ^ static_cast<uint32_t>(r & 7)) << 4), w[4 * v4], w[4 * v4 + 1],
                        w[4 * v4 + 2], w[4 * v4 + 3]);
         }
-        pair_sync(quad);  // both warps have loaded dP^T and written their scale bytes
-        // dS^T for the dK product, with its scales (one byte per query block)
-        tmem_st16(dp_tm + 16 * h, w);
-        if (h == 0) {
-          uint32_t sc;
-          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sc) : "r"(pair_sc) : "memory");
-          tmem_st1(dp_tm + C::kSfTs + quad, sc);
-        }
+        // dS^T for the dK product over this warp's own columns, with its
+        // scales (query blocks 2h, 2h + 1)
+        tmem_st16(dp_tm + 64 * h, w);
+        tmem_st1(dp_tm + (h ? C::kSfTsHi : C::kSfTs) + quad, sfw);
       }
       tmem_st_wait();
       fence_async_shared();  // dS and its atom, before the tensor core reads them
