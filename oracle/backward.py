@@ -147,3 +147,55 @@ def attention_bwd_mxfp8(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarr
             for dst, src in zip(out, g):
                 dst[b, h] = src
     return out[0], out[1], out[2]
+
+
+def attention_bwd_mxfp8_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, o: np.ndarray, do: np.ndarray,
+                             lse: np.ndarray, causal: bool, scale: float, q_rows, k_rows) -> dict:
+    """``attention_bwd_mxfp8_head`` at chosen rows only, for long sequences:
+    dQ at the query rows ``q_rows`` and dK, dV at the key rows ``k_rows`` of
+    one head (inputs as there). dS is rounded in the same 32 x 32 blocks, so a
+    query row needs the dS rows of its 32-row block against every key, and a
+    key row the dS columns of its 32-key block against every query; those are
+    the only parts computed. Returns a dict with dq, dk, dv (rows in the given
+    order) and the rounded dS rows ("ds_rows"), dS columns ("ds_cols") and P
+    columns ("p_cols") they were summed from."""
+    qd, kd, vd, dod = (quantize_blocks(np.asarray(x, dtype=np.float64))[2] for x in (q, k, v, do))
+    o, lse = np.asarray(o, dtype=np.float64), np.asarray(lse, dtype=np.float64)
+    n = qd.shape[0]
+    d_row = (dod * o).sum(axis=1)
+    out = {"dq": [], "ds_rows": [], "dk": [], "dv": [], "ds_cols": [], "p_cols": []}
+    rows_of_block = {}
+    for i in q_rows:
+        rows_of_block.setdefault(int(i) // 32, []).append(int(i))
+    dq_at = {}
+    for b, rows in rows_of_block.items():
+        r0, r1 = 32 * b, min(n, 32 * b + 32)
+        p = np.exp(scale * (qd[r0:r1] @ kd.T) - lse[r0:r1, None])
+        if causal:
+            p = np.where(np.arange(n)[None, :] <= np.arange(r0, r1)[:, None], p, 0.0)
+        ds8 = quantize_blocks(p * (dod[r0:r1] @ vd.T - d_row[r0:r1, None]))[2]
+        for i in rows:
+            dq_at[i] = (scale * (ds8[i - r0] @ kd), ds8[i - r0])
+    for i in q_rows:
+        out["dq"].append(dq_at[int(i)][0])
+        out["ds_rows"].append(dq_at[int(i)][1])
+    cols_of_block = {}
+    for j in k_rows:
+        cols_of_block.setdefault(int(j) // 32, []).append(int(j))
+    dk_at = {}
+    for c, cols in cols_of_block.items():
+        c0, c1 = 32 * c, min(n, 32 * c + 32)
+        p = np.exp(scale * (qd @ kd[c0:c1].T) - lse[:, None])
+        if causal:
+            p = np.where(np.arange(c0, c1)[None, :] <= np.arange(n)[:, None], p, 0.0)
+        ds8 = quantize_blocks(p * (dod @ vd[c0:c1].T - d_row[:, None]))[2]
+        p8 = p_to_mxfp8_constant(p)
+        for j in cols:
+            dk_at[j] = (scale * (ds8[:, j - c0] @ qd), p8[:, j - c0] @ dod, ds8[:, j - c0], p8[:, j - c0])
+    for j in k_rows:
+        dk, dv, dsc, pc = dk_at[int(j)]
+        out["dk"].append(dk)
+        out["dv"].append(dv)
+        out["ds_cols"].append(dsc)
+        out["p_cols"].append(pc)
+    return {key: np.array(val) for key, val in out.items()}

@@ -143,3 +143,24 @@ def test_repeated_calls_identical_dk_dv(attn):
     a = run(attn, q, k, v, o, do, lse, True, d ** -0.5)
     b = run(attn, q, k, v, o, do, lse, True, d ** -0.5)
     assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+
+
+@pytest.mark.parametrize("name", ["bwd_bf16_b4h16n4096d128", "bwd_bf16_causal_b2h16n8192d128_qk2"])
+def test_full_workload_sampled(attn, name):
+    # the benchmark's workload at full size and in its launch configuration
+    # (O and LSE from attn_fwd, as there), sampled rows of the first and the
+    # last head against both oracles
+    w = I.WORKLOADS[name]
+    q, k, v = I.bf16_qkv(w)
+    do = I.to_bf16(I.draw_grad(w.B, w.H, w.N, w.d, seed=w.seed + 1))
+    qd, kd, vd, dod = (x.to(DEV) for x in (q, k, v, do))
+    o, lse = attn.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale)
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, dod, lse, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert attn.device_status() == attn.Status.OK
+    got = [I.as_f64(x.cpu()) for x in (dq, dk, dv)]
+    f64 = [I.as_f64(x) for x in (q, k, v)] + [I.as_f64(o.cpu()), I.as_f64(do), lse.double().cpu().numpy()]
+    rows = sample_rows(w.N, np.random.default_rng(9))
+    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
+        check_head([g[b, h] for g in got], [x[b, h] for x in f64], w.causal, w.scale, f"{name} head ({b},{h})",
+                   rows=rows)

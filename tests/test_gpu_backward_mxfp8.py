@@ -181,3 +181,41 @@ def test_repeated_calls_identical_dk_dv(attn):
     a = run(attn, q, k, v, do, o, lse, True, 128 ** -0.5)
     b = run(attn, q, k, v, do, o, lse, True, 128 ** -0.5)
     assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+
+
+@pytest.mark.parametrize("name", ["bwd_mxfp8_b4h16n4096d128", "bwd_mxfp8_causal_b2h16n16384d128"])
+def test_full_workload_sampled(attn, name):
+    # the benchmark's workload at full size and in its launch configuration
+    # (O and LSE from the MXFP8 forward, as there), checked on sampled rows of
+    # the first and the last head against the row-sampled oracle
+    from oracle.backward import attention_bwd_mxfp8_rows
+    w = I.WORKLOADS[name]
+    xq, xk, xv = I.draw_fp32(w.B, w.H, w.N, w.d, w.qk_std, w.v_std, w.seed)
+    xdo = I.draw_grad(w.B, w.H, w.N, w.d, seed=w.seed + 1)
+    t = [torch.from_numpy(x).to(DEV) for x in (xq, xk, xv, xdo)]
+    fq, fq_sf = attn.mxfp8_quantize(t[0], role=0)
+    fk, fk_sf = attn.mxfp8_quantize(t[1], role=0)
+    fv, fv_sf = attn.mxfp8_quantize(t[2], role=1)
+    o, lse = attn.attn_fwd_mxfp8(fq, fq_sf, fk, fk_sf, fv, fv_sf, causal=w.causal, scale=w.scale)
+    del fq, fq_sf, fk, fk_sf, fv, fv_sf
+    q8, q_sf = attn.mxfp8_quantize(t[0], role=2)
+    k8, k_sf = attn.mxfp8_quantize(t[1], role=2)
+    v8, v_sf = attn.mxfp8_quantize(t[2], role=0)
+    do8, do_sf = attn.mxfp8_quantize(t[3], role=2)
+    dq, dk, dv = attn.attn_bwd_mxfp8(q8, q_sf, k8, k_sf, v8, v_sf, o, do8, do_sf, lse, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert attn.device_status() == attn.Status.OK
+    o_h, lse_h = I.as_f64(o.cpu()), lse.double().cpu().numpy()
+    rows = sample_rows(w.N, np.random.default_rng(9))
+    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
+        args = (xq[b, h].astype(np.float64), xk[b, h].astype(np.float64), xv[b, h].astype(np.float64), o_h[b, h],
+                xdo[b, h].astype(np.float64), lse_h[b, h])
+        ref = attention_bwd_mxfp8_rows(*args, w.causal, w.scale, rows, rows)
+        qd, kd, dod = (quantize_blocks(x)[2] for x in (args[0], args[1], args[4]))
+        all_r = np.arange(len(rows))
+        for what, got, want, a, m, s in (
+                ("dQ", dq, ref["dq"], np.abs(ref["ds_rows"]), np.abs(kd), w.scale),
+                ("dK", dk, ref["dk"], np.abs(ref["ds_cols"]), np.abs(qd), w.scale),
+                ("dV", dv, ref["dv"], np.abs(ref["p_cols"]), np.abs(dod), 1.0)):
+            g = I.as_f64(got[b, h].cpu())[rows]
+            check(g, want, s * _max_products(a, m, all_r), s * (a @ m), f"{name} head ({b},{h}) {what}")

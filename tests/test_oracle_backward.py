@@ -187,3 +187,21 @@ def test_mxfp8_backward_within_the_fp8_rounding_bound(causal):
     assert np.all(np.abs(got_q - ex_q) <= scale * eps_ds @ np.abs(kd) + 1e-12)
     # and the rounding is really there: the outputs differ from the exact ones
     assert np.abs(got_k - ex_k).max() > 1e-6 and np.abs(got_v - ex_v).max() > 1e-6
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_mxfp8_rows_equal_the_whole_head(causal):
+    # the row-sampled form computes the same numbers as the whole head, at
+    # rows inside, at the edge of and across 32-row blocks, ragged tail included
+    from oracle.backward import attention_bwd_mxfp8_head, attention_bwd_mxfp8_rows
+    n, d, scale = 203, 16, 0.4
+    rng = np.random.default_rng(8)
+    q, k, v, do = (rng.standard_normal((1, 1, n, d)) for _ in range(4))
+    o, lse = attention_fwd(q, k, v, causal, scale)
+    args = (q[0, 0], k[0, 0], v[0, 0], o[0, 0], do[0, 0], lse[0, 0], causal, scale)
+    dq, dk, dv = attention_bwd_mxfp8_head(*args)
+    rows = np.array([0, 31, 32, 95, 100, 191, 192, 202])
+    got = attention_bwd_mxfp8_rows(*args, rows, rows[::-1])
+    np.testing.assert_allclose(got["dq"], dq[rows], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(got["dk"], dk[rows[::-1]], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(got["dv"], dv[rows[::-1]], rtol=0, atol=1e-12)
