@@ -33,8 +33,9 @@
 //               boxes of 32 queries) and TMA reduce-adds onto the transposed
 //               fp32 dQ
 //   warp 12     TMA: K_j, V_j and their atoms once; Q_i (+ LSE_i log2 e - 8,
-//               D_i and Q's two atoms) and dO_i (+ its two atoms) into a ring
+//               D_i and Q's two atoms) into a ring of stages
 //   warp 13     MMA issuer (one elected lane); tcgen05.cp of every atom
+//   warp 14     TMA: dO_i (+ its two atoms) into the same stages
 //
 // TMEM (512 columns): S^T 0-127, dP^T 128-255, dV 256-383, dK 384-511; dQ_i^T
 // takes the dP^T columns once the dK product has read dS^T, and the next dP^T
@@ -122,7 +123,7 @@ struct BwdMxCfg {
                 "1024-byte tiles");
   static_assert(kKvAtomOff + 3 * kAtomBytes <= kStageOff, "K, V atoms");
   static constexpr int kThreads = 512;
-  static constexpr int kDqWarp0 = 8, kTmaWarp = 12, kMmaWarp = 13;
+  static constexpr int kDqWarp0 = 8, kTmaWarp = 12, kMmaWarp = 13, kDoWarp = 14;
   // setmaxnreg: 4 warps x 32 x (2 x 152 + 120 + 88) = 512 threads x 128 at launch
   static constexpr uint32_t kRegsDs = 152;
   static constexpr uint32_t kRegsDq = 120;
@@ -218,14 +219,16 @@ __global__ void __launch_bounds__(512, 1)
   // (each register-count change sits inside its role's branch)
   if (warp >= C::kTmaWarp) {
   regs_to<C::kRegsProducer, C::kLaunchRegs>();
-  if (warp == C::kTmaWarp) {
+  if (warp == C::kTmaWarp || warp == C::kDoWarp) {
     // ------------------------------------------------------------ TMA
+    // Two loaders, so that neither waits behind the other's buffer: warp 12
+    // K_j, V_j (once) and Q_i, warp 14 dO_i. Q_i's stage frees after the dK
+    // product, dO_i's after the dV product, one product apart in time.
     const uint32_t leader = elect_one();
     const uint64_t pol_stream = policy_evict_first();  // K_j, V_j: this CTA alone
     const uint64_t pol_keep = policy_evict_last();     // Q_i, dO_i: every key tile of the head
-    bool ok = true;
-    int it = 0;
-    if (leader) {
+    const bool q_side = warp == C::kTmaWarp;
+    if (q_side && leader) {
       mbar_arrive_expect_tx(bar_kv, 2 * C::kTileBytes + 3 * C::kAtomBytes);
       tma_load_3d_hint(sbase + C::kKOff, &tm_k, bar_kv, 0, j * 128, bh, pol_stream);
       tma_load_3d_hint(sbase + C::kVOff, &tm_v, bar_kv, 0, j * 128, bh, pol_stream);
@@ -234,53 +237,40 @@ __global__ void __launch_bounds__(512, 1)
       bulk_load(sbase + C::kKvAtomOff + C::kAtomBytes, args.k_sf_t + a, C::kAtomBytes, bar_kv);
       bulk_load(sbase + C::kKvAtomOff + 2 * C::kAtomBytes, args.v_sf + a, C::kAtomBytes, bar_kv);
     }
-    int nq = 0, ndo = 0;  // loads issued
-    auto load_q = [&](int i) {
+    int issued = 0;
+    for (int i = 0; i < n_it; ++i) {
       const int st = i % C::kStages;
       const uint32_t ph = static_cast<uint32_t>(i / C::kStages) & 1u;
-      if (!__all_sync(0xffffffffu, wait_bar(bar_qfree(st), ph ^ 1u, abort_flag, args.status, 50))) return false;
-      if (leader) {
-        const int row = (i0 + i) * 128;
-        const uint32_t dst = sbase + C::kStageOff + st * C::kStageBytes;
-        mbar_arrive_expect_tx(bar_qfull(st), C::kTileBytes + 1024 + 2 * C::kAtomBytes);
-        tma_load_3d_hint(dst, &tm_q, bar_qfull(st), 0, row, bh, pol_keep);
-        const size_t vrow = static_cast<size_t>(bh) * args.np + row;
-        bulk_load(dst + C::kVecOff, args.lse2 + vrow, 512, bar_qfull(st));
-        bulk_load(dst + C::kVecOff + 512, args.dvec + vrow, 512, bar_qfull(st));
-        const size_t a = (head_atoms + i0 + i) * C::kAtomBytes;
-        bulk_load(dst + C::kQAtomOff, args.q_sf + a, C::kAtomBytes, bar_qfull(st));
-        bulk_load(dst + C::kQAtomOff + C::kAtomBytes, args.q_sf_t + a, C::kAtomBytes, bar_qfull(st));
+      const uint32_t dst = sbase + C::kStageOff + st * C::kStageBytes;
+      const size_t a = (head_atoms + i0 + i) * C::kAtomBytes;
+      if (q_side) {
+        if (!__all_sync(0xffffffffu, wait_bar(bar_qfree(st), ph ^ 1u, abort_flag, args.status, 50))) break;
+        if (leader) {
+          const int row = (i0 + i) * 128;
+          mbar_arrive_expect_tx(bar_qfull(st), C::kTileBytes + 1024 + 2 * C::kAtomBytes);
+          tma_load_3d_hint(dst, &tm_q, bar_qfull(st), 0, row, bh, pol_keep);
+          const size_t vrow = static_cast<size_t>(bh) * args.np + row;
+          bulk_load(dst + C::kVecOff, args.lse2 + vrow, 512, bar_qfull(st));
+          bulk_load(dst + C::kVecOff + 512, args.dvec + vrow, 512, bar_qfull(st));
+          bulk_load(dst + C::kQAtomOff, args.q_sf + a, C::kAtomBytes, bar_qfull(st));
+          bulk_load(dst + C::kQAtomOff + C::kAtomBytes, args.q_sf_t + a, C::kAtomBytes, bar_qfull(st));
+        }
+      } else {
+        if (!__all_sync(0xffffffffu, wait_bar(bar_dofree(st), ph ^ 1u, abort_flag, args.status, 51))) break;
+        if (leader) {
+          mbar_arrive_expect_tx(bar_dofull(st), C::kTileBytes + 2 * C::kAtomBytes);
+          tma_load_3d_hint(dst + C::kTileBytes, &tm_do, bar_dofull(st), 0, (i0 + i) * 128, bh, pol_keep);
+          bulk_load(dst + C::kDoAtomOff, args.do_sf + a, C::kAtomBytes, bar_dofull(st));
+          bulk_load(dst + C::kDoAtomOff + C::kAtomBytes, args.do_sf_t + a, C::kAtomBytes, bar_dofull(st));
+        }
       }
-      ++nq;
-      return true;
-    };
-    auto load_do = [&](int i) {
-      const int st = i % C::kStages;
-      const uint32_t ph = static_cast<uint32_t>(i / C::kStages) & 1u;
-      if (!__all_sync(0xffffffffu, wait_bar(bar_dofree(st), ph ^ 1u, abort_flag, args.status, 51))) return false;
-      if (leader) {
-        const uint32_t dst = sbase + C::kStageOff + st * C::kStageBytes;
-        mbar_arrive_expect_tx(bar_dofull(st), C::kTileBytes + 2 * C::kAtomBytes);
-        tma_load_3d_hint(dst + C::kTileBytes, &tm_do, bar_dofull(st), 0, (i0 + i) * 128, bh, pol_keep);
-        const size_t a = (head_atoms + i0 + i) * C::kAtomBytes;
-        bulk_load(dst + C::kDoAtomOff, args.do_sf + a, C::kAtomBytes, bar_dofull(st));
-        bulk_load(dst + C::kDoAtomOff + C::kAtomBytes, args.do_sf_t + a, C::kAtomBytes, bar_dofull(st));
-      }
-      ++ndo;
-      return true;
-    };
-    // Q_i one iteration ahead of dO_i (S^T_{i+1} comes before dP^T_{i+1})
-    ok = load_q(0);
-    for (; ok && it < n_it; ++it) {
-      if (it + 1 < n_it) ok = load_q(it + 1);
-      if (ok) ok = load_do(it);
+      ++issued;
     }
-    if (!ok) {
-      drain_bar(bar_kv, 0);
-      for (int s = nq - C::kStages < 0 ? 0 : nq - C::kStages; s < nq; ++s)
-        drain_bar(bar_qfull(s % C::kStages), (s / C::kStages) & 1);
-      for (int s = ndo - C::kStages < 0 ? 0 : ndo - C::kStages; s < ndo; ++s)
-        drain_bar(bar_dofull(s % C::kStages), (s / C::kStages) & 1);
+    if (issued < n_it) {
+      // a wait gave up: the copies in flight land before the CTA leaves
+      if (q_side) drain_bar(bar_kv, 0);
+      for (int s = issued - C::kStages < 0 ? 0 : issued - C::kStages; s < issued; ++s)
+        drain_bar(q_side ? bar_qfull(s % C::kStages) : bar_dofull(s % C::kStages), (s / C::kStages) & 1);
     }
     __syncwarp();
   } else if (warp == C::kMmaWarp) {
