@@ -22,9 +22,11 @@
 //               (at d = 128 the stage's dO_i buffer, free once the dV product
 //               has read it and handed back to the TMA warp afterwards; at
 //               d = 64 a buffer of its own) into TMA reduce-adds onto the fp32 dQ
-//   warp 12     TMA: K_j, V_j once; Q_i (with LSE_i log2 e and D_i) and dO_i
-//               into a ring of stages, loaded and released separately
+//   warp 12     TMA: K_j, V_j once; Q_i (with LSE_i log2 e and D_i) into a
+//               ring of stages
 //   warp 13     MMA issuer (one elected lane)
+//   warp 14     TMA: dO_i into the same stages (loaded and released apart
+//               from Q_i)
 //
 // TMEM: S^T (P^T as bf16 pairs over its first 64 columns) at 0, dP^T (dS^T
 // over its first 64) at 128, dV at 256, dK at 256 + d, and at d = 64 dQ_i at
@@ -92,7 +94,7 @@ struct BwdCfg {
   static constexpr uint32_t kSlack = kSmemBytes - kUsed;
   static_assert(kUsed + 256 <= 232448u, "shared memory");
   static constexpr int kThreads = 512;
-  static constexpr int kDqWarp0 = 8, kTmaWarp = 12, kMmaWarp = 13;
+  static constexpr int kDqWarp0 = 8, kTmaWarp = 12, kMmaWarp = 13, kDoWarp = 14;
   // setmaxnreg: 4 warps x 32 x (2 x 136 + 152 + 88) = 512 threads x 128 at launch
   static constexpr uint32_t kRegsDs = 136;
   static constexpr uint32_t kRegsDq = 152;
@@ -259,14 +261,15 @@ __global__ void __launch_bounds__(512, 1)
   // region by the setmaxnreg that dominates it)
   if (warp >= C::kTmaWarp) {
   regs_to<C::kRegsProducer, C::kLaunchRegs>();
-  if (warp == C::kTmaWarp) {
+  if (warp == C::kTmaWarp || warp == C::kDoWarp) {
     // ------------------------------------------------------------ TMA
+    // Two loaders, so that neither waits behind the other's buffer: warp 12
+    // K_j, V_j (once) and Q_i (with LSE_i log2 e and D_i), warp 14 dO_i.
     const uint32_t leader = elect_one();
     const uint64_t pol_stream = policy_evict_first();  // K_j, V_j: read by this CTA alone
     const uint64_t pol_keep = policy_evict_last();     // Q_i, dO_i: read by every key tile of the head
-    bool ok = true;
-    int it = 0;
-    if (leader) {
+    const bool q_side = warp == C::kTmaWarp;
+    if (q_side && leader) {
       mbar_arrive_expect_tx(bar_kv, 2 * C::kTileBytes);
 #pragma unroll
       for (int b = 0; b < C::kBoxes; ++b) {
@@ -274,52 +277,40 @@ __global__ void __launch_bounds__(512, 1)
         tma_load_3d_hint(sbase + C::kVOff + b * C::kBoxBytes, &tm_v, bar_kv, b * 64, j * 128, bh, pol_stream);
       }
     }
-    // Q_i (and its vectors) one iteration ahead of dO_i: the S^T product needs
-    // Q_{i+1} before the dP^T product needs dO_{i+1}
-    int nq = 0, ndo = 0;  // loads issued
-    auto load_q = [&](int i) {
+    int issued = 0;
+    for (int i = 0; i < n_it; ++i) {
       const int st = i % C::kStages;
       const uint32_t ph = static_cast<uint32_t>(i / C::kStages) & 1u;
-      if (!__all_sync(0xffffffffu, wait_bar(bar_qfree(st), ph ^ 1u, abort_flag, args.status, 30))) return false;
-      if (leader) {
-        const int row = (i0 + i) * 128;
-        const uint32_t dst = sbase + C::kStageOff + st * C::kStageBytes;
-        mbar_arrive_expect_tx(bar_qfull(st), C::kTileBytes + 1024);
+      const uint32_t dst = sbase + C::kStageOff + st * C::kStageBytes;
+      if (q_side) {
+        if (!__all_sync(0xffffffffu, wait_bar(bar_qfree(st), ph ^ 1u, abort_flag, args.status, 30))) break;
+        if (leader) {
+          const int row = (i0 + i) * 128;
+          mbar_arrive_expect_tx(bar_qfull(st), C::kTileBytes + 1024);
 #pragma unroll
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d_hint(dst + b * C::kBoxBytes, &tm_q, bar_qfull(st), b * 64, row, bh, pol_keep);
-        const size_t vrow = static_cast<size_t>(bh) * args.np + row;
-        bulk_g2s(dst + C::kVecOff, args.lse2 + vrow, 512, bar_qfull(st));
-        bulk_g2s(dst + C::kVecOff + 512, args.dvec + vrow, 512, bar_qfull(st));
-      }
-      ++nq;
-      return true;
-    };
-    auto load_do = [&](int i) {
-      const int st = i % C::kStages;
-      const uint32_t ph = static_cast<uint32_t>(i / C::kStages) & 1u;
-      if (!__all_sync(0xffffffffu, wait_bar(bar_dofree(st), ph ^ 1u, abort_flag, args.status, 29))) return false;
-      if (leader) {
-        const uint32_t dst = sbase + C::kStageOff + st * C::kStageBytes + C::kTileBytes;
-        mbar_arrive_expect_tx(bar_dofull(st), C::kTileBytes);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d_hint(dst + b * C::kBoxBytes, &tm_q, bar_qfull(st), b * 64, row, bh, pol_keep);
+          const size_t vrow = static_cast<size_t>(bh) * args.np + row;
+          bulk_g2s(dst + C::kVecOff, args.lse2 + vrow, 512, bar_qfull(st));
+          bulk_g2s(dst + C::kVecOff + 512, args.dvec + vrow, 512, bar_qfull(st));
+        }
+      } else {
+        if (!__all_sync(0xffffffffu, wait_bar(bar_dofree(st), ph ^ 1u, abort_flag, args.status, 29))) break;
+        if (leader) {
+          mbar_arrive_expect_tx(bar_dofull(st), C::kTileBytes);
 #pragma unroll
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d_hint(dst + b * C::kBoxBytes, &tm_do, bar_dofull(st), b * 64, (i0 + i) * 128, bh, pol_keep);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d_hint(dst + C::kTileBytes + b * C::kBoxBytes, &tm_do, bar_dofull(st), b * 64, (i0 + i) * 128,
+                             bh, pol_keep);
+        }
       }
-      ++ndo;
-      return true;
-    };
-    ok = load_q(0);
-    for (; ok && it < n_it; ++it) {
-      if (it + 1 < n_it) ok = load_q(it + 1);
-      if (ok) ok = load_do(it);
+      ++issued;
     }
-    if (!ok) {
-      drain_bar(bar_kv, 0);
-      for (int s = nq - C::kStages < 0 ? 0 : nq - C::kStages; s < nq; ++s)
-        drain_bar(bar_qfull(s % C::kStages), (s / C::kStages) & 1);
-      for (int s = ndo - C::kStages < 0 ? 0 : ndo - C::kStages; s < ndo; ++s)
-        drain_bar(bar_dofull(s % C::kStages), (s / C::kStages) & 1);
+    if (issued < n_it) {
+      // a wait gave up: the copies in flight land before the CTA leaves
+      if (q_side) drain_bar(bar_kv, 0);
+      for (int s = issued - C::kStages < 0 ? 0 : issued - C::kStages; s < issued; ++s)
+        drain_bar(q_side ? bar_qfull(s % C::kStages) : bar_dofull(s % C::kStages), (s / C::kStages) & 1);
     }
     __syncwarp();
   } else if (warp == C::kMmaWarp) {

@@ -499,12 +499,13 @@ __global__ void __launch_bounds__(512, 1)
         mbar_arrive(bar_dpld);
         uint32_t w[16];
         uint32_t sfw = 0;
+        // dS 2^8 = P^T 2^8 (dP^T - D) over two 32 x 32 blocks: 32 queries of
+        // this row each, the blocks' 32 rows being the warp's lanes; both
+        // blocks' maxima are reduced across the warp side by side
+        float amax[2] = {0.f, 0.f};
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           reg_fence32(u[kk]);
-          // dS 2^8 = P^T 2^8 (dP^T - D) over one 32 x 32 block: 32 queries of
-          // this row, the block's 32 rows being the warp's lanes
-          float amax = 0.f;
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
             const float4 d4 = lds_f4(vec + 512u + 4u * (64 * h + 32 * kk + 4 * c4));
@@ -513,14 +514,20 @@ __global__ void __launch_bounds__(512, 1)
             for (int e = 0; e < 4; ++e) {
               const int i = 32 * kk + 4 * c4 + e;
               p8[i] = p8[i] * (__uint_as_float(u[kk][4 * c4 + e]) - dv4[e]);
-              amax = fmaxf(amax, fabsf(p8[i]));
+              amax[kk] = fmaxf(amax[kk], fabsf(p8[i]));
             }
           }
+        }
 #pragma unroll
-          for (int sh = 16; sh > 0; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
+        for (int sh = 16; sh > 0; sh >>= 1) {
+          amax[0] = fmaxf(amax[0], __shfl_xor_sync(0xffffffffu, amax[0], sh));
+          amax[1] = fmaxf(amax[1], __shfl_xor_sync(0xffffffffu, amax[1], sh));
+        }
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
           // the E8M0 byte of dS is that of dS 2^8 minus 8 (clamped at the
           // bottom of the range, where the codes then carry the difference)
-          const uint32_t b8 = e8m0_for_amax(amax);
+          const uint32_t b8 = e8m0_for_amax(amax[kk]);
           const uint32_t b = b8 < 8u ? 0u : b8 - 8u;
           const float inv = e8m0_inverse(b + 8u);
 #pragma unroll
