@@ -46,8 +46,8 @@
 // are dead at the time (the same page, section "TMEM allocation and scale
 // factor placement"):
 //   S^T region  32-35 P^T's (the constant), 36-39 dO_i's (dV); 40-47 K^T's and
-//               dS's (dQ_i), once the P warps have loaded S^T_{i+1}, then V's
-//               and dO_{i+1}'s (dP_{i+1}), once dQ_i is complete
+//               dS's (dQ_i) and 48-55 V's and dO_{i+1}'s (dP_{i+1}), once the
+//               P warps have loaded S^T_{i+1}
 //   dP^T region 32-35 and 96-99 dS^T's (query blocks 0-1 and 2-3), 36-39
 //               Q_i's (dK); 40-47 K's and Q_{i+1}'s (S_{i+1}), once the dS
 //               warps have loaded dP^T_i
@@ -136,6 +136,7 @@ struct BwdMxCfg {
   // operand's at 32 or 40, the B operand's 4 further
   static constexpr uint32_t kSfTs = 32;  // TMEM-A products: P^T / dS^T (queries 0-63), then dO_i / Q_i
   static constexpr uint32_t kSfTsHi = 96;  // dS^T's scales for queries 64-127
+  static constexpr uint32_t kSfDp = 48;    // dP_{i+1} (S^T region)
   static constexpr uint32_t kSfSs = 40;  // shared-memory products: dQ_i and dP_{i+1} (S^T region), S_{i+1} (dP^T region)
   // the constant E8M0 byte of P^T: 2^-8 (P = 1 is held as 256)
   static constexpr uint32_t kPScaleByte = 119u;
@@ -319,6 +320,17 @@ __global__ void __launch_bounds__(512, 1)
                          idesc_mxf8(128, 128, b_mn, kk, kk), kk > 0 ? 1u : 0u, tmem + sf, tmem + sf + 4);
       }
     };
+    // the same product with the scales already in TMEM columns sf, sf + 4
+    auto issue_ss_nocp = [&](uint32_t a_lo, uint32_t b_lo, uint32_t d_col, uint32_t sf) {
+      a_lo = opaque(a_lo);
+      b_lo = opaque(b_lo);
+      if (leader) {
+#pragma unroll
+        for (uint32_t kk = 0; kk < 4; ++kk)
+          mma_mxf8_ss_lo(tmem + d_col, a_lo + 2 * kk, b_lo + 2 * kk, desc_hi, idesc_mxf8(128, 128, false, kk, kk),
+                         kk > 0 ? 1u : 0u, tmem + sf, tmem + sf + 4);
+      }
+    };
     // D += A B with A (E4M3) in TMEM region a_reg -- k-steps 0, 1 (queries
     // 0-63) at columns 0-15, k-steps 2, 3 at 64-79 -- its scales at a_reg + 32
     // (P^T: one constant column; dS^T: bytes of query blocks 0, 1 there and of
@@ -394,13 +406,19 @@ __global__ void __launch_bounds__(512, 1)
       commit(bar_dq);
       commit(bar_dsfree);
       if (more) {
-        // dP^T_{i+1} overwrites dQ_i^T once the dQ warps have loaded it; its
-        // scales take dQ_i's columns, free once dQ_i is complete
-        ok = wait(bar_dqread, par, 62) && wait(bar_dofull(st1), par1, 63);
+        // dP^T_{i+1}'s scales go into S^T columns 48-55 as soon as dO_{i+1}
+        // has landed (the P warps have loaded S^T_{i+1}); the product itself
+        // overwrites dQ_i^T once the dQ warps have loaded it
+        ok = wait(bar_dofull(st1), par1, 63);
+        if (!ok) break;
+        if (leader) {
+          sf_copy_to_tmem(tmem + C::kColS + C::kSfDp, atom_v);
+          sf_copy_to_tmem(tmem + C::kColS + C::kSfDp + 4, stage_addr(st1) + C::kDoAtomOff);
+        }
+        ok = wait(bar_dqread, par, 62);
         if (!ok) break;
         tc_fence_after();
-        issue_ss(v_km, st_km + st1 * kStageStep + kTileStep, C::kColDp, C::kColS + C::kSfSs, atom_v,
-                 stage_addr(st1) + C::kDoAtomOff, false);
+        issue_ss_nocp(v_km, st_km + st1 * kStageStep + kTileStep, C::kColDp, C::kColS + C::kSfDp);
         commit(bar_dp);
       }
     }
