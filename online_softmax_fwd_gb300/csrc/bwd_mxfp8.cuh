@@ -38,7 +38,8 @@
 //   warp 14     TMA: dO_i (+ its two atoms) into the same stages
 //
 // TMEM (512 columns): S^T 0-127, dP^T 128-255, dV 256-383, dK 384-511; dQ_i^T
-// takes the dP^T columns once the dK product has read dS^T, and the next dP^T
+// takes the dP^T columns, issued right behind the dK product that reads dS^T
+// from them (one thread's products run in issue order), and the next dP^T
 // waits until the dQ warps have loaded dQ_i^T. P^T and dS^T as E4M3 (four
 // queries per column) take columns 0-15 (queries 0-63, warp h = 0) and 64-79
 // (queries 64-127, h = 1) of their region, among the columns each warp loaded
@@ -391,13 +392,15 @@ __global__ void __launch_bounds__(512, 1)
       // dK += dS^T Q_i (B = Q_i MN-major, its atom whose rows are d columns)
       issue_ts(C::kColDp, st_mn + st * kStageStep, C::kColDk, stage_addr(st) + C::kQAtomOff + C::kAtomBytes,
                it == 0, true);
-      commit(bar_kdone);
       commit(bar_qfree(st));  // Q_i: read by S^T_i and this product
-      // dQ_i^T = K^T dS^T overwrites dS^T_i (and S^T_{i+1}'s scales) once the
-      // dK product (and with it S^T_{i+1}) is complete; its scales go into the
-      // S^T region once the P warps have loaded S^T_{i+1}; K^T is written once
-      ok = wait(bar_kdone, par, 60) && (!more || wait(bar_sld, static_cast<uint32_t>(it + 1) & 1u, 61)) &&
-           (it > 0 || wait(bar_ktr, 0, 70));
+      // dQ_i^T = K^T dS^T over the dP^T columns, issued right behind dK: the
+      // tensor core runs one thread's products in issue order, so dK has read
+      // dS^T before dQ_i writes over it (as the O product reads P before the
+      // next S product overwrites it in the forward kernel). Its scales go
+      // into the S^T region once the P warps have loaded S^T_{i+1} (which also
+      // means S^T_{i+1}, whose scales sit in the dP^T columns, is complete);
+      // K^T is written once.
+      ok = (!more || wait(bar_sld, static_cast<uint32_t>(it + 1) & 1u, 61)) && (it > 0 || wait(bar_ktr, 0, 70));
       if (!ok) break;
       tc_fence_after();
       // A = K^T (rows d, its atom whose rows are d columns), B = dS (rows
