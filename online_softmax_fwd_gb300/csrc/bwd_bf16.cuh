@@ -28,10 +28,12 @@
 //   warp 14     TMA: dO_i into the same stages (loaded and released apart
 //               from Q_i)
 //
-// TMEM: S^T (P^T as bf16 pairs over its first 64 columns) at 0, dP^T (dS^T
-// over its first 64) at 128, dV at 256, dK at 256 + d, and at d = 64 dQ_i at
-// 384. At d = 128 dQ_i reuses the dP^T columns once the dK product has read
-// dS^T, and the next dP^T waits until the dQ warps have loaded dQ_i. dS also
+// TMEM: S^T at 0 (P^T as bf16 pairs over columns 0-31 and 64-95, each half
+// over columns its own warp loaded), dP^T at 128 (dS^T likewise), dV at 256,
+// dK at 256 + d, and at d = 64 dQ_i at 384. At d = 128 dQ_i reuses the dP^T
+// columns, issued right behind the dK product that reads dS^T from them (one
+// thread's products run in issue order), and the next dP^T waits until the
+// dQ warps have loaded dQ_i. dS also
 // goes to shared memory, keys x queries with queries contiguous, as the
 // MN-major A operand of the dQ product.
 #pragma once
@@ -357,14 +359,15 @@ __global__ void __launch_bounds__(512, 1)
           mma_ss_lo(tmem + col, a_lo + kmajor_step(kk), b_lo + kmajor_step(kk), desc_hi, kIdSq, kk > 0 ? 1u : 0u);
       }
     };
-    // dV += P^T dO_i, dK += dS^T Q_i (contraction over the 128 queries)
+    // dV += P^T dO_i, dK += dS^T Q_i (contraction over the 128 queries; A's
+    // queries 0-63 at columns 0-31 of its region, 64-127 at 64-95)
     auto issue_acc = [&](uint32_t a_col, uint32_t b_lo, uint32_t d_col, bool first) {
       a_col = opaque(a_col);
       b_lo = opaque(b_lo);
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts_lo(tmem + d_col, tmem + a_col + kk * 8, b_lo + kk * 128, desc_hi, kIdAcc,
+          mma_ts_lo(tmem + d_col, tmem + a_col + (kk < 4 ? 8 * kk : 64 + 8 * (kk - 4)), b_lo + kk * 128, desc_hi, kIdAcc,
                     (!first || kk > 0) ? 1u : 0u);
       }
     };
@@ -414,13 +417,10 @@ __global__ void __launch_bounds__(512, 1)
       if (!ok) break;
       tc_fence_after();
       issue_acc(C::kColDp, st_mn + st * kStageStep, C::kColDk, it == 0);  // B = Q_i
-      commit(bar_kdone);
       commit(bar_qfree(st));
       if constexpr (C::kDqAlias) {
-        // dQ_i overwrites dS^T(i) once the dK product has read it
-        ok = wait(bar_kdone, par, 37);
-        if (!ok) break;
-        tc_fence_after();
+        // dQ_i over dS^T(i), right behind the dK product that reads it: one
+        // thread's products run in issue order
         issue_dq();
         commit(bar_dq);
         commit(bar_dsfree);
@@ -444,9 +444,9 @@ __global__ void __launch_bounds__(512, 1)
         commit(bar_dq);
         commit(bar_dsfree);
         if (more) {
-          // dP^T(i+1) overwrites dS^T(i) once the dK product has read it
-          ok = wait(bar_kdone, par, 37) &&
-               wait(bar_dofull(st1), static_cast<uint32_t>((it + 1) / C::kStages) & 1u, 46);
+          // dP^T(i+1) over dS^T(i), behind the dK product that reads it (issue
+          // order)
+          ok = wait(bar_dofull(st1), static_cast<uint32_t>((it + 1) / C::kStages) & 1u, 46);
           if (!ok) break;
           tc_fence_after();
           issue_sq(v_km, st_km + st1 * kStageStep + kTileStep, C::kColDp);
@@ -463,10 +463,8 @@ __global__ void __launch_bounds__(512, 1)
   } else if (warp < C::kDqWarp0) {
     // ------------------------------------------------------------ P^T, dS^T (thread = key row)
     // Warps w and w + 4 share key rows 32 (w % 4) .. and take queries
-    // 64 h .. 64 h + 63 (h = w / 4). P^T and dS^T are stored as bf16 pairs
-    // over the first half of the fp32 columns they come from, which the other
-    // warp of the pair may still have to read: the pair loads its columns,
-    // meets at a barrier, then stores.
+    // 64 h .. 64 h + 63 (h = w / 4). Each stores its half of P^T and dS^T as
+    // bf16 pairs over the first 32 of the 64 fp32 columns it loaded itself.
     regs_to<C::kRegsDs, C::kLaunchRegs>();
     const int quad = warp & 3, h = warp >> 2;
     const int r = quad * 32 + lane;
@@ -487,9 +485,9 @@ __global__ void __launch_bounds__(512, 1)
       int lim = args.n - 1 - q0;  // last valid query column
       // S^T(i) is complete, and the stage's vectors have landed (the stage is
       // refilled only after this warpgroup's dS^T(i) has been consumed)
-      ok = pair_all(quad, wait_bar(bar_s, par, abort_flag, args.status, 40) &&
-                              wait_bar(bar_qfull(it % C::kStages), static_cast<uint32_t>(it / C::kStages) & 1u,
-                                       abort_flag, args.status, 45));
+      ok = __all_sync(0xffffffffu, wait_bar(bar_s, par, abort_flag, args.status, 40) &&
+                                       wait_bar(bar_qfull(it % C::kStages), static_cast<uint32_t>(it / C::kStages) & 1u,
+                                                abort_flag, args.status, 45));
       if (!ok) break;
       tc_fence_after();
       uint32_t pk[32];  // this warp's 64 queries of the P^T row, as bf16 pairs
@@ -498,7 +496,6 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) tmem_ld32(s_tm + 32 * (2 * h + kk), u[kk]);
         tmem_ld_wait();
-        pair_sync(quad);
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           const int k = 2 * h + kk;
@@ -520,7 +517,7 @@ __global__ void __launch_bounds__(512, 1)
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) w[e] = pk[16 * kk + e];
-          tmem_st16(s_tm + 16 * k, w);
+          tmem_st16(s_tm + 64 * h + 16 * kk, w);
         }
       }
       tmem_st_wait();
@@ -531,7 +528,7 @@ __global__ void __launch_bounds__(512, 1)
       {
         bool w_ok = wait_bar(bar_dp, par, abort_flag, args.status, 41);
         if (w_ok && it > 0) w_ok = wait_bar(bar_dsfree, par ^ 1u, abort_flag, args.status, 42);
-        ok = pair_all(quad, w_ok);
+        ok = __all_sync(0xffffffffu, w_ok);
       }
       if (!ok) break;
       tc_fence_after();
@@ -540,7 +537,6 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) tmem_ld32(dp_tm + 32 * (2 * h + kk), u[kk]);
         tmem_ld_wait();
-        pair_sync(quad);
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           const int k = 2 * h + kk;
@@ -557,7 +553,7 @@ __global__ void __launch_bounds__(512, 1)
             w[2 * c4] = pack_bf16x2(ds0, ds1);
             w[2 * c4 + 1] = pack_bf16x2(ds2, ds3);
           }
-          tmem_st16(dp_tm + 16 * k, w);
+          tmem_st16(dp_tm + 64 * h + 16 * kk, w);
           // shared memory: key row r, queries 32k .. 32k+31 = 16-byte chunks
           // 4(k%2) .. 4(k%2)+3 of box k/2, 128-byte swizzled
 #pragma unroll
