@@ -50,10 +50,11 @@ KERNEL_SOURCES = {
               "online_softmax_fwd_gb300/csrc/fwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/ptx.cuh",
               "online_softmax_fwd_gb300/csrc/exp2_fma.cuh", "online_softmax_fwd_gb300/csrc/schedule.h",
               "online_softmax_fwd_gb300/csrc/schedule.cu"],
-    "bwd": ["online_softmax_fwd_gb300/csrc/bwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/bwd_aux.cu",
+    "bwd": ["online_softmax_fwd_gb300/csrc/bwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/bwd_common.cuh",
+            "online_softmax_fwd_gb300/csrc/bwd_aux.cu",
             "online_softmax_fwd_gb300/csrc/fwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/ptx.cuh",
             "online_softmax_fwd_gb300/csrc/exp2_fma.cuh", "online_softmax_fwd_gb300/csrc/schedule.h"],
-    "bwd_mxfp8": ["online_softmax_fwd_gb300/csrc/bwd_mxfp8.cuh", "online_softmax_fwd_gb300/csrc/bwd_bf16.cuh",
+    "bwd_mxfp8": ["online_softmax_fwd_gb300/csrc/bwd_mxfp8.cuh", "online_softmax_fwd_gb300/csrc/bwd_common.cuh",
                   "online_softmax_fwd_gb300/csrc/bwd_aux.cu", "online_softmax_fwd_gb300/csrc/mxfp8_common.cuh",
                   "online_softmax_fwd_gb300/csrc/quant_mxfp8.cu", "online_softmax_fwd_gb300/csrc/fwd_bf16.cuh",
                   "online_softmax_fwd_gb300/csrc/ptx.cuh"],

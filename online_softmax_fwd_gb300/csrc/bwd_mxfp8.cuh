@@ -62,7 +62,8 @@
 
 #include <cstdint>
 
-#include "bwd_bf16.cuh"
+#include "bwd_common.cuh"
+#include "fwd_bf16.cuh"
 #include "mxfp8_common.cuh"
 #include "ptx.cuh"
 
