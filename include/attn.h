@@ -45,7 +45,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1, /* null pointer, negative size, non-finite or non-positive scale, ... */
-  ATTN_ERR_UNSUPPORTED = 2, /* a well-formed request this build does not implement (e.g. d = 96) */
+  ATTN_ERR_UNSUPPORTED = 2, /* a well-formed request the library does not implement (e.g. d = 96) */
   ATTN_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
   ATTN_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed (launch, tensor map, ...) */
   ATTN_ERR_TIMEOUT = 5      /* a kernel gave up waiting on a pipeline barrier (see attn_get_device_status) */
