@@ -81,3 +81,15 @@ def test_reference_arm_json_line_backward():
     assert line["config"]["pass"] == "bwd" and line["config"]["causal"] is True
     assert line["cpu_baseline"]["kind"] == "oracle" and "backward" in line["cpu_baseline"]["sample"]
 
+
+
+def test_reference_arm_json_line_mxfp8_backward():
+    # the MXFP8 backward's reference arm times the float64 MXFP8 backward oracle on one head
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--shape",
+                        "1,1,256,128,0,1,1", "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"].startswith("attention bwd") and line["value"] > 0
+    assert line["config"]["pass"] == "bwd" and line["config"]["dtype"] == "mxfp8"
+    assert line["cpu_baseline"]["kind"] == "oracle" and "MXFP8 backward" in line["cpu_baseline"]["sample"]
