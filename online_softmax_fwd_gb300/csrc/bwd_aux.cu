@@ -3,9 +3,10 @@
 //             every query row (rows N .. np-1 of a head get 0), and the fp32
 //             dQ accumulator zeroed;
 //   bwd_prep_mxfp8: the same with dO from its E4M3 codes times its blocks'
-//             E8M0 scales, and LSE_i log2(e) - 8 (the MXFP8 kernel's exp then
-//             gives P 2^8, the constant scale of P in E4M3); its accumulator
-//             is transposed, [B*H, d, np];
+//             E8M0 scales, stored as -D_i and 8 - LSE_i log2(e) (the MXFP8
+//             kernel adds them in pairs; its exp then gives P 2^8, the
+//             constant scale of P in E4M3); its accumulator is transposed,
+//             [B*H, d, np];
 //   bwd_post: dQ = s * accumulator, rounded to bf16 (bwd_post_t: from the
 //             transposed accumulator).
 // All are bandwidth-bound elementwise passes.
@@ -115,8 +116,8 @@ __global__ void __launch_bounds__(256) bwd_prep_mxfp8_kernel(const __nv_bfloat16
 #pragma unroll
   for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
   if (lane == 0) {
-    dvec[prow] = acc;
-    lse2[prow] = lse[grow] * 1.4426950408889634f - 8.0f;
+    dvec[prow] = -acc;
+    lse2[prow] = 8.0f - lse[grow] * 1.4426950408889634f;
   }
 }
 

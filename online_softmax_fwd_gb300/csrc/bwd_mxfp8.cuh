@@ -32,8 +32,8 @@
 //               the dQ buffer (warp 8 + b: d rows 32 b .. 32 b + 31, four
 //               boxes of 32 queries) and TMA reduce-adds onto the transposed
 //               fp32 dQ
-//   warp 12     TMA: K_j, V_j and their atoms once; Q_i (+ LSE_i log2 e - 8,
-//               D_i and Q's two atoms) into a ring of stages
+//   warp 12     TMA: K_j, V_j and their atoms once; Q_i (+ 8 - LSE_i log2 e,
+//               -D_i and Q's two atoms) into a ring of stages
 //   warp 13     MMA issuer (one elected lane); tcgen05.cp of every atom
 //   warp 14     TMA: dO_i (+ its two atoms) into the same stages
 //
@@ -77,8 +77,8 @@ struct BwdMxArgs {
   const uint8_t* v_sf;    // V atoms, rows = key (dP product)
   const uint8_t* do_sf;   // dO atoms, rows = query (dP product)
   const uint8_t* do_sf_t; // dO atoms, rows = d column (dV product)
-  const float* lse2;      // LSE * log2(e), [B*H, np] (0 past N)
-  const float* dvec;      // D = rowsum(dO * O), [B*H, np] (0 past N)
+  const float* lse2;      // 8 - LSE * log2(e), [B*H, np] (0 past N)
+  const float* dvec;      // -D = -rowsum(dO * O), [B*H, np] (0 past N)
   __nv_bfloat16* dk;      // [B*H, N, 128]
   __nv_bfloat16* dv;      // [B*H, N, 128]
   unsigned int* status;
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_tm = tmem + lane_off + C::kColS;
     const uint32_t dp_tm = tmem + lane_off + C::kColDp;
-    const float sl2 = args.scale_log2;
+    const float2 sl2_2 = make_float2(args.scale_log2, args.scale_log2);
     // this thread's row of dS (keys x queries, 128-byte swizzled rows)
     const uint32_t ds_row = sbase + C::kDsOff + r * 128;
     // dQ's B atom: row = query m, block = key block (this warp's quad); every
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(512, 1)
       const uint32_t par = static_cast<uint32_t>(it) & 1u;
       const int st = it % C::kStages;
       const int q0 = (i0 + it) * 128;
-      // this query tile's LSE log2 e - 8 and D, in its stage
+      // this query tile's 8 - LSE log2 e and -D, in its stage
       const uint32_t vec = sbase + C::kStageOff + st * C::kStageBytes + C::kVecOff;
       const bool need_mask = (q0 + 128 > args.n) || (CAUSAL && it == 0) || (j * 128 + 128 > args.n);
       const int lim = key_valid ? args.n - 1 - q0 : -1;  // last valid query column of this row
@@ -466,7 +466,7 @@ __global__ void __launch_bounds__(512, 1)
                                                 abort_flag, args.status, 65));
       if (!ok) break;
       tc_fence_after();
-      // P^T 2^8 = exp2(S^T s log2 e - (LSE log2 e - 8)) for this warp's 64 queries
+      // P^T 2^8 = exp2(S^T s log2 e + (8 - LSE log2 e)) for this warp's 64 queries
       float p8[64];
       {
         uint32_t u[2][32];
@@ -481,11 +481,15 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
             const float4 l4 = lds_f4(vec + 4u * (64 * h + 32 * kk + 4 * c4));
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(u[kk][4 * c4]), __uint_as_float(u[kk][4 * c4 + 1])),
+                                          sl2_2, make_float2(l4.x, l4.y));
+            const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(u[kk][4 * c4 + 2]), __uint_as_float(u[kk][4 * c4 + 3])),
+                                          sl2_2, make_float2(l4.z, l4.w));
+            const float xs[4] = {x01.x, x01.y, x23.x, x23.y};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int c = 64 * h + 32 * kk + 4 * c4 + e;
-              float p = ex2_mufu(__fmaf_rn(__uint_as_float(u[kk][4 * c4 + e]), sl2, -lv[e]));
+              float p = ex2_mufu(xs[e]);
               if (need_mask && (c > lim || (CAUSAL && kj > q0 + c))) p = 0.f;
               p8[32 * kk + 4 * c4 + e] = p;
             }
@@ -530,14 +534,22 @@ __global__ void __launch_bounds__(512, 1)
           reg_fence32(u[kk]);
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 d4 = lds_f4(vec + 512u + 4u * (64 * h + 32 * kk + 4 * c4));
-            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int i = 32 * kk + 4 * c4 + e;
-              p8[i] = p8[i] * (__uint_as_float(u[kk][4 * c4 + e]) - dv4[e]);
-              amax[kk] = fmaxf(amax[kk], fabsf(p8[i]));
-            }
+            const float4 d4 = lds_f4(vec + 512u + 4u * (64 * h + 32 * kk + 4 * c4));  // -D
+            const int i = 32 * kk + 4 * c4;
+            const float2 t01 = __fmul2_rn(make_float2(p8[i], p8[i + 1]),
+                                          __fadd2_rn(make_float2(__uint_as_float(u[kk][4 * c4]),
+                                                                 __uint_as_float(u[kk][4 * c4 + 1])),
+                                                     make_float2(d4.x, d4.y)));
+            const float2 t23 = __fmul2_rn(make_float2(p8[i + 2], p8[i + 3]),
+                                          __fadd2_rn(make_float2(__uint_as_float(u[kk][4 * c4 + 2]),
+                                                                 __uint_as_float(u[kk][4 * c4 + 3])),
+                                                     make_float2(d4.z, d4.w)));
+            p8[i] = t01.x;
+            p8[i + 1] = t01.y;
+            p8[i + 2] = t23.x;
+            p8[i + 3] = t23.y;
+            amax[kk] = fmax3(amax[kk], fabsf(t01.x), fabsf(t01.y));
+            amax[kk] = fmax3(amax[kk], fabsf(t23.x), fabsf(t23.y));
           }
         }
 #pragma unroll
@@ -552,10 +564,13 @@ __global__ void __launch_bounds__(512, 1)
           const uint32_t b8 = e8m0_for_amax(amax[kk]);
           const uint32_t b = b8 < 8u ? 0u : b8 - 8u;
           const float inv = e8m0_inverse(b + 8u);
+          const float2 inv_2 = make_float2(inv, inv);
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int i = 32 * kk + 4 * e;
-            w[8 * kk + e] = pack_e4m3x4(p8[i] * inv, p8[i + 1] * inv, p8[i + 2] * inv, p8[i + 3] * inv);
+            const float2 a = __fmul2_rn(make_float2(p8[i], p8[i + 1]), inv_2);
+            const float2 c = __fmul2_rn(make_float2(p8[i + 2], p8[i + 3]), inv_2);
+            w[8 * kk + e] = pack_e4m3x4(a.x, a.y, c.x, c.y);
           }
           const uint32_t qb = static_cast<uint32_t>(2 * h + kk);
           sfw |= b << (8 * kk);
