@@ -1,7 +1,8 @@
 // The backward pass's small kernels around its main kernels:
 //   bwd_prep: D_i = sum_c dO_ic O_ic (fp32 from bf16) and LSE_i log2(e) for
-//             every query row (rows N .. np-1 of a head get 0), and the fp32
-//             dQ accumulator zeroed;
+//             every query row, stored negated (the kernel adds them in pairs;
+//             rows N .. np-1 of a head get 0), and the fp32 dQ accumulator
+//             zeroed;
 //   bwd_prep_mxfp8: the same with dO from its E4M3 codes times its blocks'
 //             E8M0 scales, stored as -D_i and 8 - LSE_i log2(e) (the MXFP8
 //             kernel adds them in pairs; its exp then gives P 2^8, the
@@ -61,8 +62,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 #pragma unroll
   for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
   if (lane == 0) {
-    dvec[prow] = acc;
-    lse2[prow] = lse[grow] * 1.4426950408889634f;
+    dvec[prow] = -acc;
+    lse2[prow] = -lse[grow] * 1.4426950408889634f;
   }
   float4* z = reinterpret_cast<float4*>(dq_acc + grow * D);
 #pragma unroll

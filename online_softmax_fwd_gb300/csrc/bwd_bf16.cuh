@@ -50,8 +50,8 @@
 namespace attn {
 
 struct BwdArgs {
-  const float* lse2;     // LSE * log2(e), [B*H, np] (0 past N)
-  const float* dvec;     // D = rowsum(dO * O), [B*H, np] (0 past N)
+  const float* lse2;     // -LSE * log2(e), [B*H, np] (0 past N)
+  const float* dvec;     // -D = -rowsum(dO * O), [B*H, np] (0 past N)
   float* dq_acc;         // fp32 [B*H, N, d], zeroed before the kernel; receives dS K (unscaled) through tm_dq
   __nv_bfloat16* dk;     // [B*H, N, d]
   __nv_bfloat16* dv;     // [B*H, N, d]
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_tm = tmem + lane_off + C::kColS;
     const uint32_t dp_tm = tmem + lane_off + C::kColDp;
-    const float sl2 = args.scale_log2;
+    const float2 sl2_2 = make_float2(args.scale_log2, args.scale_log2);
     const uint32_t ds_row = sbase + C::kDsOff + r * 128;
     bool ok = true;
     for (int it = 0; ok && it < n_it; ++it) {
@@ -473,13 +473,17 @@ __global__ void __launch_bounds__(512, 1)
           reg_fence32(u[kk]);
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 l4 = lds_f4(vec + 4u * (32 * k + 4 * c4));
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float4 l4 = lds_f4(vec + 4u * (32 * k + 4 * c4));  // -LSE log2 e
+            const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(u[kk][4 * c4]), __uint_as_float(u[kk][4 * c4 + 1])),
+                                          sl2_2, make_float2(l4.x, l4.y));
+            const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(u[kk][4 * c4 + 2]), __uint_as_float(u[kk][4 * c4 + 3])),
+                                          sl2_2, make_float2(l4.z, l4.w));
+            const float xs[4] = {x01.x, x01.y, x23.x, x23.y};
             float p[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int c = 32 * k + 4 * c4 + e;
-              p[e] = ex2_mufu(__fmaf_rn(__uint_as_float(u[kk][4 * c4 + e]), sl2, -lv[e]));
+              p[e] = ex2_mufu(xs[e]);
               if (need_mask && (c > lim || (CAUSAL && kj > q0 + c))) p[e] = 0.f;
             }
             pk[16 * kk + 2 * c4] = pack_bf16x2(p[0], p[1]);
@@ -515,14 +519,18 @@ __global__ void __launch_bounds__(512, 1)
           uint32_t w[16];
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 d4 = lds_f4(vec + 512u + 4u * (32 * k + 4 * c4));
+            const float4 d4 = lds_f4(vec + 512u + 4u * (32 * k + 4 * c4));  // -D
             const uint32_t a = pk[16 * kk + 2 * c4], b = pk[16 * kk + 2 * c4 + 1];
-            const float ds0 = bf16_lo(a) * (__uint_as_float(u[kk][4 * c4]) - d4.x);
-            const float ds1 = bf16_hi(a) * (__uint_as_float(u[kk][4 * c4 + 1]) - d4.y);
-            const float ds2 = bf16_lo(b) * (__uint_as_float(u[kk][4 * c4 + 2]) - d4.z);
-            const float ds3 = bf16_hi(b) * (__uint_as_float(u[kk][4 * c4 + 3]) - d4.w);
-            w[2 * c4] = pack_bf16x2(ds0, ds1);
-            w[2 * c4 + 1] = pack_bf16x2(ds2, ds3);
+            const float2 ds01 = __fmul2_rn(make_float2(bf16_lo(a), bf16_hi(a)),
+                                           __fadd2_rn(make_float2(__uint_as_float(u[kk][4 * c4]),
+                                                                  __uint_as_float(u[kk][4 * c4 + 1])),
+                                                      make_float2(d4.x, d4.y)));
+            const float2 ds23 = __fmul2_rn(make_float2(bf16_lo(b), bf16_hi(b)),
+                                           __fadd2_rn(make_float2(__uint_as_float(u[kk][4 * c4 + 2]),
+                                                                  __uint_as_float(u[kk][4 * c4 + 3])),
+                                                      make_float2(d4.z, d4.w)));
+            w[2 * c4] = pack_bf16x2(ds01.x, ds01.y);
+            w[2 * c4 + 1] = pack_bf16x2(ds23.x, ds23.y);
           }
           tmem_st16(dp_tm + 64 * h + 16 * kk, w);
           // shared memory: key row r, queries 32k .. 32k+31 = 16-byte chunks
