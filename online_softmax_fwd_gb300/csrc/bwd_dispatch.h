@@ -18,7 +18,7 @@ cudaError_t launch_bwd_bf16_d64(int causal, const CUtensorMap& q, const CUtensor
 cudaError_t launch_bwd_bf16_d128(int causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                  const CUtensorMap& dout, const CUtensorMap& dq, const BwdArgs& a, cudaStream_t s);
 // MXFP8 (d = 128): D from dO's E4M3 codes and its atoms whose rows are queries,
-// and LSE log2 e - 8 (P comes out of the exp already scaled by 2^8)
+// stored as -D and 8 - LSE log2 e (P comes out of the exp already scaled by 2^8)
 cudaError_t launch_bwd_prep_mxfp8(const void* o, const void* do8, const void* do_sf, const float* lse, float* lse2,
                                   float* dvec, float* dq_acc, long long bh, int n, int np, cudaStream_t stream);
 // dQ from the transposed accumulator [B*H, 128, np] (MXFP8)
