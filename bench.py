@@ -83,6 +83,37 @@ def measured_peaks() -> dict:
         return {}
 
 
+def oracle_threads() -> tuple[int, str]:
+    """Threads the float64 oracle really runs on: NumPy's BLAS pool (the
+    oracle's work is NumPy matrix products), not PyTorch's intra-op pool."""
+    try:
+        import threadpoolctl
+        for info in threadpoolctl.threadpool_info():
+            if info.get("user_api") == "blas":
+                return int(info["num_threads"]), f"threadpoolctl ({info.get('internal_api')})"
+    except Exception:
+        pass
+    try:
+        libs = set()
+        with open("/proc/self/maps") as f:
+            for line in f:
+                path = line.split()[-1]
+                base = os.path.basename(path).lower()
+                if "blas" in base and ".so" in base:
+                    libs.add(path)
+        for path in sorted(libs):
+            lib = ctypes.CDLL(path)
+            for name in ("scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads",
+                         "openblas_get_num_threads64_", "openblas_get_num_threads"):
+                fn = getattr(lib, name, None)
+                if fn is not None:
+                    fn.restype = ctypes.c_int
+                    return int(fn()), f"{name} ({os.path.basename(path)})"
+    except Exception:
+        pass
+    return os.cpu_count() or 1, "os.cpu_count (BLAS pool not found)"
+
+
 def profiled_traffic(workload: str) -> float | None:
     """DRAM bytes per launch from the committed ncu summary of this workload,
     if it was taken on the current kernel sources (else None)."""
@@ -324,14 +355,15 @@ def bench_reference_bwd(args, w: I.Workload) -> None:
         one_step()
     secs = [one_step() for _ in range(args.steps)]
     value = head_flop / float(np.mean(secs)) / 1e12
-    cores = torch.get_num_threads()
+    cores, cores_src = oracle_threads()
     sample = (f"float64 {'MXFP8 ' if w.dtype == 'mxfp8' else ''}backward oracle on one whole head "
               f"(N = {w.N}, d = {w.d}) of the workload per step")
     out = {"impl": "reference", "metric": METRIC_BWD, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(secs)), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {**w.describe(), "workload": w.name},
-           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "cores_source": cores_src, "kind": "oracle",
+                            "sample": sample},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
@@ -344,7 +376,7 @@ def bench_reference(args, w: I.Workload, world: int, rank: int) -> None:
         return
     q, k, v = I.bf16_qkv(w) if w.dtype == "bf16" else tuple(torch.from_numpy(x) for x in I.draw_fp32(
         w.B, w.H, w.N, w.d, w.qk_std, w.v_std, w.seed))
-    cores = torch.get_num_threads()
+    cores, cores_src = oracle_threads()
     per_step = max(1.0, args.reference_seconds / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_sample(w, q, k, v, per_step)
@@ -360,7 +392,8 @@ def bench_reference(args, w: I.Workload, world: int, rank: int) -> None:
            "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(secs)), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {**w.describe(), "workload": w.name},
-           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "cores_source": cores_src, "kind": "oracle",
+                            "sample": sample},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
@@ -620,22 +653,28 @@ class BwdMxfp8Step:
                 "d2h_bytes_per_step": sum(h.numel() * 2 for h in outs), "steps": n_steps}
 
 
-def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
-    import online_softmax_fwd_gb300 as attn
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    attn.lib()
+def step_class(w: I.Workload):
     if w.direction == "bwd":
-        step_cls = BwdMxfp8Step if w.dtype == "mxfp8" else BwdStep
-    else:
-        step_cls = Mxfp8Step if w.dtype == "mxfp8" else Bf16Step
-    step = step_cls(attn, w, dev, args)
+        return BwdMxfp8Step if w.dtype == "mxfp8" else BwdStep
+    return Mxfp8Step if w.dtype == "mxfp8" else Bf16Step
+
+
+def measure(step, dev, world: int, steps: int, warmup: int, flush=None) -> dict:
+    """Warm up, then time `steps` steps on the current stream: CUDA events
+    around the whole region and around each step's timed kernel call, clocks
+    sampled during the region, barrier + device synchronisation on both sides
+    and the slowest rank's region time. ``flush`` (optional) runs between
+    steps, inside the region, to evict L2 when the inputs fit in it; the
+    per-launch events then still time the kernel alone."""
+    import online_softmax_fwd_gb300 as attn
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step.run(sh)
+        if flush:
+            flush()
     torch.cuda.synchronize(dev)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     sampler = ClockSampler(dev)
     barrier(world)
     sampler.start()
@@ -644,7 +683,9 @@ def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
     region0 = torch.cuda.Event(enable_timing=True)
     region1 = torch.cuda.Event(enable_timing=True)
     region0.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
+        if flush:
+            flush()
         step.run(sh, evs[i])
     region1.record(stream)
     torch.cuda.synchronize(dev)
@@ -655,57 +696,156 @@ def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
     if st != attn.Status.OK:
         raise RuntimeError(f"device status after the timed region: {st!r}")
     region_ms = region0.elapsed_time(region1)
-    launch_ms = [a.elapsed_time(b) for a, b in evs]
-    region_ms_max = max_over_ranks(region_ms, world, dev)
-    value = w.flops * args.steps * world / (region_ms_max * 1e-3) / 1e12
+    return {"region_ms": max_over_ranks(region_ms, world, dev), "launch_ms": [a.elapsed_time(b) for a, b in evs],
+            "clocks": sampler.summary(t_wall0, t_wall1)}
 
-    e2e = None if args.no_e2e else step.e2e(dev, max(3, min(args.steps, 10)), world)
 
+def peak_for(w: I.Workload) -> tuple[float, str]:
     peaks = measured_peaks()
     bf16_peak = peaks.get("bf16_tflops")
     src = "measured bf16_tflops (burst, cuBLAS)" if bf16_peak else "fallback 1900 bf16"
     if not bf16_peak:
         bf16_peak = 1900.0
     if w.dtype == "mxfp8":
-        peak = 2.0 * bf16_peak   # FP8 dense = 2 x bf16 dense (4.5 / 2.25 PFLOP/s nominal)
-        src += " x 2 (nominal FP8/bf16 ratio)"
-    else:
-        peak = bf16_peak
-    avg_launch_s = float(np.mean(launch_ms)) * 1e-3
-    achieved = w.flops / avg_launch_s / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": profiled_traffic(w.name), "peak_source": src, "flop_per_launch": w.flops,
-                "kernel": KERNEL_NAMES[(w.direction, w.dtype)]}
+        # FP8 dense = 2 x bf16 dense (4.5 / 2.25 PFLOP/s nominal)
+        return 2.0 * bf16_peak, src + " x 2 (nominal FP8/bf16 ratio)"
+    return bf16_peak, src
+
+
+def roofline_of(w: I.Workload, launch_ms: list[float]) -> dict:
+    peak, src = peak_for(w)
+    achieved = w.flops / (float(np.mean(launch_ms)) * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": profiled_traffic(w.name), "peak_source": src, "flop_per_launch": w.flops,
+            "kernel": KERNEL_NAMES[(w.direction, w.dtype)]}
+
+
+def kernel_ms_of(launch_ms: list[float]) -> dict:
+    return {"mean": float(np.mean(launch_ms)), "min": float(np.min(launch_ms)), "max": float(np.max(launch_ms)),
+            "median": float(np.median(launch_ms))}
+
+
+class _Opts:
+    """The per-run options a step class reads, for the workload sub-records."""
+
+    def __init__(self, base, **over):
+        self.tau = base.tau if base.tau_given is not None else 8.0
+        self.tau_given = base.tau_given
+        self.exp2_emu16 = base.exp2_emu16
+        self.p_scaling = base.p_scaling
+        for k, v in over.items():
+            setattr(self, k, v)
+
+
+def sub_record(attn, w: I.Workload, dev, world: int, opts, steps: int, warmup: int) -> dict:
+    """One workload of the suite: its own timed region, roofline and clocks."""
+    step = step_class(w)(attn, w, dev, opts)
+    flush = None
+    l2_note = f"inputs larger than L2 ({step.input_bytes() / 2**20:.0f} MiB > 129 MB)"
+    if step.input_bytes() < 2 * L2_BYTES:
+        scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        flush = scratch.zero_
+        l2_note = ("inputs fit in L2: a 258 MB buffer is written between steps (inside the region); "
+                   "value uses the per-launch CUDA events, which time the kernel alone")
+    m = measure(step, dev, world, steps, warmup, flush)
+    per_step_ms = m["region_ms"] / steps
+    launch_mean = float(np.mean(m["launch_ms"]))
+    rec = {"config": {**w.describe(), "l2": l2_note, "tau": getattr(step, "tau", opts.tau),
+                      "exp2_emu16": opts.exp2_emu16},
+           "steps": steps, "warmup": warmup,
+           "value": w.flops * steps * world / (m["region_ms"] * 1e-3) / 1e12 if flush is None
+           else w.flops * world / (launch_mean * 1e-3) / 1e12,
+           "unit": UNIT, "ms_per_step": per_step_ms if flush is None else launch_mean,
+           "kernel_ms": kernel_ms_of(m["launch_ms"]), "roofline": roofline_of(w, m["launch_ms"]),
+           "clocks": m["clocks"], "gpu_launches": steps * step.launches}
+    if w.dtype == "mxfp8" and w.direction == "fwd":
+        rec["config"]["p_scaling"] = ["block_amax", "constant_2^-8", "constant_2^-8_e5m2"][opts.p_scaling]
+        q_ms = per_step_ms - launch_mean
+        rec["quantize_ms_per_step"] = q_ms
+        rec["quantize_share_of_step"] = q_ms / per_step_ms
+    del step
+    torch.cuda.empty_cache()
+    return rec
+
+
+def workload_suite(attn, args, dev, world: int) -> dict:
+    """Every forward workload besides the headline one, each timed on its own:
+    the tiny one, the causal d = 128 one (Q, K ~ N(0, 2^2)), the causal d = 64
+    one with the MUFU alone and with each software-exp2 share (the best share
+    reported beside it), and the MXFP8 one with the quantiser's share."""
+    steps, warmup = args.suite_steps, max(3, args.warmup)
+    out = {}
+    out[I.TINY.name] = sub_record(attn, I.TINY, dev, world, _Opts(args, exp2_emu16=0), steps, warmup)
+    out[I.CAUSAL_D128_WIDE.name] = sub_record(attn, I.CAUSAL_D128_WIDE, dev, world, _Opts(args, exp2_emu16=0), steps,
+                                              warmup)
+    w = I.CAUSAL_D64
+    mufu = sub_record(attn, w, dev, world, _Opts(args, exp2_emu16=0), steps, warmup)
+    sweep = {}
+    for emu in (1, 2, 3, 4):
+        r = sub_record(attn, w, dev, world, _Opts(args, exp2_emu16=emu), steps, warmup)
+        sweep[f"{emu}/16"] = r
+    best = max(sweep, key=lambda k: sweep[k]["roofline"]["achieved"])
+    mufu["software_exp2_best"] = {"share": best, **sweep[best]}
+    mufu["software_exp2_sweep"] = {k: {"value": r["value"], "kernel_ms_mean": r["kernel_ms"]["mean"],
+                                       "achieved": r["roofline"]["achieved"]} for k, r in sweep.items()}
+    out[w.name] = mufu
+    out[I.MXFP8_CAUSAL.name] = sub_record(attn, I.MXFP8_CAUSAL, dev, world,
+                                          _Opts(args, exp2_emu16=0, p_scaling=0), steps, warmup)
+    return out
+
+
+def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
+    import online_softmax_fwd_gb300 as attn
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    attn.lib()
+    step = step_class(w)(attn, w, dev, args)
+    m = measure(step, dev, world, args.steps, args.warmup)
+    region_ms_max, launch_ms = m["region_ms"], m["launch_ms"]
+    value = w.flops * args.steps * world / (region_ms_max * 1e-3) / 1e12
+
+    e2e = None if args.no_e2e else step.e2e(dev, max(3, min(args.steps, 10)), world)
+    roofline = roofline_of(w, launch_ms)
 
     cpu = None
+    threads, threads_src = oracle_threads()
     if rank == 0 and world == 1 and not args.no_cpu_baseline and w.direction == "bwd":
         ins = ((step.xq_h, step.xk_h, step.xv_h) if w.dtype == "mxfp8" else (step.q_h, step.k_h, step.v_h))
         s = oracle_bwd_sample(w, *ins, step.o_h, step.do_h, step.lse_h, args.cpu_seconds)
-        cpu = {"value": s["value"], "unit": UNIT, "cores": torch.get_num_threads(), "kind": "oracle",
+        cpu = {"value": s["value"], "unit": UNIT, "cores": threads, "cores_source": threads_src, "kind": "oracle",
                "sample": f"float64 {'MXFP8 ' if w.dtype == 'mxfp8' else ''}backward oracle on the workload's first "
                          f"{s['heads_touched']} whole head(s) (O and LSE from the forward kernel), "
                          f"{s['seconds']:.1f} s"}
     elif rank == 0 and world == 1 and not args.no_cpu_baseline:
         s = oracle_sample(w, *cpu_inputs(step, w), args.cpu_seconds)
-        cpu = {"value": s["value"], "unit": UNIT, "cores": torch.get_num_threads(), "kind": "oracle",
+        cpu = {"value": s["value"], "unit": UNIT, "cores": threads, "cores_source": threads_src, "kind": "oracle",
                "sample": f"float64 one-shot oracle on {s['rows']} query rows of the workload's first "
                          f"{s['heads_touched']} head(s) against all their keys, {s['seconds']:.1f} s"
                          + (" (inputs: the oracle's own MXFP8 quantisation, dequantised)" if w.dtype == "mxfp8" else "")}
-    clocks = sampler.summary(t_wall0, t_wall1)
+    input_mib = step.input_bytes() / 2**20
+    gpu_launches = args.steps * step.launches
+    del step
+    torch.cuda.empty_cache()
+    suite = None
+    if not args.no_suite and w.name == DEFAULT_WORKLOAD and w.direction == "fwd":
+        suite = workload_suite(attn, args, dev, world)
     if rank == 0:
         out = {"metric": METRIC_BWD if w.direction == "bwd" else METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                "warmup": args.warmup, "ms_per_step": region_ms_max / args.steps, "higher_is_better": True,
                "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8" if w.dtype == "mxfp8" else "bf16",
                "data": "synthetic",
                "config": {**w.describe(), "parallelism": f"replicas{world}" if world > 1 else "single",
-                          "l2": f"inputs larger than L2 ({step.input_bytes() / 2**20:.0f} MiB > 129 MB)",
-                          "tau": step.tau if w.dtype == "mxfp8" else args.tau, "exp2_emu16": args.exp2_emu16,
+                          "l2": f"inputs larger than L2 ({input_mib:.0f} MiB > 129 MB)",
+                          "tau": (0.0 if args.tau_given is None else args.tau) if w.dtype == "mxfp8" else args.tau,
+                          "exp2_emu16": args.exp2_emu16,
                           **({"p_scaling": ["block_amax", "constant_2^-8", "constant_2^-8_e5m2"][args.p_scaling]}
                              if w.dtype == "mxfp8" and w.direction == "fwd" else
                              {"p_scaling": "constant_2^-8", "ds_blocks": "32x32"} if w.dtype == "mxfp8" else {})},
-               "e2e": e2e, "gpu_launches": args.steps * step.launches, "roofline": roofline, "cpu_baseline": cpu,
-               "clocks": clocks, "kernel_ms": {"mean": float(np.mean(launch_ms)), "min": float(np.min(launch_ms)),
-                                               "max": float(np.max(launch_ms))}}
+               "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roofline, "cpu_baseline": cpu,
+               "clocks": m["clocks"], "kernel_ms": kernel_ms_of(launch_ms),
+               "host_overhead_us_per_call": 1e3 * (region_ms_max / args.steps - float(np.mean(launch_ms)))}
+        if suite is not None:
+            out["workloads"] = suite
         print(json.dumps(out), flush=True)
 
 
@@ -736,6 +876,9 @@ def main() -> None:
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-suite", action="store_true",
+                    help="skip the other forward workloads (timed after the headline one by default)")
+    ap.add_argument("--suite-steps", type=int, default=20)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

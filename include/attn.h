@@ -117,14 +117,30 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o
                             void* stream);
 
 /*
- * attn_fwd_host_noalloc -- attn_fwd_host without a caller workspace: the chunk
- * buffers live in a fixed device array of the library,
- * attn_fwd_host_noalloc_max_workspace() bytes (128 MiB), found once per
- * device; nothing is allocated or freed. Problems whose
+ * attn_fwd_host_noalloc -- attn_fwd_host without a caller workspace, for
+ * callers that cannot allocate device memory: a process whose device memory
+ * budget is fixed at start-up, or a plug-in inside a host framework whose own
+ * allocator owns the device, so that a cudaMalloc of its own would fail or
+ * break that framework's accounting. The pages have no counterpart: this is a
+ * convenience of the library, not part of the method.
+ *
+ * The chunk buffers live in one fixed device array of the library,
+ * attn_fwd_host_noalloc_max_workspace() bytes (128 MiB); nothing is allocated
+ * or freed, by the library or by a routine it calls. Problems whose
  * attn_fwd_host_workspace_bytes(B, H, N, d) exceeds that size are rejected
- * with ATTN_ERR_UNSUPPORTED before any work. Calls on one device share the
- * array and are serialised: each call's work starts after the previous call's
- * copies back have finished, whatever streams the calls use. Other arguments,
+ * with ATTN_ERR_UNSUPPORTED before any work. The array is a device variable of
+ * the library's module: with lazy module loading (CUDA_MODULE_LOADING=LAZY, the
+ * runtime's default) a device reserves it when this entry point first runs
+ * there; with eager loading every context that loads the library reserves it,
+ * and keeps it until the process exits.
+ *
+ * The first call on a device does a one-time set-up with that device current:
+ * it looks up the array's device address and creates one event. Make that
+ * first call before any stream capture. Calls on one device share the array and
+ * are serialised by the library: each call's work starts after the previous
+ * call's copies back have finished, whatever streams the calls use, so calls
+ * issued on different streams do not race on it. Nothing in the array needs to
+ * start at zero (each call overwrites the parts it reads). Other arguments,
  * ordering and errors as attn_fwd_host; results identical to it.
  */
 size_t attn_fwd_host_noalloc_max_workspace(void);
@@ -267,7 +283,8 @@ const char* attn_status_string(attn_status_t status);
  *                     an fp32 dQ accumulator, D and LSE log2(e).
  * Asynchronous on `stream` (three kernels: preparation, the main kernel, dQ
  * conversion); nothing is allocated. Errors as attn_fwd, plus
- * ATTN_ERR_INVALID_ARG for a null or too small workspace.
+ * ATTN_ERR_INVALID_ARG for a null or too small workspace and
+ * ATTN_ERR_UNSUPPORTED for B*H > 65535.
  */
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,

@@ -62,65 +62,92 @@ unsigned int* status_word() {
   return p;
 }
 
+// cuTensorMapEncodeTiled is a pure function of its arguments, so a small
+// per-thread cache of recent encodings spares repeated calls on the same
+// buffers (the common case of a training or serving loop) the host work.
+struct MapKey {
+  CUtensorMapDataType type;
+  CUtensorMapSwizzle swizzle;
+  const void* base;
+  cuuint64_t dims[3];
+  cuuint64_t strides[2];
+  cuuint32_t box[3];
+};
+
+bool encode_3d(CUtensorMap* m, CUtensorMapDataType type, const void* base, const cuuint64_t (&dims)[3],
+               const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3], CUtensorMapSwizzle swizzle) {
+  constexpr int kEntries = 8;
+  struct Entry {
+    MapKey key;
+    CUtensorMap map;
+    bool valid;
+  };
+  thread_local Entry cache[kEntries];
+  thread_local int next = 0;
+  MapKey key;
+  std::memset(&key, 0, sizeof key);  // padding bytes take part in the comparison
+  key.type = type;
+  key.swizzle = swizzle;
+  key.base = base;
+  std::memcpy(key.dims, dims, sizeof key.dims);
+  std::memcpy(key.strides, strides, sizeof key.strides);
+  std::memcpy(key.box, box, sizeof key.box);
+  for (auto& e : cache)
+    if (e.valid && std::memcmp(&e.key, &key, sizeof key) == 0) {
+      *m = e.map;
+      return true;
+    }
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, type, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  Entry& e = cache[next];
+  next = (next + 1) % kEntries;
+  e.key = key;
+  e.map = *m;
+  e.valid = true;
+  return true;
+}
+
 // 3-D map over a contiguous [B*H, N, d] bf16 tensor: d innermost, 64-column
 // boxes (128 bytes, the 128-byte swizzle span) of 128 rows; rows past N of a
 // head read as zero.
 bool make_map(CUtensorMap* m, const void* base, int d, int n, long long bh) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(bh)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2u, static_cast<cuuint64_t>(d) * 2u * static_cast<cuuint64_t>(n)};
   cuuint32_t box[3] = {64, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // 3-D map over a contiguous [B*H, N, 128] E4M3 tensor: one 128-byte swizzle
 // row per sequence row, boxes of 128 rows.
 bool make_map_e4m3(CUtensorMap* m, const void* base, int n, long long bh) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
   cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(bh)};
   cuuint64_t strides[2] = {128u, 128u * static_cast<cuuint64_t>(n)};
   cuuint32_t box[3] = {128, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // 3-D map over a contiguous [B*H, N, d] fp32 tensor for reduce-adds: 32-column
 // boxes (128 bytes, the 128-byte swizzle span) of 128 rows; rows past N are
 // not written.
 bool make_map_f32(CUtensorMap* m, void* base, int d, int n, long long bh) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(bh)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4u, static_cast<cuuint64_t>(d) * 4u * static_cast<cuuint64_t>(n)};
   cuuint32_t box[3] = {32, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // 3-D map over a transposed fp32 accumulator [B*H, d, np] for reduce-adds:
 // x = the sequence (N valid of a row stride of np), 32 x 32 boxes (128-byte
 // rows, 128-byte swizzle); columns past N are not written.
 bool make_map_f32_t(CUtensorMap* m, void* base, int d, int n, int np, long long bh) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(bh)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(np) * 4u, static_cast<cuuint64_t>(np) * 4u * static_cast<cuuint64_t>(d)};
   cuuint32_t box[3] = {32, 32, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // SMs of the current device, queried once per device (the persistent grid size)
@@ -239,6 +266,8 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return (d > 0) ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
   if (N > kMaxN || static_cast<long long>(B) * H * ((N + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  // the preparation and conversion kernels put the head index on the grid's y axis
+  if (static_cast<long long>(B) * H > 65535) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || N == 0) return ATTN_OK;
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
   const size_t need = attn_bwd_workspace_bytes(B, H, N, d);

@@ -65,6 +65,7 @@
 #include "bwd_common.cuh"
 #include "fwd_bf16.cuh"
 #include "mxfp8_common.cuh"
+#include "kernel_setup.h"
 #include "ptx.cuh"
 
 namespace attn {
@@ -719,16 +720,10 @@ cudaError_t launch_bwd_mxfp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, c
                              const CUtensorMap& tm_do, const CUtensorMap& tm_dq, const BwdMxArgs& args,
                              cudaStream_t stream) {
   using C = BwdMxCfg;
-  auto kernel = attn_bwd_mxfp8_kernel<CAUSAL>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  constexpr auto kernel = attn_bwd_mxfp8_kernel<CAUSAL>;
+  // shared-memory opt-in and the setmaxnreg register check, once per device
+  const cudaError_t e = kernel_ready<kernel>(C::kSmemBytes, C::kLaunchRegs);
   if (e != cudaSuccess) return e;
-  // the setmaxnreg split must fit the registers the CTA is launched with
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, kernel);
-  if (e != cudaSuccess) return e;
-  // (each warpgroup moves from exactly this count: setmaxnreg.inc only raises
-  // it, setmaxnreg.dec only lowers it)
-  if (fa.numRegs != C::kLaunchRegs) return cudaErrorInvalidConfiguration;
   const long long ctas = static_cast<long long>(args.bh) * args.n_tiles;
   kernel<<<static_cast<unsigned>(ctas), C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_do, tm_dq, args);
   return cudaGetLastError();

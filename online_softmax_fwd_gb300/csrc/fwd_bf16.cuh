@@ -40,6 +40,7 @@
 #include <cstdint>
 
 #include "exp2_fma.cuh"
+#include "kernel_setup.h"
 #include "ptx.cuh"
 #include "schedule.h"
 
@@ -608,18 +609,10 @@ template <int D, bool CAUSAL, int EMU>
 cudaError_t launch_fwd_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                             const FwdArgs& args, const WorkList& wl, int ctas, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kernel = attn_fwd_bf16_kernel<D, CAUSAL, EMU>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  constexpr auto kernel = attn_fwd_bf16_kernel<D, CAUSAL, EMU>;
+  // shared-memory opt-in and the setmaxnreg register check, once per device
+  const cudaError_t e = kernel_ready<kernel>(C::kSmemBytes, C::kLaunchRegs);
   if (e != cudaSuccess) return e;
-  // The setmaxnreg split redistributes the registers the CTA is launched
-  // with; it must not ask for more than that, or the increase would wait for
-  // ever. Refuse to launch if the compiled register count differs.
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, kernel);
-  if (e != cudaSuccess) return e;
-  // (each warpgroup moves from exactly this count: setmaxnreg.inc only raises
-  // it, setmaxnreg.dec only lowers it)
-  if (fa.numRegs != C::kLaunchRegs) return cudaErrorInvalidConfiguration;
   kernel<<<static_cast<unsigned>(ctas), C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, args, wl);
   return cudaGetLastError();
 }

@@ -36,6 +36,7 @@
 #include "exp2_fma.cuh"
 #include "fwd_bf16.cuh"
 #include "mxfp8_common.cuh"
+#include "kernel_setup.h"
 #include "ptx.cuh"
 #include "schedule.h"
 
@@ -549,16 +550,10 @@ __global__ void __launch_bounds__(384, 1)
 template <bool CAUSAL, int EMU, int PS>
 cudaError_t launch_fwd_mxfp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const FwdMxArgs& args, const WorkList& wl, int ctas, cudaStream_t stream) {
-  auto kernel = attn_fwd_mxfp8_kernel<CAUSAL, EMU, PS>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MxCfg::kSmemBytes);
+  constexpr auto kernel = attn_fwd_mxfp8_kernel<CAUSAL, EMU, PS>;
+  // shared-memory opt-in and the setmaxnreg register check, once per device
+  const cudaError_t e = kernel_ready<kernel>(MxCfg::kSmemBytes, MxCfg::kLaunchRegs);
   if (e != cudaSuccess) return e;
-  // the setmaxnreg split must fit the registers the CTA is launched with
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, kernel);
-  if (e != cudaSuccess) return e;
-  // (each warpgroup moves from exactly this count: setmaxnreg.inc only raises
-  // it, setmaxnreg.dec only lowers it)
-  if (fa.numRegs != MxCfg::kLaunchRegs) return cudaErrorInvalidConfiguration;
   kernel<<<static_cast<unsigned>(ctas), MxCfg::kThreads, MxCfg::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, args, wl);
   return cudaGetLastError();
 }

@@ -9,10 +9,11 @@ Modules
   attention      one-shot softmax(Q K^T s) V and LSE (the definition), plus the
                  blockwise online recurrence used only to check the definition
                  against the identities the pages state.
-  exp2_model     the software exp2 (range reduction + degree-3 Horner) as a
-                 NumPy model, and its accuracy statistics.
-  cmodel         ctypes loader for ``exp2_model.c``: the same software exp2 in
-                 scalar C with a fused multiply-add, for bit-exact comparison.
+  exp2_model     the accuracy statistics of a software exp2 (the columns the
+                 page prints) and a bf16 rounding from the value itself.
+  cmodel         ctypes loader for ``exp2_model.c``: the software exp2 (range
+                 reduction + degree-3 Horner) in scalar C with a fused
+                 multiply-add, the one model of it, for bit-exact comparison.
   rescale_stats  the lagging-max (tau) rescale simulator and its statistics.
   mxfp8          the E4M3 / E8M0 32x32 block quantiser and its dequantisation.
   backward       the gradient of the forward (dQ, dK, dV) with P rebuilt from

@@ -83,7 +83,7 @@ def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool, sca
 def blockwise_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool, scale: float,
                         block: int = 128, tau: float | None = None, dtype=np.float64,
                         p_cast=None, row_index: np.ndarray | None = None,
-                        scores: np.ndarray | None = None) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+                        scores: np.ndarray | None = None, max_history: bool = False):
     """The streaming recurrence over key blocks, for one (batch, head) per call
     or for [..., N, d] batched inputs.
 
@@ -108,6 +108,10 @@ def blockwise_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: boo
     scores Q K^T [..., n_q, n_k] directly, for simulations over a chosen score
     distribution; q and k are then not used (pass None). Returns (O, LSE, fired) where fired
     [..., N, nblocks] is True where the running max moved (block 0 included).
+    With ``max_history`` a fourth array [..., N, nblocks] is returned: the
+    reference max (raw score units) that each block's P was taken against (a
+    causal row's P is zero on keys it cannot see, whatever this value), -inf
+    for blocks past the last causal row.
     """
     f = dtype
     v = np.asarray(v).astype(f)
@@ -126,6 +130,7 @@ def blockwise_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: boo
     o = np.zeros(lead + (n_q, v.shape[-1]), dtype=f)
     nblocks = (n_k + block - 1) // block
     fired = np.zeros(lead + (n_q, nblocks), dtype=bool)
+    m_used = np.full(lead + (n_q, nblocks), -np.inf, dtype=np.float64)
     rows = np.arange(n_q) if row_index is None else np.asarray(row_index)
     last_row = int(rows.max()) if rows.size else -1
     for jb in range(nblocks):
@@ -160,8 +165,11 @@ def blockwise_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: boo
         o = (corr[..., None] * o + pv @ v[..., j0:j1, :]).astype(f)
         m = m_new.astype(f)
         fired[..., jb] = move
+        m_used[..., jb] = m
     out = o / l[..., None]
     lse = m.astype(np.float64) * scale + np.log(l.astype(np.float64))
+    if max_history:
+        return out, lse, fired, m_used
     return out, lse, fired
 
 

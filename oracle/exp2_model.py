@@ -1,59 +1,30 @@
-"""Software exp2 on the FMA pipe: NumPy model and accuracy statistics.
+"""Software exp2: accuracy statistics, and the bf16 rounding they need.
 
 TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).
 
-The method ("FlashAttention-4's Softmax Tricks", section "The emulated exp2";
-"Software-Emulated Exponential" on the KernelWiki page) splits
-2^x = 2^floor(x) * 2^frac(x):
+The software exp2 itself is modelled once, in scalar C (``exp2_model.c``,
+loaded by ``oracle.cmodel``): a true fused multiply-add and one add rounded
+toward minus infinity, so it gives the device's bits. That model follows the
+method of "FlashAttention-4's Softmax Tricks", section "The emulated exp2", and
+"Software-Emulated Exponential" on the KernelWiki page. The input is clamped
+at -127. The integer part comes from a rounding-down add of 2^23 + 2^22, and
+the fraction from subtracting it back. A degree-3 polynomial (the printed
+coefficients below, constant term 1) gives 2^frac in Horner form. Shifting the
+integer into the exponent field by an integer add finishes it.
 
-  1. clamp x from below at -127;
-  2. add 2^23 + 2^22 with rounding toward -inf, which leaves floor(x) as an
-     integer in the low mantissa bits of the sum;
-  3. subtract the constant again (exact) and take frac = x - floor(x) in [0, 1);
-  4. evaluate 2^frac with a degree-3 polynomial in Horner form (3 FMAs), using
-     the Sollya fpminimax coefficients printed on the first page (constant
-     term 1);
-  5. add floor(x) << 23 to the polynomial's bit pattern as a 32-bit integer,
-     which multiplies it by 2^floor(x) (floor(x) taken mod 512).
-
-This NumPy model is for the statistics only. Its multiply-add is "exact product
-in float64, one float64 add, one rounding to float32", which double-rounds in
-rare cases; the bit-exact scalar model with a true fused multiply-add is
-``exp2_model.c`` (``oracle.cmodel``).
+This module holds what the tests compare that model (and the device) against:
+the four accuracy columns the page prints for it, measured against float64
+exp2, and a bf16 rounding taken from the value itself.
 """
 from __future__ import annotations
 
 import numpy as np
 
-# Degree-3 coefficients, constant term first ("FlashAttention-4's Softmax
-# Tricks", section "The emulated exp2", the P3 tuple: Sollya fpminimax for
-# relative error with p0 = 1). Degree 4 and 5 coefficients are not printed.
+# Degree-3 coefficients, constant term first, as printed on "FlashAttention-4's
+# Softmax Tricks", section "The emulated exp2" (Sollya fpminimax for relative
+# error with the constant term fixed at 1). Degree 4 and 5 are not printed.
 POLY3 = (1.0, 0.695146143436431884765625, 0.227564394474029541015625,
          0.077119089663028717041015625)
-ROUND_MAGIC = float(2 ** 23 + 2 ** 22)
-CLAMP_LO = -127.0
-
-
-def _mul_add_f32(a: np.ndarray, b: np.ndarray, c: float) -> np.ndarray:
-    # float32*float32 is exact in float64; the sum is rounded, then narrowed.
-    return (a.astype(np.float64) * b.astype(np.float64) + np.float64(np.float32(c))).astype(np.float32)
-
-
-def exp2_emulated(x) -> np.ndarray:
-    """Software exp2 of float32 inputs, float32 result (NumPy model)."""
-    x = np.maximum(np.asarray(x, dtype=np.float32), np.float32(CLAMP_LO))
-    # Step 2 leaves MAGIC + floor(x) in the sum; for x in [-127, 2^22) that sum is
-    # an exactly representable float32, so form it directly from floor(x).
-    whole = np.floor(x.astype(np.float64))
-    rounded = (whole + ROUND_MAGIC).astype(np.float32)
-    frac = x - (rounded - np.float32(ROUND_MAGIC))          # exact, in [0, 1)
-    poly = np.full(x.shape, np.float32(POLY3[-1]), dtype=np.float32)
-    for coef in reversed(POLY3[:-1]):
-        poly = _mul_add_f32(poly, frac, coef)
-    with np.errstate(over="ignore"):
-        shifted = rounded.view(np.int32) << np.int32(23)    # keeps floor(x) mod 512
-        bits = shifted + poly.view(np.int32)                # 32-bit wrap-around add
-    return bits.view(np.float32)
 
 
 def bf16_round(y) -> np.ndarray:

@@ -158,8 +158,8 @@ def test_bwd_rejects_bad_arguments(lib):
     assert lib.attn_bwd_workspace_bytes(B, H, N, 96) == 0
     assert lib.attn_bwd_workspace_bytes(0, H, N, d) == 0
 
-    def args(ws=A * 9, ws_bytes=need, d_=d, causal=1, scale=0.1, b=B, q=A, lse=A * 6):
-        return (q, A * 2, A * 3, A * 4, A * 5, lse, A * 7, A * 8, A * 10, b, H, N, d_, causal, scale, ws, ws_bytes,
+    def args(ws=A * 9, ws_bytes=need, d_=d, causal=1, scale=0.1, b=B, q=A, lse=A * 6, h=H):
+        return (q, A * 2, A * 3, A * 4, A * 5, lse, A * 7, A * 8, A * 10, b, h, N, d_, causal, scale, ws, ws_bytes,
                 None)
 
     assert lib.attn_bwd(*args(d_=96)) == 2
@@ -172,6 +172,7 @@ def test_bwd_rejects_bad_arguments(lib):
     assert lib.attn_bwd(*args(q=A + 8)) == 3
     assert lib.attn_bwd(*args(lse=A * 6 + 2)) == 3
     assert lib.attn_bwd(*args(ws=A * 9 + 16)) == 3
+    assert lib.attn_bwd(*args(b=300, h=300)) == 2   # B*H above the preparation kernel's grid limit
     assert lib.attn_bwd(*args(b=0)) == 0     # nothing to do
 
 

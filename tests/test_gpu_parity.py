@@ -12,7 +12,7 @@ import torch
 
 import attn_inputs as I
 from oracle.attention import attention_fwd, attention_rows
-from parity import compare, sample_rows
+from parity import compare, compare_method, method_reference, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -34,18 +34,29 @@ def run(attn, q, k, v, causal, scale, **kw):
 
 
 def check_full(attn, q, k, v, causal, scale, what, stress=False, **kw):
+    """Every element against the exact oracle; stress inputs (peaked rows whose
+    bf16 rounding of P alone exceeds 1e-2) are gated elementwise against the
+    method at the kernel's precision instead, with the exact oracle still
+    gating the mean and the LSE."""
     o, lse = run(attn, q, k, v, causal, scale, **kw)
     qq, kk, vv = I.as_f64(q), I.as_f64(k), I.as_f64(v)
     o_ref, lse_ref = attention_fwd(qq, kk, vv, causal, scale)
-    weight = attention_fwd(qq, kk, np.abs(vv), causal, scale)[0] if stress else None
-    return compare(I.as_f64(o), lse.double().numpy(), o_ref, lse_ref, what, abs_v_weight=weight)
+    st = compare(I.as_f64(o), lse.double().numpy(), o_ref, lse_ref, what, max_gate=not stress)
+    if stress:
+        tau = kw.get("tau", 8.0)
+        for b in range(qq.shape[0]):
+            for h in range(qq.shape[1]):
+                o_m, _, delta, big_a, suspect = method_reference(qq[b, h], kk[b, h], vv[b, h], causal, scale, tau)
+                compare_method(I.as_f64(o)[b, h], o_m, delta, big_a, suspect, f"{what} b={b} h={h}")
+    return st
 
 
 @pytest.mark.parametrize("causal", [False, True])
 def test_tiny_workload(attn, causal):
     w = I.TINY
     q, k, v = I.bf16_qkv(w)
-    check_full(attn, q, k, v, causal, w.scale, f"{w.name} causal={causal}")
+    st = check_full(attn, q, k, v, causal, w.scale, f"{w.name} causal={causal}")
+    assert st["o_over_1e-2"] == 0 and st["floor_exceptions"] == 0
 
 
 SMALL = [(1, 1, 1, 64), (1, 1, 7, 128), (1, 2, 128, 64), (1, 1, 129, 128), (2, 3, 255, 64), (1, 2, 256, 128),
@@ -177,8 +188,12 @@ def test_full_size_workloads_sampled(attn, w):
         rows = sample_rows(w.N, rng)
         o_ref, lse_ref = attention_rows(I.as_f64(q[b, h, rows]), I.as_f64(k[b, h]), I.as_f64(v[b, h]), rows,
                                         w.causal, w.scale)
-        compare(I.as_f64(o[b, h, rows]), lse[b, h, rows].double().numpy(), o_ref, lse_ref,
-                f"{w.name} b={b} h={h}")
+        st = compare(I.as_f64(o[b, h, rows]), lse[b, h, rows].double().numpy(), o_ref, lse_ref,
+                     f"{w.name} b={b} h={h}")
+        # the sampled rows of all three workloads have |O| < 4 (the causal Q, K ~ N(0, 2^2)
+        # one reaches 3.4), so no element's rounding floor exceeds 1e-2: the plain
+        # bound holds for every element
+        assert st["o_over_1e-2"] == 0 and st["floor_exceptions"] == 0
 
 
 @pytest.mark.parametrize("shape,causal", [((1, 1, (1 << 20) + 37, 64), True), ((1, 2, (1 << 18) + 5, 128), False)],
