@@ -742,7 +742,7 @@ def sub_record(attn, w: I.Workload, dev, world: int, opts, steps: int, warmup: i
     step = step_class(w)(attn, w, dev, opts)
     flush = None
     l2_note = f"inputs larger than L2 ({step.input_bytes() / 2**20:.0f} MiB > 129 MB)"
-    if step.input_bytes() < 2 * L2_BYTES:
+    if step.input_bytes() <= L2_BYTES:
         scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
         flush = scratch.zero_
         l2_note = ("inputs fit in L2: a 258 MB buffer is written between steps (inside the region); "

@@ -93,6 +93,31 @@ attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, 
                           int N, int d, int causal, float scale, float tau, int exp2_emu16, void* stream);
 
 /*
+ * attn_fwd_rescale_log -- attn_fwd_ex (software-exp2 share 0) that also
+ * records every rescale decision, for checking them against the lagging-max
+ * rule of "FlashAttention-4's Softmax Tricks", section "Conditional rescaling,
+ * and when it's exact": a row keeps its stale max when the block's maximum
+ * raises it by at most tau (log2 units of the scaled score) and moves it
+ * otherwise; a warp rescales its O rows when any of its 32 rows moved.
+ *
+ *   rescale_log  device bytes [B, H, N, ceil(N/128)] (128-key blocks), owned
+ *                by the caller. The kernel writes byte (b, h, i, j) for every
+ *                key block j that row i's query tile streams: bit 0 = row i's
+ *                running max moved at block j (always set at block 0, where
+ *                the max starts at -inf), bit 1 = the row's warp (rows
+ *                32 floor(i/32) .. +31 of the head) rescaled O at block j
+ *                (j > 0). Bytes of blocks a tile does not stream (causal:
+ *                blocks past its diagonal block) are left as they were.
+ * A slower debugging variant of the same kernel (the extra stores sit in the
+ * softmax loop); O and LSE are the same as attn_fwd_ex's. Errors as
+ * attn_fwd_ex, plus ATTN_ERR_INVALID_ARG for a null rescale_log on a
+ * non-empty problem.
+ */
+attn_status_t attn_fwd_rescale_log(const void* q, const void* k, const void* v, void* o, float* lse,
+                                   unsigned char* rescale_log, int B, int H, int N, int d, int causal, float scale,
+                                   float tau, void* stream);
+
+/*
  * attn_fwd_host -- attn_fwd with Q, K, V, O and LSE in HOST memory.
  *
  *   q, k, v, o, lse   host pointers, same layouts as attn_fwd. Page-locked

@@ -43,6 +43,9 @@ _SIGNATURES = {
     # ..., scale, tau, exp2_emu16, stream
     "attn_fwd_ex": ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
                     + [ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
+    # q, k, v, o, lse, rescale_log, B, H, N, d, causal, scale, tau, stream
+    "attn_fwd_rescale_log": ([ctypes.c_void_p] * 6 + [ctypes.c_int] * 5
+                             + [ctypes.c_float, ctypes.c_float, ctypes.c_void_p], ctypes.c_int),
     "attn_mxfp8_scale_bytes": ([ctypes.c_int] * 4, ctypes.c_size_t),
     # x, x_e4m3, x_scales, B, H, N, d, role, stream
     "attn_mxfp8_quantize": ([ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [ctypes.c_void_p], ctypes.c_int),
@@ -154,6 +157,25 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
                                    int(bool(causal)), float(scale), float(tau), int(exp2_emu16), h)
             _check(st, "attn_fwd_ex")
     return o, lse
+
+
+def attn_fwd_rescale_log(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                         scale: float | None = None, tau: float = 8.0, stream=None):
+    """attn_fwd_ex (MUFU exp2) plus the rescale log: returns (o, lse, log)
+    with log uint8 [B, H, N, ceil(N/128)] (bit 0 = the row's max moved at that
+    key block, bit 1 = its warp rescaled O). Bytes of blocks a row's tile does
+    not stream stay 0."""
+    B, H, N, d = _check_qkv(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    log = torch.zeros((B, H, N, (N + 127) // 128), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        st = lib().attn_fwd_rescale_log(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(log), B, H, N, d,
+                                        int(bool(causal)), float(scale), float(tau), _stream_handle(stream))
+        _check(st, "attn_fwd_rescale_log")
+    return o, lse, log
 
 
 def attn_fwd_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int, causal: int,

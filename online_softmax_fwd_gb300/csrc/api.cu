@@ -200,12 +200,10 @@ __global__ void exp2_emulated_kernel(const float* __restrict__ x, float* __restr
     y[i] = attn::exp2_fma(x[i]);
 }
 
-}  // namespace
-
-extern "C" {
-
-attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-                          int d, int causal, float scale, float tau, int exp2_emu16, void* stream) {
+// The bf16 forward: argument checks, tensor maps, work list, dispatch. A
+// non-null rescale_log selects the logging instantiation (MUFU exp2 only).
+attn_status_t fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, uint8_t* rescale_log,
+                       int B, int H, int N, int d, int causal, float scale, float tau, int exp2_emu16, void* stream) {
   bool empty = false;
   attn_status_t st = check_fwd_args(q, k, v, o, lse, B, H, N, d, causal, scale, tau, exp2_emu16, &empty);
   if (st != ATTN_OK || empty) return st;
@@ -224,6 +222,7 @@ attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, 
   a.scale = scale;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.tau = tau;
+  a.rescale_log = rescale_log;
   const int n_pairs = (N + 255) / 256;
   a.n_pairs = n_pairs;
   a.bh = static_cast<int>(bh);
@@ -242,13 +241,34 @@ attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, 
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (d == 64)
+  if (rescale_log)
+    e = attn::launch_fwd_bf16_log(d, causal, mq, mk, mv, a, wl, ctas, s);
+  else if (d == 64)
     e = causal ? attn::launch_fwd_bf16_d64_c1(exp2_emu16, mq, mk, mv, a, wl, ctas, s)
                : attn::launch_fwd_bf16_d64_c0(exp2_emu16, mq, mk, mv, a, wl, ctas, s);
   else
     e = causal ? attn::launch_fwd_bf16_d128_c1(exp2_emu16, mq, mk, mv, a, wl, ctas, s)
                : attn::launch_fwd_bf16_d128_c0(exp2_emu16, mq, mk, mv, a, wl, ctas, s);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                          int d, int causal, float scale, float tau, int exp2_emu16, void* stream) {
+  return fwd_bf16(q, k, v, o, lse, nullptr, B, H, N, d, causal, scale, tau, exp2_emu16, stream);
+}
+
+attn_status_t attn_fwd_rescale_log(const void* q, const void* k, const void* v, void* o, float* lse,
+                                   unsigned char* rescale_log, int B, int H, int N, int d, int causal, float scale,
+                                   float tau, void* stream) {
+  bool empty = false;
+  const attn_status_t st = check_fwd_args(q, k, v, o, lse, B, H, N, d, causal, scale, tau, 0, &empty);
+  if (st != ATTN_OK || empty) return st;
+  if (!rescale_log) return ATTN_ERR_INVALID_ARG;
+  return fwd_bf16(q, k, v, o, lse, rescale_log, B, H, N, d, causal, scale, tau, 0, stream);
 }
 
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {

@@ -61,6 +61,11 @@ struct FwdArgs {
   float scale;           // s
   float scale_log2;      // s * log2(e)
   float tau;             // rescale threshold, log2 units
+  // Rescale log (only read by the logging instantiations, else null): one
+  // byte per (head, row, key block), bit 0 = the row's running max moved at
+  // this block, bit 1 = the row's warp rescaled O (any of its 32 rows moved,
+  // block > 0).
+  uint8_t* rescale_log;
 };
 
 template <int D>
@@ -160,7 +165,7 @@ __device__ __forceinline__ void softmax_p_half(const float2 (&s)[64], float2 sl2
   }
 }
 
-template <int D, bool CAUSAL, int EMU>
+template <int D, bool CAUSAL, int EMU, bool LOG = false>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const FwdArgs args,
@@ -523,8 +528,15 @@ __global__ void __launch_bounds__(384, 1)
         softmax_p_half<EMU, true, 0>(s, sl2_2, neg_ms_2, s_tm, acc);
       else
         softmax_p_half<EMU, false, 0>(s, sl2_2, neg_ms_2, s_tm, acc);
-      // correction of O (before any O MMA of this block)
-      if (j > 0 && __any_sync(0xffffffffu, fire)) {
+      // correction of O (before any O MMA of this block), for the whole warp
+      // if any of its rows moved its max
+      const bool warp_rescales = j > 0 && __any_sync(0xffffffffu, fire);
+      if constexpr (LOG) {
+        if (grow < args.n)
+          args.rescale_log[(static_cast<size_t>(bh) * args.n + grow) * nkv + j] =
+              static_cast<uint8_t>((fire ? 1u : 0u) | (warp_rescales ? 2u : 0u));
+      }
+      if (warp_rescales) {
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
           uint32_t ob[32];
@@ -605,11 +617,11 @@ __global__ void __launch_bounds__(384, 1)
 // Launch one instantiation: a persistent grid of `ctas` CTAs of 384 threads,
 // one per SM (at most one per item; the work list, when used, is built for
 // that many).
-template <int D, bool CAUSAL, int EMU>
+template <int D, bool CAUSAL, int EMU, bool LOG = false>
 cudaError_t launch_fwd_bf16(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                             const FwdArgs& args, const WorkList& wl, int ctas, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  constexpr auto kernel = attn_fwd_bf16_kernel<D, CAUSAL, EMU>;
+  constexpr auto kernel = attn_fwd_bf16_kernel<D, CAUSAL, EMU, LOG>;
   // shared-memory opt-in and the setmaxnreg register check, once per device
   const cudaError_t e = kernel_ready<kernel>(C::kSmemBytes, C::kLaunchRegs);
   if (e != cudaSuccess) return e;

@@ -21,6 +21,10 @@ cudaError_t launch_fwd_bf16_d128_c0(int emu16, const CUtensorMap& q, const CUten
 cudaError_t launch_fwd_bf16_d128_c1(int emu16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                     const FwdArgs& a, const WorkList& wl, int ctas, cudaStream_t s);
 
+// the rescale-logging instantiations (MUFU exp2 only; fwd_rescale_log.cu)
+cudaError_t launch_fwd_bf16_log(int d, int causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                const FwdArgs& a, const WorkList& wl, int ctas, cudaStream_t s);
+
 cudaError_t launch_fwd_mxfp8_d128(int causal, int emu16, const CUtensorMap& q, const CUtensorMap& k,
                                   const CUtensorMap& v, const FwdMxArgs& a, const WorkList& wl, int ctas,
                                   cudaStream_t s);

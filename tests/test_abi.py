@@ -206,3 +206,13 @@ def test_quantize_roles(lib):
     assert q(3) == 1 and q(-1) == 1
     assert q(0, d=64) == 2
     assert lib.attn_mxfp8_quantize(A, A * 2, A * 3, 0, 2, 256, 128, 2, None) == 0   # role 2 accepted; empty
+
+
+def test_rescale_log_rejects_bad_arguments(lib):
+    A = 1 << 20
+    f = lambda log=A * 6, tau=8.0, b=1, d=64: lib.attn_fwd_rescale_log(A, A * 2, A * 3, A * 4, A * 5, log, b, 2, 256,
+                                                                        d, 0, 0.125, tau, None)
+    assert f(log=0) == 1                # the log is required
+    assert f(tau=-1.0) == 1 and f(tau=17.0) == 1
+    assert f(d=96) == 2
+    assert f(log=0, b=0) == 0           # empty problem: nothing to do, nothing checked

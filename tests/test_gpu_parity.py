@@ -12,7 +12,7 @@ import torch
 
 import attn_inputs as I
 from oracle.attention import attention_fwd, attention_rows
-from parity import compare, compare_method, method_reference, sample_rows
+from parity import compare, method_reference, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -33,22 +33,29 @@ def run(attn, q, k, v, causal, scale, **kw):
     return o.cpu(), lse.cpu()
 
 
+def method_bounds(q, k, v, causal, scale, tau, rows=None):
+    """(o_m, delta) of the method at the kernel's precision, stacked over the
+    heads of [B, H, R, d] float64 inputs (k, v [B, H, N, d])."""
+    B, H = q.shape[:2]
+    o_m = np.empty(q.shape[:3] + (v.shape[-1],))
+    delta = np.empty_like(o_m)
+    for b in range(B):
+        for h in range(H):
+            o_m[b, h], _, delta[b, h], _, _ = method_reference(q[b, h], k[b, h], v[b, h], causal, scale, tau,
+                                                               row_index=rows)
+    return o_m, delta
+
+
 def check_full(attn, q, k, v, causal, scale, what, stress=False, **kw):
-    """Every element against the exact oracle; stress inputs (peaked rows whose
-    bf16 rounding of P alone exceeds 1e-2) are gated elementwise against the
-    method at the kernel's precision instead, with the exact oracle still
-    gating the mean and the LSE."""
+    """Every element against the exact oracle. With ``stress`` (peaked rows,
+    a lagging max) the method's own floor applies: where the method at the
+    kernel's precision is itself more than 1e-2 from the exact result, the
+    element is gated against the method's tight bound."""
     o, lse = run(attn, q, k, v, causal, scale, **kw)
     qq, kk, vv = I.as_f64(q), I.as_f64(k), I.as_f64(v)
     o_ref, lse_ref = attention_fwd(qq, kk, vv, causal, scale)
-    st = compare(I.as_f64(o), lse.double().numpy(), o_ref, lse_ref, what, max_gate=not stress)
-    if stress:
-        tau = kw.get("tau", 8.0)
-        for b in range(qq.shape[0]):
-            for h in range(qq.shape[1]):
-                o_m, _, delta, big_a, suspect = method_reference(qq[b, h], kk[b, h], vv[b, h], causal, scale, tau)
-                compare_method(I.as_f64(o)[b, h], o_m, delta, big_a, suspect, f"{what} b={b} h={h}")
-    return st
+    method = method_bounds(qq, kk, vv, causal, scale, kw.get("tau", 8.0)) if stress else None
+    return compare(I.as_f64(o), lse.double().numpy(), o_ref, lse_ref, what, method=method)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -81,9 +88,13 @@ def test_software_exp2_shares(attn, emu, d, causal):
 
 @pytest.mark.parametrize("tau", [0.0, 4.0, 8.0, 16.0])
 def test_rescale_thresholds(attn, tau):
-    # Q, K ~ N(0, 2^2): the running max keeps growing along the keys
+    # Q, K ~ N(0, 2^2): the running max keeps growing along the keys. With
+    # tau > 0 the method itself (float64, P rounded to bf16) is up to 0.018
+    # from the exact result on the peaked rows; with tau = 0 it is within 1e-2.
     q, k, v = (I.to_bf16(x) for x in I.draw_fp32(1, 2, 1536, 128, qk_std=2.0, seed=9))
-    check_full(attn, q, k, v, True, 128 ** -0.5, f"tau={tau}", stress=tau > 8.0, tau=tau)
+    st = check_full(attn, q, k, v, True, 128 ** -0.5, f"tau={tau}", stress=True, tau=tau)
+    if tau == 0.0:
+        assert st["o_over_1e-2"] == 0 and st["method_floor_exceptions"] == 0
 
 
 def test_scores_rising_along_keys(attn):
@@ -188,12 +199,21 @@ def test_full_size_workloads_sampled(attn, w):
         rows = sample_rows(w.N, rng)
         o_ref, lse_ref = attention_rows(I.as_f64(q[b, h, rows]), I.as_f64(k[b, h]), I.as_f64(v[b, h]), rows,
                                         w.causal, w.scale)
+        method = None
+        if w.qk_std != 1.0:
+            method = method_bounds(I.as_f64(q[b, h, rows])[None, None], I.as_f64(k[b, h])[None, None],
+                                   I.as_f64(v[b, h])[None, None], w.causal, w.scale, 8.0, rows=rows)
+            method = (method[0][0, 0], method[1][0, 0])
         st = compare(I.as_f64(o[b, h, rows]), lse[b, h, rows].double().numpy(), o_ref, lse_ref,
-                     f"{w.name} b={b} h={h}")
-        # the sampled rows of all three workloads have |O| < 4 (the causal Q, K ~ N(0, 2^2)
-        # one reaches 3.4), so no element's rounding floor exceeds 1e-2: the plain
-        # bound holds for every element
-        assert st["o_over_1e-2"] == 0 and st["floor_exceptions"] == 0
+                     f"{w.name} b={b} h={h}", method=method)
+        # the sampled rows of all three workloads have |O| < 4, so no element's
+        # output-rounding floor exceeds 1e-2. On the unit-variance workloads every
+        # element is within 1e-2; on the causal Q, K ~ N(0, 2^2) one the method
+        # itself (tau = 8, P rounded to bf16) is 0.0113 from the exact result on one
+        # sampled element, which is then held to the method's bound instead
+        assert st["floor_exceptions"] == 0
+        if w.qk_std == 1.0:
+            assert st["o_over_1e-2"] == 0
 
 
 @pytest.mark.parametrize("shape,causal", [((1, 1, (1 << 20) + 37, 64), True), ((1, 2, (1 << 18) + 5, 128), False)],

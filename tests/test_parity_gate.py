@@ -147,3 +147,24 @@ def test_max_history_is_the_running_max():
     _, _, _, mh8 = blockwise_attention(q, k, v, False, 0.25, block=32, tau=8.0, max_history=True)
     assert np.all(np.diff(mh8, axis=1) >= 0)
     assert np.all((s.max(axis=1) - mh8[:, -1]) * 0.25 * LOG2E <= 8.0 + 1e-12)
+
+
+def test_method_floor_exempts_only_what_the_method_itself_misses():
+    # peaked rows with tau = 4: the method (float64, P rounded to bf16, bf16
+    # output) is itself more than 1e-2 from the exact result on a few elements
+    q, k, v = _peaked(n=640, d=64, qk_std=4.0, seed=9)
+    scale = 64 ** -0.5
+    o_ref, lse_ref = attention_fwd(q[None, None], k[None, None], v[None, None], True, scale)
+    o_ref, lse_ref = o_ref[0, 0], lse_ref[0, 0]
+    o_m, lse_m, delta, _, _ = method_reference(q, k, v, True, scale, 4.0)
+    out = bf16_rn(o_m)
+    with pytest.raises(AssertionError):
+        compare(out, lse_m, o_ref, lse_ref, "no method floor")        # the flat 1e-2 cannot hold
+    st = compare(out, lse_m, o_ref, lse_ref, "method floor", method=(o_m, delta))
+    assert st["method_floor_exceptions"] > 0 and st["o_over_1e-2"] <= st["method_floor_exceptions"]
+    # an exempt element two bf16 steps away from the method fails
+    i = np.argwhere(np.abs(out - o_ref) > 1e-2)[0]
+    bad = out.copy()
+    bad[tuple(i)] += 2 * 2.0 ** (np.floor(np.log2(abs(bad[tuple(i)]))) - 7) * np.sign(bad[tuple(i)])
+    with pytest.raises(AssertionError):
+        compare(bad, lse_m, o_ref, lse_ref, "two steps off the method", method=(o_m, delta))
