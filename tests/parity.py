@@ -118,6 +118,33 @@ def compare(o, lse, o_ref, lse_ref, what: str = "", max_gate: bool = True, mean_
     return stats
 
 
+def compare_heads(o, lse, o_ref, lse_ref, q, k, v, causal: bool, scale: float, tau: float = 8.0,
+                  what: str = "", rows=None, mean_gate: bool = True, exp_rel_err: float = 2.0 ** -21) -> dict:
+    """``compare`` over [B, H, R, dv] outputs with the method's floor computed
+    where it is needed: for every head with an element more than 1e-2 from
+    O_ref (beyond its output-rounding floor), the method at the kernel's
+    precision is formed for that head (q [B, H, R, d] the compared rows at
+    positions ``rows``, default 0 .. R-1; k, v [B, H, N, *]) and the element is
+    held to it. Heads without such an element are gated by the flat 1e-2.
+    ``exp_rel_err`` is the relative error of the kernel's exp2 (the MUFU's by
+    default; the software exp2's 8.77e-5 when a share of it is used)."""
+    o = np.asarray(o, dtype=np.float64)
+    o_ref = np.asarray(o_ref, dtype=np.float64)
+    err = np.abs(o - o_ref)
+    rnd = bf16_rn(o_ref)
+    exc = np.abs(rnd - o_ref) > O_MAX_ABS
+    suspect = ((err > O_MAX_ABS) & ~exc) | (exc & (_bf16_steps(o, rnd) > 1))
+    o_m = o_ref.copy()
+    delta = np.zeros_like(o_ref)
+    heads = np.argwhere(suspect.any(axis=(2, 3)))
+    for b, h in heads:
+        o_m[b, h], _, delta[b, h], _, _ = method_reference(q[b, h], k[b, h], v[b, h], causal, scale, tau,
+                                                           exp_rel_err=exp_rel_err, row_index=rows)
+    st = compare(o, lse, o_ref, lse_ref, what, mean_gate=mean_gate, method=(o_m, delta))
+    st["heads_with_method_floor"] = int(len(heads))
+    return st
+
+
 def method_reference(q, k, v, causal: bool, scale: float, tau: float, exp_rel_err: float = 2.0 ** -21,
                      block: int = 128, row_index=None):
     """The method at the kernel's precision for ONE head (float64 q [R, d]
