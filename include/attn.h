@@ -93,6 +93,21 @@ attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, 
                           int N, int d, int causal, float scale, float tau, int exp2_emu16, void* stream);
 
 /*
+ * attn_fwd_2cta -- attn_fwd on CTA pairs (d = 128, non-causal): the 2-CTA tile
+ * of "FlashAttention-4's Softmax Tricks", section "The emulated exp2" (the
+ * 2-CTA non-causal d = 128 configuration). Two CTAs on two SMs share each
+ * product (tcgen05 cta_group::2, issued by the pair's first CTA): the pair's
+ * query tiles are 256 rows, each CTA holding 128 of them, and each CTA stages
+ * only half of every 128-key block of K and V, so the pair reads each block
+ * from L2 once. Same arguments, layouts, results (within the same tolerance)
+ * and errors as attn_fwd, with tau = 8 and the MUFU exp2; d != 128 or
+ * causal != 0 give ATTN_ERR_UNSUPPORTED. The grid is as many CTA pairs as the
+ * device holds at once (queried on the first call on a device).
+ */
+attn_status_t attn_fwd_2cta(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                            int d, int causal, float scale, void* stream);
+
+/*
  * attn_fwd_rescale_log -- attn_fwd_ex (software-exp2 share 0) that also
  * records every rescale decision, for checking them against the lagging-max
  * rule of "FlashAttention-4's Softmax Tricks", section "Conditional rescaling,

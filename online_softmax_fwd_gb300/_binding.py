@@ -43,6 +43,8 @@ _SIGNATURES = {
     # ..., scale, tau, exp2_emu16, stream
     "attn_fwd_ex": ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
                     + [ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
+    # q, k, v, o, lse, B, H, N, d, causal, scale, stream
+    "attn_fwd_2cta": ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_void_p], ctypes.c_int),
     # q, k, v, o, lse, rescale_log, B, H, N, d, causal, scale, tau, stream
     "attn_fwd_rescale_log": ([ctypes.c_void_p] * 6 + [ctypes.c_int] * 5
                              + [ctypes.c_float, ctypes.c_float, ctypes.c_void_p], ctypes.c_int),
@@ -156,6 +158,24 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
             st = lib().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
                                    int(bool(causal)), float(scale), float(tau), int(exp2_emu16), h)
             _check(st, "attn_fwd_ex")
+    return o, lse
+
+
+def attn_fwd_2cta(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                  scale: float | None = None, o: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                  stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """attn_fwd on CTA pairs (d = 128, non-causal): same inputs and outputs."""
+    B, H, N, d = _check_qkv(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        st = lib().attn_fwd_2cta(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(bool(causal)),
+                                 float(scale), _stream_handle(stream))
+        _check(st, "attn_fwd_2cta")
     return o, lse
 
 

@@ -121,6 +121,15 @@ bool make_map(CUtensorMap* m, const void* base, int d, int n, long long bh) {
   return encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// The same over a [B*H, N, d] bf16 tensor with 64-row boxes: half of a
+// 128-key block, the share of one CTA of a pair.
+bool make_map_half_rows(CUtensorMap* m, const void* base, int d, int n, long long bh) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2u, static_cast<cuuint64_t>(d) * 2u * static_cast<cuuint64_t>(n)};
+  cuuint32_t box[3] = {64, 64, 1};
+  return encode_3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 // 3-D map over a contiguous [B*H, N, 128] E4M3 tensor: one 128-byte swizzle
 // row per sequence row, boxes of 128 rows.
 bool make_map_e4m3(CUtensorMap* m, const void* base, int n, long long bh) {
@@ -158,6 +167,20 @@ int sm_count() {
   int n = cache[dev].load(std::memory_order_relaxed);
   if (n > 0) return n;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+  cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// CTA pairs of the 2-CTA forward resident at once on the current device,
+// queried once per device
+int pair_count() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  n = attn::fwd_bf16_d128_2cta_max_clusters();
+  if (n <= 0) return 0;
   cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
@@ -259,6 +282,47 @@ extern "C" {
 attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
                           int d, int causal, float scale, float tau, int exp2_emu16, void* stream) {
   return fwd_bf16(q, k, v, o, lse, nullptr, B, H, N, d, causal, scale, tau, exp2_emu16, stream);
+}
+
+attn_status_t attn_fwd_2cta(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                            int d, int causal, float scale, void* stream) {
+  bool empty = false;
+  attn_status_t st = check_fwd_args(q, k, v, o, lse, B, H, N, d, causal, scale, 8.0f, 0, &empty);
+  if (st != ATTN_OK || empty) return st;
+  if (d != 128 || causal) return ATTN_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  CUtensorMap mq, mkh, mv;
+  if (!make_map(&mq, q, d, N, bh) || !make_map_half_rows(&mkh, k, d, N, bh) || !make_map(&mv, v, d, N, bh))
+    return ATTN_ERR_CUDA;
+  unsigned int* status = status_word();
+  if (!status) return ATTN_ERR_CUDA;
+  attn::FwdArgs a;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.status = status;
+  a.n = N;
+  a.n_kv_blocks = (N + 127) / 128;
+  a.scale = scale;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.tau = 8.0f;
+  a.rescale_log = nullptr;
+  const int n_groups = (N + 511) / 512;  // a work item: 512 query rows of one head
+  a.n_pairs = n_groups;
+  a.bh = static_cast<int>(bh);
+  a.band = static_cast<int>(band_for(4LL * N * d, bh));
+  const int pairs = pair_count();
+  if (pairs <= 0) return ATTN_ERR_CUDA;
+  const long long items = bh * n_groups;
+  attn::WorkList wl;
+  int clusters = static_cast<int>(std::min<long long>(items, std::min(pairs, attn::kListMaxCtas)));
+  a.use_list = attn::work_list_for(a.bh, n_groups, a.n_kv_blocks, a.band, false, clusters, &wl) ? 1 : 0;
+  if (!a.use_list) {
+    std::memset(&wl, 0, sizeof(wl));
+    clusters = static_cast<int>(std::min<long long>(items, pairs));
+  }
+  const cudaError_t e =
+      attn::launch_fwd_bf16_d128_2cta(mq, mkh, mv, a, wl, clusters, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 attn_status_t attn_fwd_rescale_log(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -21,6 +21,12 @@ cudaError_t launch_fwd_bf16_d128_c0(int emu16, const CUtensorMap& q, const CUten
 cudaError_t launch_fwd_bf16_d128_c1(int emu16, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                     const FwdArgs& a, const WorkList& wl, int ctas, cudaStream_t s);
 
+// the CTA-pair instantiation (d = 128, non-causal; fwd_d128_2cta.cu): k_half is
+// a map of K with 64-row boxes; the grid is `clusters` pairs of CTAs
+cudaError_t launch_fwd_bf16_d128_2cta(const CUtensorMap& q, const CUtensorMap& k_half, const CUtensorMap& v,
+                                      const FwdArgs& a, const WorkList& wl, int clusters, cudaStream_t s);
+int fwd_bf16_d128_2cta_max_clusters();
+
 // the rescale-logging instantiations (MUFU exp2 only; fwd_rescale_log.cu)
 cudaError_t launch_fwd_bf16_log(int d, int causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                 const FwdArgs& a, const WorkList& wl, int ctas, cudaStream_t s);

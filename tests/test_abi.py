@@ -216,3 +216,12 @@ def test_rescale_log_rejects_bad_arguments(lib):
     assert f(tau=-1.0) == 1 and f(tau=17.0) == 1
     assert f(d=96) == 2
     assert f(log=0, b=0) == 0           # empty problem: nothing to do, nothing checked
+
+
+def test_2cta_accepts_only_d128_non_causal(lib):
+    A = 1 << 20
+    f = lambda d=128, causal=0, b=1, scale=0.1: lib.attn_fwd_2cta(A, A * 2, A * 3, A * 4, A * 5, b, 2, 300, d, causal,
+                                                                  scale, None)
+    assert f(causal=1) == 2 and f(d=64) == 2 and f(d=96) == 2
+    assert f(scale=0.0) == 1 and f(causal=2) == 1
+    assert f(b=0) == 0
