@@ -45,16 +45,22 @@ L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = {
     "bf16": ["online_softmax_fwd_gb300/csrc/fwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/ptx.cuh",
              "online_softmax_fwd_gb300/csrc/exp2_fma.cuh", "online_softmax_fwd_gb300/csrc/schedule.h",
-             "online_softmax_fwd_gb300/csrc/schedule.cu"],
+             "online_softmax_fwd_gb300/csrc/schedule.cu", "online_softmax_fwd_gb300/csrc/kernel_setup.h"],
+    "bf16_2cta": ["online_softmax_fwd_gb300/csrc/fwd_bf16_2cta.cuh", "online_softmax_fwd_gb300/csrc/fwd_bf16.cuh",
+                  "online_softmax_fwd_gb300/csrc/ptx.cuh", "online_softmax_fwd_gb300/csrc/schedule.h",
+                  "online_softmax_fwd_gb300/csrc/schedule.cu", "online_softmax_fwd_gb300/csrc/kernel_setup.h"],
     "mxfp8": ["online_softmax_fwd_gb300/csrc/fwd_mxfp8.cuh", "online_softmax_fwd_gb300/csrc/mxfp8_common.cuh",
+              "online_softmax_fwd_gb300/csrc/kernel_setup.h",
               "online_softmax_fwd_gb300/csrc/fwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/ptx.cuh",
               "online_softmax_fwd_gb300/csrc/exp2_fma.cuh", "online_softmax_fwd_gb300/csrc/schedule.h",
               "online_softmax_fwd_gb300/csrc/schedule.cu"],
     "bwd": ["online_softmax_fwd_gb300/csrc/bwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/bwd_common.cuh",
+            "online_softmax_fwd_gb300/csrc/kernel_setup.h",
             "online_softmax_fwd_gb300/csrc/bwd_aux.cu",
             "online_softmax_fwd_gb300/csrc/fwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/ptx.cuh",
             "online_softmax_fwd_gb300/csrc/exp2_fma.cuh", "online_softmax_fwd_gb300/csrc/schedule.h"],
     "bwd_mxfp8": ["online_softmax_fwd_gb300/csrc/bwd_mxfp8.cuh", "online_softmax_fwd_gb300/csrc/bwd_common.cuh",
+                  "online_softmax_fwd_gb300/csrc/kernel_setup.h",
                   "online_softmax_fwd_gb300/csrc/bwd_aux.cu", "online_softmax_fwd_gb300/csrc/mxfp8_common.cuh",
                   "online_softmax_fwd_gb300/csrc/quant_mxfp8.cu", "online_softmax_fwd_gb300/csrc/fwd_bf16.cuh",
                   "online_softmax_fwd_gb300/csrc/ptx.cuh"],
@@ -415,8 +421,11 @@ class Bf16Step:
         w = self.w
         if ev:
             ev[0].record()
-        st = self.attn.attn_fwd_raw(*self.ptrs, w.B, w.H, w.N, w.d, int(w.causal), float(w.scale), sh,
-                                    tau=self.args.tau, exp2_emu16=self.args.exp2_emu16)
+        if getattr(self.args, "two_cta", False):
+            st = self.attn.lib().attn_fwd_2cta(*self.ptrs, w.B, w.H, w.N, w.d, int(w.causal), float(w.scale), sh)
+        else:
+            st = self.attn.attn_fwd_raw(*self.ptrs, w.B, w.H, w.N, w.d, int(w.causal), float(w.scale), sh,
+                                        tau=self.args.tau, exp2_emu16=self.args.exp2_emu16)
         if ev:
             ev[1].record()
         if st != 0:
@@ -712,12 +721,12 @@ def peak_for(w: I.Workload) -> tuple[float, str]:
     return bf16_peak, src
 
 
-def roofline_of(w: I.Workload, launch_ms: list[float]) -> dict:
+def roofline_of(w: I.Workload, launch_ms: list[float], kernel: str | None = None) -> dict:
     peak, src = peak_for(w)
     achieved = w.flops / (float(np.mean(launch_ms)) * 1e-3) / 1e12
     return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": profiled_traffic(w.name), "peak_source": src, "flop_per_launch": w.flops,
-            "kernel": KERNEL_NAMES[(w.direction, w.dtype)]}
+            "kernel": kernel or KERNEL_NAMES[(w.direction, w.dtype)]}
 
 
 def kernel_ms_of(launch_ms: list[float]) -> dict:
@@ -733,6 +742,7 @@ class _Opts:
         self.tau_given = base.tau_given
         self.exp2_emu16 = base.exp2_emu16
         self.p_scaling = base.p_scaling
+        self.two_cta = False
         for k, v in over.items():
             setattr(self, k, v)
 
@@ -756,7 +766,8 @@ def sub_record(attn, w: I.Workload, dev, world: int, opts, steps: int, warmup: i
            "value": w.flops * steps * world / (m["region_ms"] * 1e-3) / 1e12 if flush is None
            else w.flops * world / (launch_mean * 1e-3) / 1e12,
            "unit": UNIT, "ms_per_step": per_step_ms if flush is None else launch_mean,
-           "kernel_ms": kernel_ms_of(m["launch_ms"]), "roofline": roofline_of(w, m["launch_ms"]),
+           "kernel_ms": kernel_ms_of(m["launch_ms"]),
+           "roofline": roofline_of(w, m["launch_ms"], "attn_fwd_bf16_2cta_kernel" if opts.two_cta else None),
            "clocks": m["clocks"], "gpu_launches": steps * step.launches}
     if w.dtype == "mxfp8" and w.direction == "fwd":
         rec["config"]["p_scaling"] = ["block_amax", "constant_2^-8", "constant_2^-8_e5m2"][opts.p_scaling]
@@ -789,6 +800,9 @@ def workload_suite(attn, args, dev, world: int) -> dict:
     mufu["software_exp2_sweep"] = {k: {"value": r["value"], "kernel_ms_mean": r["kernel_ms"]["mean"],
                                        "achieved": r["roofline"]["achieved"]} for k, r in sweep.items()}
     out[w.name] = mufu
+    # the non-causal d = 128 workload once more on CTA pairs (attn_fwd_2cta)
+    out[I.NONCAUSAL_D128.name + "_2cta"] = sub_record(attn, I.NONCAUSAL_D128, dev, world,
+                                                      _Opts(args, exp2_emu16=0, two_cta=True), steps, warmup)
     out[I.MXFP8_CAUSAL.name] = sub_record(attn, I.MXFP8_CAUSAL, dev, world,
                                           _Opts(args, exp2_emu16=0, p_scaling=0), steps, warmup)
     return out
@@ -805,7 +819,7 @@ def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
     value = w.flops * args.steps * world / (region_ms_max * 1e-3) / 1e12
 
     e2e = None if args.no_e2e else step.e2e(dev, max(3, min(args.steps, 10)), world)
-    roofline = roofline_of(w, launch_ms)
+    roofline = roofline_of(w, launch_ms, "attn_fwd_bf16_2cta_kernel" if args.two_cta else None)
 
     cpu = None
     threads, threads_src = oracle_threads()
@@ -837,7 +851,7 @@ def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
                "config": {**w.describe(), "parallelism": f"replicas{world}" if world > 1 else "single",
                           "l2": f"inputs larger than L2 ({input_mib:.0f} MiB > 129 MB)",
                           "tau": (0.0 if args.tau_given is None else args.tau) if w.dtype == "mxfp8" else args.tau,
-                          "exp2_emu16": args.exp2_emu16,
+                          "exp2_emu16": args.exp2_emu16, **({"kernel": "2cta"} if args.two_cta else {}),
                           **({"p_scaling": ["block_amax", "constant_2^-8", "constant_2^-8_e5m2"][args.p_scaling]}
                              if w.dtype == "mxfp8" and w.direction == "fwd" else
                              {"p_scaling": "constant_2^-8", "ds_blocks": "32x32"} if w.dtype == "mxfp8" else {})},
@@ -879,6 +893,8 @@ def main() -> None:
     ap.add_argument("--no-suite", action="store_true",
                     help="skip the other forward workloads (timed after the headline one by default)")
     ap.add_argument("--suite-steps", type=int, default=20)
+    ap.add_argument("--two-cta", action="store_true",
+                    help="bf16 d = 128 non-causal forward on CTA pairs (attn_fwd_2cta)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -62,13 +62,17 @@ struct Fwd2Cfg {
   __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + (t ? 128u : 0u); }
 };
 
-// Bounded wait at cluster scope (a barrier other CTAs arrive on); as wait_bar.
+// Bounded wait at cluster scope (a barrier other CTAs arrive on); as
+// wait_bar. RELAXED: no acquire (the P hand-over, whose data is TMEM ordered
+// by the tcgen05 fences).
+template <bool RELAXED>
 __device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                                  unsigned int* status, uint32_t where) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
+  auto try_once = [&] { return RELAXED ? mbar_try_wait_cluster_relaxed(bar, parity) : mbar_try_wait_cluster(bar, parity); };
+  if (try_once()) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (try_once()) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > kWaitLimitCycles) {
       *abort_flag = 1u;
@@ -250,8 +254,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
       auto wait = [&](uint32_t bar, uint32_t parity, uint32_t where) {
         return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, args.status, where));
       };
+      // the load reports of CTA 1 (release / acquire at cluster scope: CTA 1's
+      // shared memory, written by its TMA, is read by these products)
       auto wait_cl = [&](uint32_t bar, uint32_t parity, uint32_t where) {
-        return __all_sync(0xffffffffu, wait_bar_cluster(bar, parity, abort_flag, args.status, where));
+        return __all_sync(0xffffffffu, wait_bar_cluster<false>(bar, parity, abort_flag, args.status, where));
+      };
+      // P of both CTAs (relaxed: TMEM, ordered by the tcgen05 fences)
+      auto wait_p = [&](uint32_t bar, uint32_t parity, uint32_t where) {
+        return __all_sync(0xffffffffu, wait_bar_cluster<true>(bar, parity, abort_flag, args.status, where));
       };
       // a ring slot has landed in both CTAs
       auto wait_slot = [&](uint32_t slot, uint32_t parity, uint32_t where) {
@@ -322,11 +332,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
           uint32_t ks_next = ks, kph_next = kph;
           advance2(ks_next, kph_next);
           const uint32_t par = (gb + j) & 1;
-          ok = wait_cl(bar_p(0, 0), par, 5);
+          ok = wait_p(bar_p(0, 0), par, 5);
           if (!ok) break;
           tc_fence_after();
           issue_pv(0, vs, 0, j == 0);
-          ok = wait_cl(bar_p(0, 1), par, 11);
+          ok = wait_p(bar_p(0, 1), par, 11);
           if (!ok) break;
           tc_fence_after();
           issue_pv(0, vs, 1, false);
@@ -339,11 +349,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
           } else {
             commit_both(bar_o(0));
           }
-          ok = wait_cl(bar_p(1, 0), par, 7);
+          ok = wait_p(bar_p(1, 0), par, 7);
           if (!ok) break;
           tc_fence_after();
           issue_pv(1, vs, 0, j == 0);
-          ok = wait_cl(bar_p(1, 1), par, 12);
+          ok = wait_p(bar_p(1, 1), par, 12);
           if (!ok) break;
           tc_fence_after();
           issue_pv(1, vs, 1, false);
@@ -378,15 +388,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(384, 1)
     const uint32_t o_tm = tmem + lane_off + C::col_o(t);
     const float sl2 = args.scale_log2;
     const float2 sl2_2 = make_float2(sl2, sl2);
-    // P of this tile is ready: CTA 0's threads arrive on their own barrier,
-    // CTA 1's on CTA 0's (release at cluster scope, after the TMEM stores)
+    // P of this tile is ready: CTA 0's threads arrive on their own barrier;
+    // in CTA 1 each warp's threads have waited for their TMEM stores and
+    // fenced them (tcgen05.fence::before_thread_sync), the warp synchronises,
+    // and one lane arrives for all 32 on CTA 0's barrier: four remote
+    // arrivals per hand-over instead of 128, relaxed (the data is TMEM, whose
+    // order the tcgen05 fences give; a release at cluster scope here cost
+    // ~800 ns per hand-over)
     const uint32_t p_bar[2] = {rank == 0 ? bar_p(t, 0) : cluster_addr(bar_p(t, 0), 0),
                                rank == 0 ? bar_p(t, 1) : cluster_addr(bar_p(t, 1), 0)};
     auto arrive_p = [&](int h) {
-      if (rank == 0)
+      if (rank == 0) {
         mbar_arrive(p_bar[h]);
-      else
-        mbar_arrive_remote(p_bar[h]);
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote_relaxed(p_bar[h], 32u);
+      }
     };
     bool ok = true;
     uint32_t gb = 0;

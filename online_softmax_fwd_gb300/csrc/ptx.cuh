@@ -331,6 +331,31 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) 
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
+// The same, counting `count` arrivals at once.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar), "r"(count)
+               : "memory");
+}
+// The same without memory ordering at cluster scope: a signal whose data
+// needs no release, e.g. TMEM contents already ordered by the tcgen05
+// fences (tcgen05.wait::st and fence::before_thread_sync before the arrive,
+// fence::after_thread_sync after the wait). A release at cluster scope on
+// that path cost ~800 ns per arrive on the GPU.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster_relaxed(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.relaxed.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // try_wait with acquire at cluster scope, for barriers that other CTAs arrive on.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;

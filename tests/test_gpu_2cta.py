@@ -82,16 +82,17 @@ def test_agrees_with_one_cta_kernel(attn):
     assert torch.equal(o2, o3) and torch.equal(l2, l3)          # repeatable
     d = (o1.float() - o2.float()).abs()
     print(f"2cta vs 1-CTA: identical {torch.equal(o1, o2)}, max |diff| {d.max().item():.3g}, "
+          f"pairs resident {torch.cuda.get_device_properties(0).multi_processor_count // 2} at most, "
           f"lse max |diff| {(l1 - l2).abs().max().item():.3g}")
-    # the same products in the same order of K steps: at most one bf16 step apart
-    assert d.max().item() <= 2.0 ** -7 * max(1.0, o1.float().abs().max().item())
-    assert (l1 - l2).abs().max().item() <= 1e-5
+    # the same products over the same K steps in the same order, the pair's B
+    # halves only staged in two shared memories: the results are identical
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
 def test_full_size_workload_sampled(attn):
     w = I.NONCAUSAL_D128
     q, k, v = I.bf16_qkv(w)
-    o, lse = run2(attn, q, k, v, w.scale)
+    o, lse = (t.cpu() for t in run2(attn, q, k, v, w.scale))
     assert torch.isfinite(lse).all()
     rng = np.random.default_rng(1)
     heads = {(0, 0), (w.B - 1, w.H - 1), (int(rng.integers(w.B)), int(rng.integers(w.H)))}
