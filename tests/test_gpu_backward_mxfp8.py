@@ -10,13 +10,13 @@ What the oracle leaves to the kernel: the bf16 rounding of the outputs (half an
 ulp, 0.29 ulp r.m.s.), fp32 accumulation, and the rare P or dS whose fp32 and
 float64 values round to neighbouring E4M3 codes (one E4M3 step, 2^-3 of the
 term) or, rarer still, a block whose fp32 and float64 maxima fall on either
-side of a scale boundary. Allowed, elementwise: ulp_bf16(x_emu) + 2^-2 T + 1e-5,
-T the output's largest single term (s |dS_ij| |K_jd| for dQ, s |dS_ij| |Q_id|
-for dK, |P_ij| |dO_id| for dV, in E4M3) -- up to two terms a whole E4M3 step
-off; at most 1e-4 of the elements beyond that and none beyond 2^-3 times the
-sum of the absolute terms; and over each output an r.m.s. error at most the
-r.m.s. of ulp_bf16(x_emu). A dropped, doubled or mis-scaled block of terms
-moves the r.m.s. far past that.
+side of a scale boundary. Allowed, for every element: ulp_bf16(x_emu) + 2^-2 T +
+1e-5, T the output's largest single term (s |dS_ij| |K_jd| for dQ, s |dS_ij|
+|Q_id| for dK, |P_ij| |dO_id| for dV, in E4M3) -- up to two terms a whole E4M3
+step off; no element beyond 2^-3 times the sum of its absolute terms; and over
+each output an r.m.s. error at most the r.m.s. of ulp_bf16(x_emu). A dropped,
+doubled or mis-scaled block of terms moves the r.m.s. far past that. Each check
+prints how many elements exceed the per-element bound (none may).
 """
 import numpy as np
 import pytest
@@ -98,8 +98,10 @@ def check(got, emu, term, total, what):
     assert np.isfinite(got).all(), f"{what}: non-finite"
     bound = ulp + 2.0 ** -2 * term + 1e-5
     over = err > bound
-    assert over.mean() <= 1e-4, (f"{what}: {int(over.sum())} of {err.size} elements beyond the bound; "
-                                 f"max err {err.max():.4g}, worst ratio {(err / bound).max():.3g}")
+    print(f"bwd mxfp8 {what}: {int(over.sum())} of {err.size} beyond the bound, worst ratio "
+          f"{(err / bound).max():.3g}, max err {err.max():.4g}")
+    assert not over.any(), (f"{what}: {int(over.sum())} of {err.size} elements beyond the bound; "
+                            f"max err {err.max():.4g}, worst ratio {(err / bound).max():.3g}")
     loose = ulp + 2.0 ** -3 * total + 1e-5
     assert not (err > loose).any(), f"{what}: an element beyond 2^-3 of its absolute terms ({err.max():.4g})"
     rms, rms_ulp = np.sqrt((err ** 2).mean()), np.sqrt((ulp ** 2).mean())
