@@ -481,11 +481,18 @@ class Mxfp8Step:
                 raise self.attn.AttnError(st, "attn_mxfp8_quantize")
         if ev:
             ev[0].record()
-        st = L.attn_fwd_mxfp8_ex(self.codes[0].data_ptr(), self.sf[0].data_ptr(), self.codes[1].data_ptr(),
-                                 self.sf[1].data_ptr(), self.codes[2].data_ptr(), self.sf[2].data_ptr(),
-                                 self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N, w.d, int(w.causal),
-                                 float(w.scale), float(self.tau), int(self.args.exp2_emu16),
-                                 int(self.args.p_scaling), sh)
+        if getattr(self.args, "unroll_kv", False):
+            st = L.attn_fwd_mxfp8_unroll_kv(self.codes[0].data_ptr(), self.sf[0].data_ptr(),
+                                            self.codes[1].data_ptr(), self.sf[1].data_ptr(),
+                                            self.codes[2].data_ptr(), self.sf[2].data_ptr(), self.o.data_ptr(),
+                                            self.lse.data_ptr(), w.B, w.H, w.N, w.d, int(w.causal),
+                                            float(w.scale), sh)
+        else:
+            st = L.attn_fwd_mxfp8_ex(self.codes[0].data_ptr(), self.sf[0].data_ptr(), self.codes[1].data_ptr(),
+                                     self.sf[1].data_ptr(), self.codes[2].data_ptr(), self.sf[2].data_ptr(),
+                                     self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N, w.d, int(w.causal),
+                                     float(w.scale), float(self.tau), int(self.args.exp2_emu16),
+                                     int(self.args.p_scaling), sh)
         if ev:
             ev[1].record()
         if st != 0:
@@ -743,6 +750,7 @@ class _Opts:
         self.exp2_emu16 = base.exp2_emu16
         self.p_scaling = base.p_scaling
         self.two_cta = False
+        self.unroll_kv = False
         for k, v in over.items():
             setattr(self, k, v)
 
@@ -771,6 +779,8 @@ def sub_record(attn, w: I.Workload, dev, world: int, opts, steps: int, warmup: i
            "clocks": m["clocks"], "gpu_launches": steps * step.launches}
     if w.dtype == "mxfp8" and w.direction == "fwd":
         rec["config"]["p_scaling"] = ["block_amax", "constant_2^-8", "constant_2^-8_e5m2"][opts.p_scaling]
+        if opts.unroll_kv:
+            rec["config"]["schedule"] = "unroll_kv"
         q_ms = per_step_ms - launch_mean
         rec["quantize_ms_per_step"] = q_ms
         rec["quantize_share_of_step"] = q_ms / per_step_ms
@@ -805,6 +815,10 @@ def workload_suite(attn, args, dev, world: int) -> dict:
                                                       _Opts(args, exp2_emu16=0, two_cta=True), steps, warmup)
     out[I.MXFP8_CAUSAL.name] = sub_record(attn, I.MXFP8_CAUSAL, dev, world,
                                           _Opts(args, exp2_emu16=0, p_scaling=0), steps, warmup)
+    # the same on the unroll-KV schedule (attn_fwd_mxfp8_unroll_kv)
+    out[I.MXFP8_CAUSAL.name + "_unroll_kv"] = sub_record(attn, I.MXFP8_CAUSAL, dev, world,
+                                                         _Opts(args, exp2_emu16=0, p_scaling=0, unroll_kv=True),
+                                                         steps, warmup)
     return out
 
 
@@ -893,6 +907,8 @@ def main() -> None:
     ap.add_argument("--no-suite", action="store_true",
                     help="skip the other forward workloads (timed after the headline one by default)")
     ap.add_argument("--suite-steps", type=int, default=20)
+    ap.add_argument("--unroll-kv", action="store_true",
+                    help="MXFP8 forward on the unroll-KV schedule (attn_fwd_mxfp8_unroll_kv)")
     ap.add_argument("--two-cta", action="store_true",
                     help="bf16 d = 128 non-causal forward on CTA pairs (attn_fwd_2cta)")
     args = ap.parse_args()

@@ -269,6 +269,22 @@ attn_status_t attn_fwd_mxfp8_ex(const void* q8, const void* q_sf, const void* k8
                                 float scale, float tau, int exp2_emu16, int p_scaling, void* stream);
 
 /*
+ * attn_fwd_mxfp8_unroll_kv -- attn_fwd_mxfp8 (tau = 0, P scaled per 32 keys
+ * from the block amax, MUFU exp2) on the unroll-KV schedule of "PyTorch
+ * FlashAttention-4 adds MXFP8 block-scaled forward and backward for
+ * Blackwell", section "Softmax conversion and unroll-KV": in the last key
+ * block of a work item the next item's first QK^T product is issued between
+ * this item's last two P V products, and the softmax takes P's fp32 row sum
+ * after handing P over. Same arguments, layouts, results (within the same
+ * tolerance) and errors as attn_fwd_mxfp8. Slower than attn_fwd_mxfp8 on
+ * GB300 (its softmax warps run the epilogue, which already hides the
+ * item-boundary wait); kept for comparison.
+ */
+attn_status_t attn_fwd_mxfp8_unroll_kv(const void* q8, const void* q_sf, const void* k8, const void* k_sf,
+                                       const void* v8, const void* v_sf, void* o, float* lse, int B, int H, int N,
+                                       int d, int causal, float scale, void* stream);
+
+/*
  * attn_selftest_wait_timeout -- exercises the kernels' failure detection
  * without a fault: launches one small kernel on stream whose warps wait, with
  * the same bounded wait the attention kernels use, on barriers that nothing

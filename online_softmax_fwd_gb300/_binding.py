@@ -57,6 +57,9 @@ _SIGNATURES = {
     "attn_fwd_mxfp8_ex": ([ctypes.c_void_p] * 8 + [ctypes.c_int] * 5
                           + [ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p],
                           ctypes.c_int),
+    # q8, q_sf, k8, k_sf, v8, v_sf, o, lse, B, H, N, d, causal, scale, stream
+    "attn_fwd_mxfp8_unroll_kv": ([ctypes.c_void_p] * 8 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_void_p],
+                                 ctypes.c_int),
     "attn_exp2_emulated": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p], ctypes.c_int),
     "attn_fwd_host_workspace_bytes": ([ctypes.c_int] * 4, ctypes.c_size_t),
     # q, k, v, o, lse (host), B, H, N, d, causal, scale, workspace, workspace_bytes, stream
@@ -338,12 +341,13 @@ P_SCALE_CONSTANT_E5M2 = 2
 def attn_fwd_mxfp8(q8: torch.Tensor, q_sf: torch.Tensor, k8: torch.Tensor, k_sf: torch.Tensor, v8: torch.Tensor,
                    v_sf: torch.Tensor, causal: bool = False, scale: float | None = None, o: torch.Tensor | None = None,
                    lse: torch.Tensor | None = None, tau: float = 0.0, exp2_emu16: int = 0,
-                   p_scaling: int = 0, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+                   p_scaling: int = 0, unroll_kv: bool = False, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
     """Attention forward from MXFP8 inputs (outputs of mxfp8_quantize); tau
     defaults to 0, the FP8 setting (attn_fwd_mxfp8). p_scaling: 0 = one scale
     per 32 keys from the block amax (P_SCALE_BLOCK_AMAX), 1 = the constant 2^-8
     (P_SCALE_CONSTANT, tau <= 0.807), 2 = the same constant with P held in
-    E5M2 (P_SCALE_CONSTANT_E5M2, tau <= 7.807)."""
+    E5M2 (P_SCALE_CONSTANT_E5M2, tau <= 7.807). unroll_kv selects the unroll-KV
+    schedule (attn_fwd_mxfp8_unroll_kv; tau 0, no software exp2, p_scaling 0)."""
     for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
         if not t.is_cuda or t.dtype != torch.uint8 or t.dim() != 4 or not t.is_contiguous() or t.shape != q8.shape:
             raise ValueError(f"{name} must be contiguous CUDA uint8 (E4M3 codes) shaped like q8")
@@ -360,8 +364,12 @@ def attn_fwd_mxfp8(q8: torch.Tensor, q_sf: torch.Tensor, k8: torch.Tensor, k_sf:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
     h = _stream_handle(stream)
     ptrs = [_ptr(t) for t in (q8, q_sf, k8, k_sf, v8, v_sf, o, lse)]
+    if unroll_kv and (tau != 0.0 or exp2_emu16 != 0 or p_scaling != P_SCALE_BLOCK_AMAX):
+        raise ValueError("the unroll-KV schedule runs with tau = 0, exp2_emu16 = 0 and p_scaling = 0")
     with torch.cuda.device(q8.device):
-        if tau == 0.0 and exp2_emu16 == 0 and p_scaling == P_SCALE_BLOCK_AMAX:
+        if unroll_kv:
+            st = lib().attn_fwd_mxfp8_unroll_kv(*ptrs, B, H, N, d, int(bool(causal)), float(scale), h)
+        elif tau == 0.0 and exp2_emu16 == 0 and p_scaling == P_SCALE_BLOCK_AMAX:
             st = lib().attn_fwd_mxfp8(*ptrs, B, H, N, d, int(bool(causal)), float(scale), h)
         else:
             st = lib().attn_fwd_mxfp8_ex(*ptrs, B, H, N, d, int(bool(causal)), float(scale), float(tau),

@@ -275,6 +275,75 @@ attn_status_t fwd_bf16(const void* q, const void* k, const void* v, void* o, flo
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// The MXFP8 forward: argument checks, tensor maps, work list, dispatch;
+// unroll_kv selects the unroll-KV schedule (MUFU exp2, per-32-key amax P only).
+attn_status_t fwd_mxfp8(const void* q8, const void* q_sf, const void* k8, const void* k_sf, const void* v8,
+                        const void* v_sf, void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
+                        float tau, int exp2_emu16, int p_scaling, bool unroll_kv, void* stream) {
+  if (B < 0 || H < 0 || N < 0 || (causal != 0 && causal != 1)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(tau) || tau < 0.f || tau > 16.f) return ATTN_ERR_INVALID_ARG;
+  if (d != 128) return d > 0 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
+  if (exp2_emu16 < 0 || exp2_emu16 > 16) return ATTN_ERR_INVALID_ARG;
+  if (exp2_emu16 != 0 && exp2_emu16 != 2 && exp2_emu16 != 4) return ATTN_ERR_UNSUPPORTED;
+  if (p_scaling != ATTN_P_SCALE_BLOCK_AMAX && p_scaling != ATTN_P_SCALE_CONSTANT &&
+      p_scaling != ATTN_P_SCALE_CONSTANT_E5M2)
+    return ATTN_ERR_INVALID_ARG;
+  // constant 2^-8: the largest P, 2^tau, must stay within the format's largest
+  // value / 256 (E4M3 448, E5M2 57344)
+  if (p_scaling == ATTN_P_SCALE_CONSTANT && !(tau <= kPConstMaxTau)) return ATTN_ERR_INVALID_ARG;
+  if (p_scaling == ATTN_P_SCALE_CONSTANT_E5M2 && !(tau <= kPConstE5m2MaxTau)) return ATTN_ERR_INVALID_ARG;
+  if (N > kMaxN || static_cast<long long>(B) * H * ((N + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (!q8 || !q_sf || !k8 || !k_sf || !v8 || !v_sf || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(q_sf) || !aligned16(k_sf) ||
+      !aligned16(v_sf) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  const long long bh = static_cast<long long>(B) * H;
+  CUtensorMap mq, mk, mv;
+  if (!make_map_e4m3(&mq, q8, N, bh) || !make_map_e4m3(&mk, k8, N, bh) || !make_map_e4m3(&mv, v8, N, bh))
+    return ATTN_ERR_CUDA;
+  unsigned int* status = status_word();
+  if (!status) return ATTN_ERR_CUDA;
+  attn::FwdMxArgs a;
+  a.q_sf = static_cast<const uint8_t*>(q_sf);
+  a.k_sf = static_cast<const uint8_t*>(k_sf);
+  a.v_sf = static_cast<const uint8_t*>(v_sf);
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.status = status;
+  a.n = N;
+  a.n_tiles = (N + 127) / 128;
+  a.n_pairs = (N + 255) / 256;
+  a.bh = static_cast<int>(bh);
+  a.band = static_cast<int>(band_for(2LL * N * 128, bh));
+  a.scale = scale;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.tau = tau;
+  const int sms = sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  // persistent grid with the same work-list schedule as the bf16 kernel
+  const long long items = bh * a.n_pairs;
+  attn::WorkList wl;
+  int ctas = static_cast<int>(std::min<long long>(items, std::min(sms, attn::kListMaxCtas)));
+  a.use_list = attn::work_list_for(a.bh, a.n_pairs, a.n_tiles, a.band, causal != 0, ctas, &wl) ? 1 : 0;
+  if (!a.use_list) {
+    std::memset(&wl, 0, sizeof(wl));
+    ctas = static_cast<int>(std::min<long long>(items, sms));
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (unroll_kv)
+    e = attn::launch_fwd_mxfp8_d128_ukv(causal, mq, mk, mv, a, wl, ctas, st);
+  else if (p_scaling == ATTN_P_SCALE_CONSTANT)
+    e = attn::launch_fwd_mxfp8_d128_pconst(causal, exp2_emu16, mq, mk, mv, a, wl, ctas, st);
+  else if (p_scaling == ATTN_P_SCALE_CONSTANT_E5M2)
+    e = attn::launch_fwd_mxfp8_d128_pconst_e5m2(causal, exp2_emu16, mq, mk, mv, a, wl, ctas, st);
+  else
+    e = attn::launch_fwd_mxfp8_d128(causal, exp2_emu16, mq, mk, mv, a, wl, ctas, st);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -489,66 +558,15 @@ attn_status_t attn_mxfp8_quantize(const float* x, void* x_e4m3, void* x_scales, 
 attn_status_t attn_fwd_mxfp8_ex(const void* q8, const void* q_sf, const void* k8, const void* k_sf, const void* v8,
                                 const void* v_sf, void* o, float* lse, int B, int H, int N, int d, int causal,
                                 float scale, float tau, int exp2_emu16, int p_scaling, void* stream) {
-  if (B < 0 || H < 0 || N < 0 || (causal != 0 && causal != 1)) return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(tau) || tau < 0.f || tau > 16.f) return ATTN_ERR_INVALID_ARG;
-  if (d != 128) return d > 0 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
-  if (exp2_emu16 < 0 || exp2_emu16 > 16) return ATTN_ERR_INVALID_ARG;
-  if (exp2_emu16 != 0 && exp2_emu16 != 2 && exp2_emu16 != 4) return ATTN_ERR_UNSUPPORTED;
-  if (p_scaling != ATTN_P_SCALE_BLOCK_AMAX && p_scaling != ATTN_P_SCALE_CONSTANT &&
-      p_scaling != ATTN_P_SCALE_CONSTANT_E5M2)
-    return ATTN_ERR_INVALID_ARG;
-  // constant 2^-8: the largest P, 2^tau, must stay within the format's largest
-  // value / 256 (E4M3 448, E5M2 57344)
-  if (p_scaling == ATTN_P_SCALE_CONSTANT && !(tau <= kPConstMaxTau)) return ATTN_ERR_INVALID_ARG;
-  if (p_scaling == ATTN_P_SCALE_CONSTANT_E5M2 && !(tau <= kPConstE5m2MaxTau)) return ATTN_ERR_INVALID_ARG;
-  if (N > kMaxN || static_cast<long long>(B) * H * ((N + 255) / 256) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
-  if (!q8 || !q_sf || !k8 || !k_sf || !v8 || !v_sf || !o || !lse) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(q_sf) || !aligned16(k_sf) ||
-      !aligned16(v_sf) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u))
-    return ATTN_ERR_MISALIGNED;
-  const long long bh = static_cast<long long>(B) * H;
-  CUtensorMap mq, mk, mv;
-  if (!make_map_e4m3(&mq, q8, N, bh) || !make_map_e4m3(&mk, k8, N, bh) || !make_map_e4m3(&mv, v8, N, bh))
-    return ATTN_ERR_CUDA;
-  unsigned int* status = status_word();
-  if (!status) return ATTN_ERR_CUDA;
-  attn::FwdMxArgs a;
-  a.q_sf = static_cast<const uint8_t*>(q_sf);
-  a.k_sf = static_cast<const uint8_t*>(k_sf);
-  a.v_sf = static_cast<const uint8_t*>(v_sf);
-  a.o = static_cast<__nv_bfloat16*>(o);
-  a.lse = lse;
-  a.status = status;
-  a.n = N;
-  a.n_tiles = (N + 127) / 128;
-  a.n_pairs = (N + 255) / 256;
-  a.bh = static_cast<int>(bh);
-  a.band = static_cast<int>(band_for(2LL * N * 128, bh));
-  a.scale = scale;
-  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  a.tau = tau;
-  const int sms = sm_count();
-  if (sms <= 0) return ATTN_ERR_CUDA;
-  // persistent grid with the same work-list schedule as the bf16 kernel
-  const long long items = bh * a.n_pairs;
-  attn::WorkList wl;
-  int ctas = static_cast<int>(std::min<long long>(items, std::min(sms, attn::kListMaxCtas)));
-  a.use_list = attn::work_list_for(a.bh, a.n_pairs, a.n_tiles, a.band, causal != 0, ctas, &wl) ? 1 : 0;
-  if (!a.use_list) {
-    std::memset(&wl, 0, sizeof(wl));
-    ctas = static_cast<int>(std::min<long long>(items, sms));
-  }
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (p_scaling == ATTN_P_SCALE_CONSTANT)
-    e = attn::launch_fwd_mxfp8_d128_pconst(causal, exp2_emu16, mq, mk, mv, a, wl, ctas, st);
-  else if (p_scaling == ATTN_P_SCALE_CONSTANT_E5M2)
-    e = attn::launch_fwd_mxfp8_d128_pconst_e5m2(causal, exp2_emu16, mq, mk, mv, a, wl, ctas, st);
-  else
-    e = attn::launch_fwd_mxfp8_d128(causal, exp2_emu16, mq, mk, mv, a, wl, ctas, st);
-  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return fwd_mxfp8(q8, q_sf, k8, k_sf, v8, v_sf, o, lse, B, H, N, d, causal, scale, tau, exp2_emu16, p_scaling,
+                   false, stream);
+}
+
+attn_status_t attn_fwd_mxfp8_unroll_kv(const void* q8, const void* q_sf, const void* k8, const void* k_sf,
+                                       const void* v8, const void* v_sf, void* o, float* lse, int B, int H, int N,
+                                       int d, int causal, float scale, void* stream) {
+  return fwd_mxfp8(q8, q_sf, k8, k_sf, v8, v_sf, o, lse, B, H, N, d, causal, scale, 0.0f, 0, ATTN_P_SCALE_BLOCK_AMAX,
+                   true, stream);
 }
 
 attn_status_t attn_fwd_mxfp8(const void* q8, const void* q_sf, const void* k8, const void* k_sf, const void* v8,

@@ -93,7 +93,14 @@ struct MxCfg {
 // tau <= log2(1.75)); 2 = the same constant with P in E5M2, whose 57344
 // leaves room for tau <= log2(224) ("FlashAttention-4's Softmax Tricks",
 // section "Where 'exact' breaks: P in FP8"). V stays E4M3.
-template <bool CAUSAL, int EMU, int PS>
+// UKV selects the unroll-KV schedule ("PyTorch FlashAttention-4 adds MXFP8...",
+// section "Softmax conversion and unroll-KV"): in an item's last key block the
+// next item's first S GEMM is issued ahead of tile 1's last P V GEMM, and the
+// softmax takes P's fp32 row sum after handing P over (P kept in registers; a
+// needed O correction then loads O in 32-column parts). Measured slower on
+// this kernel (its softmax warps run the epilogue, which hides the boundary
+// wait anyway); kept as an opt-in schedule.
+template <bool CAUSAL, int EMU, int PS, bool UKV = false>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_mxfp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const FwdMxArgs args,
@@ -274,6 +281,7 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t ks = 0, kph = 0;  // K_j
       uint32_t vs = 1, vph = 0;  // V_j
       uint32_t gb0 = 0, gb1 = 0;  // blocks of tile 0 / tile 1 before this item
+      bool s0_early = false;       // (UKV) this item's S0(0) went out in the previous item's last block
       bool ok = true;
       int qi = 0;
       for (int it = item_of(0); ok && it < total_items; it = item_of(++qi)) {
@@ -282,6 +290,8 @@ __global__ void __launch_bounds__(384, 1)
         (void)bh;
         const int n0 = blocks_of(pair, 0);
         const int n1 = blocks_of(pair, 1);
+        // (with UKV, re-waiting a phase that already completed returns at once:
+        // the next phase of either barrier needs this item's S GEMMs first)
         ok = wait(bar_q, qi & 1, 2) && wait(bar_full(ks), kph, 3);
         if (!ok) break;
         tc_fence_after();
@@ -292,9 +302,11 @@ __global__ void __launch_bounds__(384, 1)
           issue_s(1, ks, C::col_o(1));
           commit(bar_s(1));
         } else {
-          // S1's columns 40-47 are free (its last scores were loaded before its last P)
-          issue_s(0, ks, C::col_s(1) + C::kQScale);
-          commit(bar_s(0));
+          if (!s0_early) {
+            // S1's columns 40-47 are free (its last scores were loaded before its last P)
+            issue_s(0, ks, C::col_s(1) + C::kQScale);
+            commit(bar_s(0));
+          }
           // S1(0)'s scales go into O1 once the previous item's O1 has been read
           ok = wait(bar_oread(1), (qi - 1) & 1, 14);
           if (!ok) break;
@@ -302,6 +314,7 @@ __global__ void __launch_bounds__(384, 1)
           issue_s(1, ks, C::col_o(1));
           commit(bar_s(1));
         }
+        s0_early = false;
         commit(bar_empty(ks));
         if (n1 == 1) commit(bar_qe);  // this item's S GEMMs are all issued
         for (int j = 0; ok && j < n1; ++j) {
@@ -327,6 +340,21 @@ __global__ void __launch_bounds__(384, 1)
               commit(bar_s(0));
             } else {
               commit(bar_o(0));
+            }
+          }
+          if constexpr (UKV) {
+            // the next item's S0(0) ahead of tile 1's last P V: its Q and K_0
+            // are loaded once this item's S GEMMs are all issued (they are);
+            // its scales go into S1's columns 40-47, free once tile 1 has
+            // loaded its last scores
+            if (j + 1 == n1 && item_of(qi + 1) < total_items) {
+              ok = wait(bar_q, (qi + 1) & 1, 2) && wait(bar_full(ks_next), kph_next, 6) &&
+                   wait(bar_ld(1), (gb1 + j) & 1, 9);
+              if (!ok) break;
+              tc_fence_after();
+              issue_s(0, ks_next, C::col_s(1) + C::kQScale);
+              commit(bar_s(0));
+              s0_early = true;
             }
           }
           ok = wait(bar_p(1), (gb1 + j) & 1, 7);
@@ -465,41 +493,77 @@ __global__ void __launch_bounds__(384, 1)
             p0 = make_float2(exp2_col<EMU, false>(2 * c, x0.x), exp2_col<EMU, false>(2 * c + 1, x0.y));
             p1 = make_float2(exp2_col<EMU, false>(2 * c + 2, x1.x), exp2_col<EMU, false>(2 * c + 3, x1.y));
           }
-          acc[(i >> 1) & 1] = __fadd2_rn(acc[(i >> 1) & 1], p0);
-          acc[2 + ((i >> 1) & 1)] = __fadd2_rn(acc[2 + ((i >> 1) & 1)], p1);
+          if constexpr (UKV) {
+            s[c] = p0;  // kept for the row sum after the hand-over
+            s[c + 1] = p1;
+          } else {
+            acc[(i >> 1) & 1] = __fadd2_rn(acc[(i >> 1) & 1], p0);
+            acc[2 + ((i >> 1) & 1)] = __fadd2_rn(acc[2 + ((i >> 1) & 1)], p1);
+          }
           pk[8 * g + i / 2] = PS == 2 ? pack_e5m2x4(p0.x, p0.y, p1.x, p1.y) : pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
         }
-        acc[0] = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-        lsum = __fmaf_rn(acc[0].x + acc[0].y, __uint_as_float(sfb << 23), lsum);
+        if constexpr (!UKV) {
+          acc[0] = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+          lsum = __fmaf_rn(acc[0].x + acc[0].y, __uint_as_float(sfb << 23), lsum);
+        }
       }
       tmem_st32(s_tm, pk);                      // P, 4 keys per column
       tmem_st1(s_tm + C::kPScale + quad, sfw);  // row r's scales at column r / 32
       // correction of O once the scores are dead; lands before P is handed
-      // over. All of O is loaded at once (one load latency, overlapping the
-      // store of P), scaled and stored back.
+      // over
       if (j > 0 && __any_sync(0xffffffffu, fire)) {
-        uint32_t ob[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(o_tm + 32 * c, ob[c]);
         const float2 corr_2 = make_float2(corr, corr);
-        tmem_ld_wait();
+        if constexpr (UKV) {
+          // 32 columns at a time (P stays in registers for the sum)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          reg_fence32(ob[c]);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ob[32];
+            tmem_ld32(o_tm + 32 * c, ob);
+            tmem_ld_wait();
+            reg_fence32(ob);
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float2 o2 =
-                __fmul2_rn(make_float2(__uint_as_float(ob[c][i]), __uint_as_float(ob[c][i + 1])), corr_2);
-            ob[c][i] = __float_as_uint(o2.x);
-            ob[c][i + 1] = __float_as_uint(o2.y);
+            for (int i = 0; i < 32; i += 2) {
+              const float2 o2 = __fmul2_rn(make_float2(__uint_as_float(ob[i]), __uint_as_float(ob[i + 1])), corr_2);
+              ob[i] = __float_as_uint(o2.x);
+              ob[i + 1] = __float_as_uint(o2.y);
+            }
+            tmem_st32(o_tm + 32 * c, ob);
           }
-          tmem_st32(o_tm + 32 * c, ob[c]);
+        } else {
+          // all of O at once (one load latency, overlapping the store of P)
+          uint32_t ob[4][32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(o_tm + 32 * c, ob[c]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            reg_fence32(ob[c]);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float2 o2 =
+                  __fmul2_rn(make_float2(__uint_as_float(ob[c][i]), __uint_as_float(ob[c][i + 1])), corr_2);
+              ob[c][i] = __float_as_uint(o2.x);
+              ob[c][i + 1] = __float_as_uint(o2.y);
+            }
+            tmem_st32(o_tm + 32 * c, ob[c]);
+          }
         }
       }
-      l = l * corr + lsum;
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_p(t));
+      if constexpr (UKV) {
+        // the O GEMM and the next S GEMM run meanwhile
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          float2 acc[4] = {s[16 * g], s[16 * g + 1], s[16 * g + 2], s[16 * g + 3]};
+#pragma unroll
+          for (int i = 4; i < 16; ++i) acc[i & 3] = __fadd2_rn(acc[i & 3], s[16 * g + i]);
+          acc[0] = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+          lsum = __fmaf_rn(acc[0].x + acc[0].y, __uint_as_float(((sfw >> (8 * g)) & 0xffu) << 23), lsum);
+        }
+      }
+      l = l * corr + lsum;
     }
     if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar_o(t), qi & 1, abort_flag, args.status, 18 + t));
     if (ok) {
@@ -547,10 +611,10 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <bool CAUSAL, int EMU, int PS>
+template <bool CAUSAL, int EMU, int PS, bool UKV = false>
 cudaError_t launch_fwd_mxfp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const FwdMxArgs& args, const WorkList& wl, int ctas, cudaStream_t stream) {
-  constexpr auto kernel = attn_fwd_mxfp8_kernel<CAUSAL, EMU, PS>;
+  constexpr auto kernel = attn_fwd_mxfp8_kernel<CAUSAL, EMU, PS, UKV>;
   // shared-memory opt-in and the setmaxnreg register check, once per device
   const cudaError_t e = kernel_ready<kernel>(MxCfg::kSmemBytes, MxCfg::kLaunchRegs);
   if (e != cudaSuccess) return e;

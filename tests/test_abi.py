@@ -225,3 +225,12 @@ def test_2cta_accepts_only_d128_non_causal(lib):
     assert f(causal=1) == 2 and f(d=64) == 2 and f(d=96) == 2
     assert f(scale=0.0) == 1 and f(causal=2) == 1
     assert f(b=0) == 0
+
+
+def test_mxfp8_unroll_kv_rejects_bad_arguments(lib):
+    A = 1 << 20
+    f = lambda d=128, causal=0, b=1, scale=0.1, q_sf=A * 2: lib.attn_fwd_mxfp8_unroll_kv(
+        A, q_sf, A * 3, A * 4, A * 5, A * 6, A * 7, A * 8, b, 2, 300, d, causal, scale, None)
+    assert f(d=64) == 2 and f(causal=2) == 1 and f(scale=-1.0) == 1
+    assert f(q_sf=A * 2 + 4) == 3
+    assert f(b=0) == 0

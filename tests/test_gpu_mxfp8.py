@@ -234,3 +234,33 @@ def test_full_size_workload_sampled(attn, p_scaling):
         o_ref, lse_ref = mx_reference(xq[b, h], xk[b, h], xv[b, h], w.causal, w.scale, rows=rows,
                                       p_scaling=p_scaling)
         check(o[b, h, rows], lse[b, h, rows], o_ref, lse_ref, f"{w.name} b={b} h={h}")
+
+
+# The unroll-KV schedule (attn_fwd_mxfp8_unroll_kv): the next item's first S
+# GEMM goes out in the current item's last key block, so shapes with several
+# items per CTA (causal and not) and a ragged tail exercise the item boundary.
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(1, 1, 128), (1, 2, 300), (2, 40, 1000), (1, 300, 512)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_unroll_kv_schedule(attn, shape, causal):
+    B, H, N = shape
+    xq, xk, xv = I.draw_fp32(B, H, N, 128, seed=N + H)
+    o, lse = run_mxfp8(attn, causal, xq, xk, xv, 128 ** -0.5, unroll_kv=True)
+    rng = np.random.default_rng(N)
+    heads = {(0, 0), (B - 1, H - 1), (int(rng.integers(B)), int(rng.integers(H)))}
+    for b, h in sorted(heads):
+        o_ref, lse_ref = mx_reference(xq[b, h], xk[b, h], xv[b, h], causal, 128 ** -0.5)
+        check(o[b, h], lse[b, h], o_ref, lse_ref, f"unroll-KV {shape} causal={causal} b={b} h={h}")
+    # every item was computed: no NaN anywhere
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+def test_unroll_kv_full_size_workload_sampled(attn):
+    w = I.MXFP8_CAUSAL
+    xq, xk, xv = I.draw_fp32(w.B, w.H, w.N, w.d, w.qk_std, w.v_std, w.seed)
+    o, lse = run_mxfp8(attn, w.causal, xq, xk, xv, w.scale, unroll_kv=True)
+    rng = np.random.default_rng(3)
+    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
+        rows = sample_rows(w.N, rng)
+        o_ref, lse_ref = mx_reference(xq[b, h], xk[b, h], xv[b, h], w.causal, w.scale, rows=rows)
+        check(o[b, h, rows], lse[b, h, rows], o_ref, lse_ref, f"unroll-KV {w.name} b={b} h={h}")
