@@ -285,6 +285,21 @@ attn_status_t attn_fwd_mxfp8_unroll_kv(const void* q8, const void* q_sf, const v
                                        int d, int causal, float scale, void* stream);
 
 /*
+ * attn_fwd_mxfp8_rescale_log -- attn_fwd_mxfp8_ex (P scaled per 32 keys from
+ * the block amax, MUFU exp2, any tau in [0, 16]) that also records every
+ * rescale decision in rescale_log, exactly as attn_fwd_rescale_log does for
+ * the bf16 kernel: device bytes [B, H, N, ceil(N/128)], bit 0 = the row's max
+ * moved at that key block, bit 1 = its warp rescaled O; bytes of blocks a
+ * tile does not stream are left as they were. A debugging variant of the same
+ * kernel. Errors as attn_fwd_mxfp8_ex, plus ATTN_ERR_INVALID_ARG for a null
+ * rescale_log on a non-empty problem.
+ */
+attn_status_t attn_fwd_mxfp8_rescale_log(const void* q8, const void* q_sf, const void* k8, const void* k_sf,
+                                         const void* v8, const void* v_sf, void* o, float* lse,
+                                         unsigned char* rescale_log, int B, int H, int N, int d, int causal,
+                                         float scale, float tau, void* stream);
+
+/*
  * attn_selftest_wait_timeout -- exercises the kernels' failure detection
  * without a fault: launches one small kernel on stream whose warps wait, with
  * the same bounded wait the attention kernels use, on barriers that nothing

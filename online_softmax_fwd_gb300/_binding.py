@@ -60,6 +60,9 @@ _SIGNATURES = {
     # q8, q_sf, k8, k_sf, v8, v_sf, o, lse, B, H, N, d, causal, scale, stream
     "attn_fwd_mxfp8_unroll_kv": ([ctypes.c_void_p] * 8 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_void_p],
                                  ctypes.c_int),
+    # q8, q_sf, k8, k_sf, v8, v_sf, o, lse, rescale_log, B, H, N, d, causal, scale, tau, stream
+    "attn_fwd_mxfp8_rescale_log": ([ctypes.c_void_p] * 9 + [ctypes.c_int] * 5
+                                   + [ctypes.c_float, ctypes.c_float, ctypes.c_void_p], ctypes.c_int),
     "attn_exp2_emulated": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p], ctypes.c_int),
     "attn_fwd_host_workspace_bytes": ([ctypes.c_int] * 4, ctypes.c_size_t),
     # q, k, v, o, lse (host), B, H, N, d, causal, scale, workspace, workspace_bytes, stream

@@ -279,7 +279,8 @@ attn_status_t fwd_bf16(const void* q, const void* k, const void* v, void* o, flo
 // unroll_kv selects the unroll-KV schedule (MUFU exp2, per-32-key amax P only).
 attn_status_t fwd_mxfp8(const void* q8, const void* q_sf, const void* k8, const void* k_sf, const void* v8,
                         const void* v_sf, void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
-                        float tau, int exp2_emu16, int p_scaling, bool unroll_kv, void* stream) {
+                        float tau, int exp2_emu16, int p_scaling, bool unroll_kv, uint8_t* rescale_log,
+                        void* stream) {
   if (B < 0 || H < 0 || N < 0 || (causal != 0 && causal != 1)) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(tau) || tau < 0.f || tau > 16.f) return ATTN_ERR_INVALID_ARG;
@@ -320,6 +321,7 @@ attn_status_t fwd_mxfp8(const void* q8, const void* q_sf, const void* k8, const 
   a.scale = scale;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.tau = tau;
+  a.rescale_log = rescale_log;
   const int sms = sm_count();
   if (sms <= 0) return ATTN_ERR_CUDA;
   // persistent grid with the same work-list schedule as the bf16 kernel
@@ -333,7 +335,9 @@ attn_status_t fwd_mxfp8(const void* q8, const void* q_sf, const void* k8, const 
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (unroll_kv)
+  if (rescale_log)
+    e = attn::launch_fwd_mxfp8_d128_log(causal, mq, mk, mv, a, wl, ctas, st);
+  else if (unroll_kv)
     e = attn::launch_fwd_mxfp8_d128_ukv(causal, mq, mk, mv, a, wl, ctas, st);
   else if (p_scaling == ATTN_P_SCALE_CONSTANT)
     e = attn::launch_fwd_mxfp8_d128_pconst(causal, exp2_emu16, mq, mk, mv, a, wl, ctas, st);
@@ -559,14 +563,23 @@ attn_status_t attn_fwd_mxfp8_ex(const void* q8, const void* q_sf, const void* k8
                                 const void* v_sf, void* o, float* lse, int B, int H, int N, int d, int causal,
                                 float scale, float tau, int exp2_emu16, int p_scaling, void* stream) {
   return fwd_mxfp8(q8, q_sf, k8, k_sf, v8, v_sf, o, lse, B, H, N, d, causal, scale, tau, exp2_emu16, p_scaling,
-                   false, stream);
+                   false, nullptr, stream);
+}
+
+attn_status_t attn_fwd_mxfp8_rescale_log(const void* q8, const void* q_sf, const void* k8, const void* k_sf,
+                                         const void* v8, const void* v_sf, void* o, float* lse,
+                                         unsigned char* rescale_log, int B, int H, int N, int d, int causal,
+                                         float scale, float tau, void* stream) {
+  if (B > 0 && H > 0 && N > 0 && !rescale_log) return ATTN_ERR_INVALID_ARG;
+  return fwd_mxfp8(q8, q_sf, k8, k_sf, v8, v_sf, o, lse, B, H, N, d, causal, scale, tau, 0, ATTN_P_SCALE_BLOCK_AMAX,
+                   false, rescale_log, stream);
 }
 
 attn_status_t attn_fwd_mxfp8_unroll_kv(const void* q8, const void* q_sf, const void* k8, const void* k_sf,
                                        const void* v8, const void* v_sf, void* o, float* lse, int B, int H, int N,
                                        int d, int causal, float scale, void* stream) {
   return fwd_mxfp8(q8, q_sf, k8, k_sf, v8, v_sf, o, lse, B, H, N, d, causal, scale, 0.0f, 0, ATTN_P_SCALE_BLOCK_AMAX,
-                   true, stream);
+                   true, nullptr, stream);
 }
 
 attn_status_t attn_fwd_mxfp8(const void* q8, const void* q_sf, const void* k8, const void* k_sf, const void* v8,

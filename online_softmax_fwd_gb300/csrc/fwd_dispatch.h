@@ -43,6 +43,9 @@ cudaError_t launch_fwd_mxfp8_d128_pconst_e5m2(int causal, int emu16, const CUten
 // the unroll-KV schedule (fwd_mxfp8_ukv.cu)
 cudaError_t launch_fwd_mxfp8_d128_ukv(int causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                       const FwdMxArgs& a, const WorkList& wl, int ctas, cudaStream_t s);
+// the rescale-logging instantiations (fwd_mxfp8_log.cu)
+cudaError_t launch_fwd_mxfp8_d128_log(int causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                      const FwdMxArgs& a, const WorkList& wl, int ctas, cudaStream_t s);
 // the bounded-wait self-test (selftest.cu)
 cudaError_t launch_wait_timeout_selftest(unsigned int* status, long long limit_cycles, cudaStream_t stream);
 

@@ -58,6 +58,8 @@ struct FwdMxArgs {
   float scale;
   float scale_log2;
   float tau;
+  // rescale log (the LOG instantiations only, else null): as FwdArgs's
+  uint8_t* rescale_log;
 };
 
 struct MxCfg {
@@ -100,7 +102,8 @@ struct MxCfg {
 // needed O correction then loads O in 32-column parts). Measured slower on
 // this kernel (its softmax warps run the epilogue, which hides the boundary
 // wait anyway); kept as an opt-in schedule.
-template <bool CAUSAL, int EMU, int PS, bool UKV = false>
+// LOG writes each row's rescale decision per key block (see FwdArgs).
+template <bool CAUSAL, int EMU, int PS, bool UKV = false, bool LOG = false>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_mxfp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const FwdMxArgs args,
@@ -511,7 +514,13 @@ __global__ void __launch_bounds__(384, 1)
       tmem_st1(s_tm + C::kPScale + quad, sfw);  // row r's scales at column r / 32
       // correction of O once the scores are dead; lands before P is handed
       // over
-      if (j > 0 && __any_sync(0xffffffffu, fire)) {
+      const bool warp_rescales = j > 0 && __any_sync(0xffffffffu, fire);
+      if constexpr (LOG) {
+        if (grow < args.n)
+          args.rescale_log[(static_cast<size_t>(bh) * args.n + grow) * nkv + j] =
+              static_cast<uint8_t>((fire ? 1u : 0u) | (warp_rescales ? 2u : 0u));
+      }
+      if (warp_rescales) {
         const float2 corr_2 = make_float2(corr, corr);
         if constexpr (UKV) {
           // 32 columns at a time (P stays in registers for the sum)
@@ -611,10 +620,10 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <bool CAUSAL, int EMU, int PS, bool UKV = false>
+template <bool CAUSAL, int EMU, int PS, bool UKV = false, bool LOG = false>
 cudaError_t launch_fwd_mxfp8(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const FwdMxArgs& args, const WorkList& wl, int ctas, cudaStream_t stream) {
-  constexpr auto kernel = attn_fwd_mxfp8_kernel<CAUSAL, EMU, PS, UKV>;
+  constexpr auto kernel = attn_fwd_mxfp8_kernel<CAUSAL, EMU, PS, UKV, LOG>;
   // shared-memory opt-in and the setmaxnreg register check, once per device
   const cudaError_t e = kernel_ready<kernel>(MxCfg::kSmemBytes, MxCfg::kLaunchRegs);
   if (e != cudaSuccess) return e;

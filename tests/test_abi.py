@@ -234,3 +234,13 @@ def test_mxfp8_unroll_kv_rejects_bad_arguments(lib):
     assert f(d=64) == 2 and f(causal=2) == 1 and f(scale=-1.0) == 1
     assert f(q_sf=A * 2 + 4) == 3
     assert f(b=0) == 0
+
+
+def test_mxfp8_rescale_log_rejects_bad_arguments(lib):
+    A = 1 << 20
+    f = lambda log=A * 9, tau=0.0, b=1, d=128: lib.attn_fwd_mxfp8_rescale_log(
+        A, A * 2, A * 3, A * 4, A * 5, A * 6, A * 7, A * 8, log, b, 2, 256, d, 0, 0.1, tau, None)
+    assert f(log=0) == 1
+    assert f(tau=-1.0) == 1 and f(tau=17.0) == 1
+    assert f(d=64) == 2
+    assert f(log=0, b=0) == 0

@@ -5,7 +5,9 @@ raises it by at most tau (log2 units of the scaled score), else move it; a
 warp rescales O when any of its 32 rows moved (block > 0).
 
 attn_fwd_rescale_log writes the decisions of the same kernel as attn_fwd
-(bit 0: the row moved its max, bit 1: its warp rescaled O). The oracle's
+(bit 0: the row moved its max, bit 1: its warp rescaled O), and
+attn_fwd_mxfp8_rescale_log those of the MXFP8 kernel (checked against the
+recurrence on the dequantised inputs). The oracle's
 blockwise recurrence gives the row decisions in float64 (``fired``) and the
 reference max of every block. A decision whose growth lies within the fp32
 error of the scores of tau can go either way in fp32; such a decision and the
@@ -170,3 +172,52 @@ def test_a_tie_at_tau_zero_does_not_move_the_max(attn):
         run = np.maximum.accumulate(bm, axis=1)
         ties += int((bm[:, 1:] == run[:, :-1]).sum())
     assert ties > 100   # the case is exercised
+
+
+# The MXFP8 kernel: the same rule on the scores of the quantised inputs. The
+# oracle's decisions come from the float64 recurrence on the dequantised Q
+# and K (the values the block-scaled products multiply).
+def mx_run_log(attn, xq, xk, xv, causal, scale, tau):
+    import ctypes
+    from test_gpu_mxfp8 import quantize_gpu
+    q8, q_sf = quantize_gpu(attn, xq, 0)
+    k8, k_sf = quantize_gpu(attn, xk, 0)
+    v8, v_sf = quantize_gpu(attn, xv, 1)
+    B, H, N, d = xq.shape
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=DEV)
+    log = torch.zeros((B, H, N, (N + 127) // 128), dtype=torch.uint8, device=DEV)
+    st = attn.lib().attn_fwd_mxfp8_rescale_log(*(t.data_ptr() for t in (q8, q_sf, k8, k_sf, v8, v_sf, o, lse, log)),
+                                               B, H, N, d, int(causal), scale, tau, None)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert attn.device_status() == attn.Status.OK
+    # O and LSE as the product kernel's (attn_fwd_mxfp8_ex with the same tau)
+    o2, lse2 = attn.attn_fwd_mxfp8(q8, q_sf, k8, k_sf, v8, v_sf, causal=causal, scale=scale, tau=tau)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    return log.cpu().numpy()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("tau", [0.0, 8.0])
+@pytest.mark.parametrize("inputs", ["ramp", "qk_std2"])
+def test_mxfp8_rescale_decisions_match_the_rule(attn, inputs, tau, causal):
+    from oracle.mxfp8 import quantize_blocks
+    if inputs == "ramp":
+        xq, xk, xv = I.draw_fp32(1, 2, 1024, 128, seed=13)
+        xq += 1.0
+        xk += np.linspace(0.0, 1.5, 1024, dtype=np.float32)[None, None, :, None]
+    else:
+        xq, xk, xv = I.draw_fp32(1, 2, 1536, 128, qk_std=2.0, seed=9)
+    scale = 128 ** -0.5
+    log = mx_run_log(attn, xq, xk, xv, causal, scale, tau)
+    totals = {"decisions": 0, "left_out": 0, "row_moves": 0, "warp_rescales": 0}
+    for h in range(xq.shape[1]):
+        qd = quantize_blocks(xq[0, h].astype(np.float64))[2]
+        kd = quantize_blocks(xk[0, h].astype(np.float64))[2]
+        st = check_head(log[0, h], qd, kd, causal, scale, tau, f"mxfp8 {inputs} tau={tau} causal={causal} h={h}")
+        totals = {kk: totals[kk] + st[kk] for kk in totals}
+    print(f"mxfp8 rescale log {inputs} tau={tau} causal={causal}: {totals}")
+    assert totals["left_out"] <= 0.01 * totals["decisions"]
+    assert totals["row_moves"] > 0
