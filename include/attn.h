@@ -116,7 +116,8 @@ attn_status_t attn_fwd_2cta(const void* q, const void* k, const void* v, void* o
  * otherwise; a warp rescales its O rows when any of its 32 rows moved.
  *
  *   rescale_log  device bytes [B, H, N, ceil(N/128)] (128-key blocks), owned
- *                by the caller. The kernel writes byte (b, h, i, j) for every
+ *                by the caller; rescale_log_bytes is its size (at least
+ *                B*H*N*ceil(N/128), else ATTN_ERR_INVALID_ARG). The kernel writes byte (b, h, i, j) for every
  *                key block j that row i's query tile streams: bit 0 = row i's
  *                running max moved at block j (always set at block 0, where
  *                the max starts at -inf), bit 1 = the row's warp (rows
@@ -125,12 +126,12 @@ attn_status_t attn_fwd_2cta(const void* q, const void* k, const void* v, void* o
  *                blocks past its diagonal block) are left as they were.
  * A slower debugging variant of the same kernel (the extra stores sit in the
  * softmax loop); O and LSE are the same as attn_fwd_ex's. Errors as
- * attn_fwd_ex, plus ATTN_ERR_INVALID_ARG for a null rescale_log on a
- * non-empty problem.
+ * attn_fwd_ex, plus ATTN_ERR_INVALID_ARG for a null or too small rescale_log
+ * on a non-empty problem.
  */
 attn_status_t attn_fwd_rescale_log(const void* q, const void* k, const void* v, void* o, float* lse,
-                                   unsigned char* rescale_log, int B, int H, int N, int d, int causal, float scale,
-                                   float tau, void* stream);
+                                   unsigned char* rescale_log, size_t rescale_log_bytes, int B, int H, int N, int d,
+                                   int causal, float scale, float tau, void* stream);
 
 /*
  * attn_fwd_host -- attn_fwd with Q, K, V, O and LSE in HOST memory.
@@ -288,16 +289,17 @@ attn_status_t attn_fwd_mxfp8_unroll_kv(const void* q8, const void* q_sf, const v
  * attn_fwd_mxfp8_rescale_log -- attn_fwd_mxfp8_ex (P scaled per 32 keys from
  * the block amax, MUFU exp2, any tau in [0, 16]) that also records every
  * rescale decision in rescale_log, exactly as attn_fwd_rescale_log does for
- * the bf16 kernel: device bytes [B, H, N, ceil(N/128)], bit 0 = the row's max
- * moved at that key block, bit 1 = its warp rescaled O; bytes of blocks a
- * tile does not stream are left as they were. A debugging variant of the same
- * kernel. Errors as attn_fwd_mxfp8_ex, plus ATTN_ERR_INVALID_ARG for a null
- * rescale_log on a non-empty problem.
+ * the bf16 kernel: device bytes [B, H, N, ceil(N/128)] (rescale_log_bytes at
+ * least that), bit 0 = the row's max moved at that key block, bit 1 = its warp
+ * rescaled O; bytes of blocks a tile does not stream are left as they were. A
+ * debugging variant of the same kernel. Errors as attn_fwd_mxfp8_ex, plus
+ * ATTN_ERR_INVALID_ARG for a null or too small rescale_log on a non-empty
+ * problem.
  */
 attn_status_t attn_fwd_mxfp8_rescale_log(const void* q8, const void* q_sf, const void* k8, const void* k_sf,
                                          const void* v8, const void* v_sf, void* o, float* lse,
-                                         unsigned char* rescale_log, int B, int H, int N, int d, int causal,
-                                         float scale, float tau, void* stream);
+                                         unsigned char* rescale_log, size_t rescale_log_bytes, int B, int H, int N,
+                                         int d, int causal, float scale, float tau, void* stream);
 
 /*
  * attn_selftest_wait_timeout -- exercises the kernels' failure detection

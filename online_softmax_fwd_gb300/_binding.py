@@ -45,8 +45,8 @@ _SIGNATURES = {
                     + [ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
     # q, k, v, o, lse, B, H, N, d, causal, scale, stream
     "attn_fwd_2cta": ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_void_p], ctypes.c_int),
-    # q, k, v, o, lse, rescale_log, B, H, N, d, causal, scale, tau, stream
-    "attn_fwd_rescale_log": ([ctypes.c_void_p] * 6 + [ctypes.c_int] * 5
+    # q, k, v, o, lse, rescale_log, rescale_log_bytes, B, H, N, d, causal, scale, tau, stream
+    "attn_fwd_rescale_log": ([ctypes.c_void_p] * 6 + [ctypes.c_size_t] + [ctypes.c_int] * 5
                              + [ctypes.c_float, ctypes.c_float, ctypes.c_void_p], ctypes.c_int),
     "attn_mxfp8_scale_bytes": ([ctypes.c_int] * 4, ctypes.c_size_t),
     # x, x_e4m3, x_scales, B, H, N, d, role, stream
@@ -60,8 +60,8 @@ _SIGNATURES = {
     # q8, q_sf, k8, k_sf, v8, v_sf, o, lse, B, H, N, d, causal, scale, stream
     "attn_fwd_mxfp8_unroll_kv": ([ctypes.c_void_p] * 8 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_void_p],
                                  ctypes.c_int),
-    # q8, q_sf, k8, k_sf, v8, v_sf, o, lse, rescale_log, B, H, N, d, causal, scale, tau, stream
-    "attn_fwd_mxfp8_rescale_log": ([ctypes.c_void_p] * 9 + [ctypes.c_int] * 5
+    # q8, q_sf, k8, k_sf, v8, v_sf, o, lse, rescale_log, rescale_log_bytes, B, H, N, d, causal, scale, tau, stream
+    "attn_fwd_mxfp8_rescale_log": ([ctypes.c_void_p] * 9 + [ctypes.c_size_t] + [ctypes.c_int] * 5
                                    + [ctypes.c_float, ctypes.c_float, ctypes.c_void_p], ctypes.c_int),
     "attn_exp2_emulated": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p], ctypes.c_int),
     "attn_fwd_host_workspace_bytes": ([ctypes.c_int] * 4, ctypes.c_size_t),
@@ -198,8 +198,8 @@ def attn_fwd_rescale_log(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, caus
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     log = torch.zeros((B, H, N, (N + 127) // 128), dtype=torch.uint8, device=q.device)
     with torch.cuda.device(q.device):
-        st = lib().attn_fwd_rescale_log(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(log), B, H, N, d,
-                                        int(bool(causal)), float(scale), float(tau), _stream_handle(stream))
+        st = lib().attn_fwd_rescale_log(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(log), log.numel(), B, H,
+                                        N, d, int(bool(causal)), float(scale), float(tau), _stream_handle(stream))
         _check(st, "attn_fwd_rescale_log")
     return o, lse, log
 

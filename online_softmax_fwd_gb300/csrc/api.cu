@@ -185,6 +185,12 @@ int pair_count() {
   return n;
 }
 
+// Bytes of a rescale log: one per (head, row, 128-key block).
+size_t rescale_log_size(int B, int H, int N) {
+  if (B <= 0 || H <= 0 || N <= 0) return 0;
+  return static_cast<size_t>(B) * H * N * ((static_cast<size_t>(N) + 127) / 128);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 long long band_for(long long kv_head_bytes, long long bh) {
@@ -399,12 +405,12 @@ attn_status_t attn_fwd_2cta(const void* q, const void* k, const void* v, void* o
 }
 
 attn_status_t attn_fwd_rescale_log(const void* q, const void* k, const void* v, void* o, float* lse,
-                                   unsigned char* rescale_log, int B, int H, int N, int d, int causal, float scale,
-                                   float tau, void* stream) {
+                                   unsigned char* rescale_log, size_t rescale_log_bytes, int B, int H, int N, int d,
+                                   int causal, float scale, float tau, void* stream) {
   bool empty = false;
   const attn_status_t st = check_fwd_args(q, k, v, o, lse, B, H, N, d, causal, scale, tau, 0, &empty);
   if (st != ATTN_OK || empty) return st;
-  if (!rescale_log) return ATTN_ERR_INVALID_ARG;
+  if (!rescale_log || rescale_log_bytes < rescale_log_size(B, H, N)) return ATTN_ERR_INVALID_ARG;
   return fwd_bf16(q, k, v, o, lse, rescale_log, B, H, N, d, causal, scale, tau, 0, stream);
 }
 
@@ -568,9 +574,10 @@ attn_status_t attn_fwd_mxfp8_ex(const void* q8, const void* q_sf, const void* k8
 
 attn_status_t attn_fwd_mxfp8_rescale_log(const void* q8, const void* q_sf, const void* k8, const void* k_sf,
                                          const void* v8, const void* v_sf, void* o, float* lse,
-                                         unsigned char* rescale_log, int B, int H, int N, int d, int causal,
-                                         float scale, float tau, void* stream) {
-  if (B > 0 && H > 0 && N > 0 && !rescale_log) return ATTN_ERR_INVALID_ARG;
+                                         unsigned char* rescale_log, size_t rescale_log_bytes, int B, int H, int N,
+                                         int d, int causal, float scale, float tau, void* stream) {
+  if (B > 0 && H > 0 && N > 0 && (!rescale_log || rescale_log_bytes < rescale_log_size(B, H, N)))
+    return ATTN_ERR_INVALID_ARG;
   return fwd_mxfp8(q8, q_sf, k8, k_sf, v8, v_sf, o, lse, B, H, N, d, causal, scale, tau, 0, ATTN_P_SCALE_BLOCK_AMAX,
                    false, rescale_log, stream);
 }

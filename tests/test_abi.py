@@ -210,9 +210,11 @@ def test_quantize_roles(lib):
 
 def test_rescale_log_rejects_bad_arguments(lib):
     A = 1 << 20
-    f = lambda log=A * 6, tau=8.0, b=1, d=64: lib.attn_fwd_rescale_log(A, A * 2, A * 3, A * 4, A * 5, log, b, 2, 256,
-                                                                        d, 0, 0.125, tau, None)
+    need = 1 * 2 * 256 * 2              # B H N ceil(N / 128)
+    f = lambda log=A * 6, tau=8.0, b=1, d=64, nbytes=need: lib.attn_fwd_rescale_log(
+        A, A * 2, A * 3, A * 4, A * 5, log, nbytes, b, 2, 256, d, 0, 0.125, tau, None)
     assert f(log=0) == 1                # the log is required
+    assert f(nbytes=need - 1) == 1      # and must hold one byte per (head, row, key block)
     assert f(tau=-1.0) == 1 and f(tau=17.0) == 1
     assert f(d=96) == 2
     assert f(log=0, b=0) == 0           # empty problem: nothing to do, nothing checked
@@ -238,9 +240,11 @@ def test_mxfp8_unroll_kv_rejects_bad_arguments(lib):
 
 def test_mxfp8_rescale_log_rejects_bad_arguments(lib):
     A = 1 << 20
-    f = lambda log=A * 9, tau=0.0, b=1, d=128: lib.attn_fwd_mxfp8_rescale_log(
-        A, A * 2, A * 3, A * 4, A * 5, A * 6, A * 7, A * 8, log, b, 2, 256, d, 0, 0.1, tau, None)
+    need = 1 * 2 * 256 * 2
+    f = lambda log=A * 9, tau=0.0, b=1, d=128, nbytes=need: lib.attn_fwd_mxfp8_rescale_log(
+        A, A * 2, A * 3, A * 4, A * 5, A * 6, A * 7, A * 8, log, nbytes, b, 2, 256, d, 0, 0.1, tau, None)
     assert f(log=0) == 1
+    assert f(nbytes=need - 1) == 1
     assert f(tau=-1.0) == 1 and f(tau=17.0) == 1
     assert f(d=64) == 2
     assert f(log=0, b=0) == 0

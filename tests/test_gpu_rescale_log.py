@@ -188,7 +188,7 @@ def mx_run_log(attn, xq, xk, xv, causal, scale, tau):
     lse = torch.empty((B, H, N), dtype=torch.float32, device=DEV)
     log = torch.zeros((B, H, N, (N + 127) // 128), dtype=torch.uint8, device=DEV)
     st = attn.lib().attn_fwd_mxfp8_rescale_log(*(t.data_ptr() for t in (q8, q_sf, k8, k_sf, v8, v_sf, o, lse, log)),
-                                               B, H, N, d, int(causal), scale, tau, None)
+                                               log.numel(), B, H, N, d, int(causal), scale, tau, None)
     assert st == 0
     torch.cuda.synchronize()
     assert attn.device_status() == attn.Status.OK
