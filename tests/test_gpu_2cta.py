@@ -105,3 +105,23 @@ def test_full_size_workload_sampled(attn):
                            I.as_f64(k[b, h])[None, None], I.as_f64(v[b, h])[None, None], False, w.scale, 8.0,
                            f"2cta {w.name} b={b} h={h}", rows=rows)
         assert st["o_over_1e-2"] == 0
+
+
+def test_bit_identical_to_one_cta_kernel_many_shapes_and_repeats(attn):
+    # CTA 1 hands P to CTA 0 with a relaxed remote arrive (its data is TMEM,
+    # ordered by the tcgen05 fences): a missed ordering would show up as a
+    # product reading stale P, i.e. an output that differs from the one-CTA
+    # kernel's. Many shapes (ragged tails, several items per pair, peaked
+    # rows), each run three times.
+    rng = np.random.default_rng(11)
+    shapes = [(1, 1, 200, 128), (2, 3, 777, 128), (1, 24, 1536, 128), (4, 8, 1024, 128), (1, 150, 512, 128),
+              (2, 16, 2048, 128)]
+    for i, (B, H, N, d) in enumerate(shapes):
+        qk_std = 2.0 if i % 2 else 1.0
+        q, k, v = (I.to_bf16(x).to(DEV) for x in I.draw_fp32(B, H, N, d, qk_std=qk_std, seed=int(rng.integers(1000))))
+        o1, l1 = attn.attn_fwd(q, k, v)
+        for _ in range(3):
+            o2, l2 = attn.attn_fwd_2cta(q, k, v)
+            torch.cuda.synchronize()
+            assert torch.equal(o1, o2) and torch.equal(l1, l2), f"{(B, H, N, d)}: 2-CTA output differs"
+    assert attn.device_status() == attn.Status.OK
