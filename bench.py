@@ -728,11 +728,14 @@ def peak_for(w: I.Workload) -> tuple[float, str]:
     return bf16_peak, src
 
 
-def roofline_of(w: I.Workload, launch_ms: list[float], kernel: str | None = None) -> dict:
+def roofline_of(w: I.Workload, launch_ms: list[float], kernel: str | None = None, variant: str = "") -> dict:
+    """Roofline of the timed kernel; ``variant`` ("_2cta", "_unroll_kv") names a
+    kernel other than the workload's default, whose DRAM traffic comes from its
+    own launch list (None if it has none)."""
     peak, src = peak_for(w)
     achieved = w.flops / (float(np.mean(launch_ms)) * 1e-3) / 1e12
     return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "traffic": profiled_traffic(w.name), "peak_source": src, "flop_per_launch": w.flops,
+            "traffic": profiled_traffic(w.name + variant), "peak_source": src, "flop_per_launch": w.flops,
             "kernel": kernel or KERNEL_NAMES[(w.direction, w.dtype)]}
 
 
@@ -775,7 +778,8 @@ def sub_record(attn, w: I.Workload, dev, world: int, opts, steps: int, warmup: i
            else w.flops * world / (launch_mean * 1e-3) / 1e12,
            "unit": UNIT, "ms_per_step": per_step_ms if flush is None else launch_mean,
            "kernel_ms": kernel_ms_of(m["launch_ms"]),
-           "roofline": roofline_of(w, m["launch_ms"], "attn_fwd_bf16_2cta_kernel" if opts.two_cta else None),
+           "roofline": roofline_of(w, m["launch_ms"], "attn_fwd_bf16_2cta_kernel" if opts.two_cta else None,
+                                   "_2cta" if opts.two_cta else "_unroll_kv" if opts.unroll_kv else ""),
            "clocks": m["clocks"], "gpu_launches": steps * step.launches}
     if w.dtype == "mxfp8" and w.direction == "fwd":
         rec["config"]["p_scaling"] = ["block_amax", "constant_2^-8", "constant_2^-8_e5m2"][opts.p_scaling]
@@ -833,7 +837,8 @@ def bench_ours(args, w: I.Workload, world: int, rank: int, local: int) -> None:
     value = w.flops * args.steps * world / (region_ms_max * 1e-3) / 1e12
 
     e2e = None if args.no_e2e else step.e2e(dev, max(3, min(args.steps, 10)), world)
-    roofline = roofline_of(w, launch_ms, "attn_fwd_bf16_2cta_kernel" if args.two_cta else None)
+    roofline = roofline_of(w, launch_ms, "attn_fwd_bf16_2cta_kernel" if args.two_cta else None,
+                           "_2cta" if args.two_cta else "_unroll_kv" if args.unroll_kv else "")
 
     cpu = None
     threads, threads_src = oracle_threads()
