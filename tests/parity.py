@@ -73,12 +73,15 @@ def compare(o, lse, o_ref, lse_ref, what: str = "", max_gate: bool = True, mean_
     """Assert the gate against the exact oracle; returns the statistics.
 
     ``method`` = (o_m, delta), the method at the kernel's precision and its
-    bound (``method_reference``), adds the method's floor: an element where
-    RN_bf16(o_m), the result of the method itself, lies more than 1e-2 from
-    O_ref is gated at |O - o_m| <= delta + half an ulp instead of 1e-2 (with a
-    lagging max the bf16 rounding of the dominant P is the method's own error,
-    up to 2^-9 |V|, on top of the output's half ulp). ``max_gate=False`` only
-    reports the elementwise figures."""
+    bound (``method_reference``), adds the method's floor. The kernel may land
+    anywhere in o_m +- delta before its output is rounded to bf16, so every
+    output the method admits lies within delta + half an ulp of o_m. An
+    element where some of those outputs lie more than 1e-2 from O_ref
+    (|o_m - O_ref| + delta + half an ulp > 1e-2) is gated at |O - o_m| <=
+    delta + half an ulp instead of 1e-2: with a lagging max the bf16 rounding
+    of the dominant P is the method's own error, up to 2^-9 |V|, and the
+    output's half ulp comes on top of it. ``max_gate=False`` only reports the
+    elementwise figures."""
     o = np.asarray(o, dtype=np.float64)
     o_ref = np.asarray(o_ref, dtype=np.float64)
     err = np.abs(o - o_ref)
@@ -90,8 +93,8 @@ def compare(o, lse, o_ref, lse_ref, what: str = "", max_gate: bool = True, mean_
     mexc = np.zeros_like(exc)
     if method is not None:
         o_m, delta = (np.asarray(x, dtype=np.float64) for x in method)
-        mexc = (np.abs(bf16_rn(o_m) - o_ref) > O_MAX_ABS) & ~exc
         mbound = delta + 0.5 * bf16_ulp(np.abs(o_m) + delta)
+        mexc = (np.abs(o_m - o_ref) + mbound > O_MAX_ABS) & ~exc
         ok_exc = ok_exc | ((exc | mexc) & (np.abs(o - o_m) <= mbound))
     lerr = np.abs(np.asarray(lse, dtype=np.float64) - np.asarray(lse_ref, dtype=np.float64))
     plain = ~(exc | mexc)
@@ -119,7 +122,8 @@ def compare(o, lse, o_ref, lse_ref, what: str = "", max_gate: bool = True, mean_
 
 
 def compare_heads(o, lse, o_ref, lse_ref, q, k, v, causal: bool, scale: float, tau: float = 8.0,
-                  what: str = "", rows=None, mean_gate: bool = True, exp_rel_err: float = 2.0 ** -21) -> dict:
+                  what: str = "", rows=None, mean_gate: bool = True, exp_rel_err: float = 2.0 ** -21,
+                  block: int = 128) -> dict:
     """``compare`` over [B, H, R, dv] outputs with the method's floor computed
     where it is needed: for every head with an element more than 1e-2 from
     O_ref (beyond its output-rounding floor), the method at the kernel's
@@ -127,7 +131,8 @@ def compare_heads(o, lse, o_ref, lse_ref, q, k, v, causal: bool, scale: float, t
     positions ``rows``, default 0 .. R-1; k, v [B, H, N, *]) and the element is
     held to it. Heads without such an element are gated by the flat 1e-2.
     ``exp_rel_err`` is the relative error of the kernel's exp2 (the MUFU's by
-    default; the software exp2's 8.77e-5 when a share of it is used)."""
+    default; the software exp2's 8.77e-5 when a share of it is used);
+    ``block`` the keys per block of the kernel's recurrence."""
     o = np.asarray(o, dtype=np.float64)
     o_ref = np.asarray(o_ref, dtype=np.float64)
     err = np.abs(o - o_ref)
@@ -139,7 +144,7 @@ def compare_heads(o, lse, o_ref, lse_ref, q, k, v, causal: bool, scale: float, t
     heads = np.argwhere(suspect.any(axis=(2, 3)))
     for b, h in heads:
         o_m[b, h], _, delta[b, h], _, _ = method_reference(q[b, h], k[b, h], v[b, h], causal, scale, tau,
-                                                           exp_rel_err=exp_rel_err, row_index=rows)
+                                                           exp_rel_err=exp_rel_err, block=block, row_index=rows)
     st = compare(o, lse, o_ref, lse_ref, what, mean_gate=mean_gate, method=(o_m, delta))
     st["heads_with_method_floor"] = int(len(heads))
     return st

@@ -18,7 +18,7 @@ import numpy as np
 import pytest
 
 from oracle.attention import attention_fwd
-from parity import bf16_rn, compare, compare_method, method_reference
+from parity import bf16_rn, bf16_ulp, compare, compare_method, method_reference
 
 LOG2E = 1.0 / math.log(2.0)
 
@@ -168,3 +168,35 @@ def test_method_floor_exempts_only_what_the_method_itself_misses():
     bad[tuple(i)] += 2 * 2.0 ** (np.floor(np.log2(abs(bad[tuple(i)]))) - 7) * np.sign(bad[tuple(i)])
     with pytest.raises(AssertionError):
         compare(bad, lse_m, o_ref, lse_ref, "two steps off the method", method=(o_m, delta))
+
+
+def test_method_floor_covers_the_band_the_method_admits():
+    # An element whose method result rounds to within 1e-2 of the exact one,
+    # while the method's band (o_m +- delta, then the bf16 rounding) reaches
+    # past 1e-2: the other bf16 neighbour, inside the band, is an output the
+    # method's arithmetic admits and passes; two steps further out it fails.
+    q, k, v = _peaked(n=640, d=64, qk_std=2.0, seed=0)
+    scale = 0.37
+    o_ref, lse_ref = attention_fwd(q[None, None], k[None, None], v[None, None], True, scale)
+    o_ref, lse_ref = o_ref[0, 0], lse_ref[0, 0]
+    o_m, lse_m, delta, _, suspect = method_reference(q, k, v, True, scale, 8.0)
+    mbound = delta + 0.5 * bf16_ulp(np.abs(o_m) + delta)
+    rnd = bf16_rn(o_m)
+    step = bf16_ulp(np.abs(rnd))
+    away = rnd + np.sign(rnd - o_ref) * step            # the neighbour away from O_ref
+    band_only = ((np.abs(rnd - o_ref) <= 1e-2) & (np.abs(o_m - o_ref) + mbound > 1e-2)
+                 & (np.abs(away - o_m) <= mbound) & (np.abs(away - o_ref) > 1e-2) & ~suspect[:, None]
+                 & (np.abs(bf16_rn(o_ref) - o_ref) <= 1e-2))
+    i = tuple(np.argwhere(band_only)[0])
+    # the method's own output is within 1e-2 there, the neighbour is not
+    assert abs(rnd[i] - o_ref[i]) <= 1e-2 < abs(away[i] - o_ref[i])
+    base = compare(rnd, lse_m, o_ref, lse_ref, "method output", method=(o_m, delta))
+    out = rnd.copy()
+    out[i] = away[i]
+    st = compare(out, lse_m, o_ref, lse_ref, "band element", method=(o_m, delta))
+    assert st["exceptions_failed"] == 0 and st["o_over_1e-2_floor_ok"] == 0
+    assert st["o_over_1e-2"] == base["o_over_1e-2"] + 1
+    far = out.copy()
+    far[i] = away[i] + 2 * np.sign(rnd[i] - o_ref[i]) * step[i]
+    with pytest.raises(AssertionError):
+        compare(far, lse_m, o_ref, lse_ref, "two steps past the band element", method=(o_m, delta))
