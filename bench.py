@@ -898,6 +898,8 @@ def main() -> None:
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
     ap.add_argument("--shape", default=None,
                     help="B,H,N,d[,causal[,mxfp8[,bwd]]] instead of a named workload (profiling a smaller case)")
+    ap.add_argument("--qk-std", type=float, default=1.0,
+                    help="standard deviation of Q and K for --shape (the causal d128 workload uses 2)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--exp2-emu16", type=int, default=0)
     ap.add_argument("--tau", type=float, default=None,
@@ -929,8 +931,8 @@ def main() -> None:
         dt = "mxfp8" if len(f) > 5 and f[5] else "bf16"
         direction = "bwd" if len(f) > 6 and f[6] else "fwd"
         w = I.Workload(f"custom_b{f[0]}h{f[1]}n{f[2]}d{f[3]}{'_causal' if causal else ''}{'_mxfp8' if dt == 'mxfp8' else ''}"
-                       f"{'_bwd' if direction == 'bwd' else ''}", f[0], f[1], f[2], f[3], causal, dtype=dt,
-                       direction=direction)
+                       f"{'_bwd' if direction == 'bwd' else ''}{f'_qk{args.qk_std:g}' if args.qk_std != 1.0 else ''}",
+                       f[0], f[1], f[2], f[3], causal, dtype=dt, direction=direction, qk_std=args.qk_std)
     world, rank, local = dist_setup(args.gpus)
     try:
         if args.impl == "reference":
