@@ -8,7 +8,8 @@ or execute anything in this package; the library under
 Modules
   attention      one-shot softmax(Q K^T s) V and LSE (the definition), plus the
                  blockwise online recurrence used only to check the definition
-                 against the identities the pages state.
+                 against the identities the pages state, and the exact merge of
+                 (O, LSE) results over disjoint key sets.
   exp2_model     the accuracy statistics of a software exp2 (the columns the
                  page prints) and a bf16 rounding from the value itself.
   cmodel         ctypes loader for ``exp2_model.c``: the software exp2 (range

@@ -221,3 +221,33 @@ def lse_combine(m_a: np.ndarray, l_a: np.ndarray, m_b: np.ndarray, l_b: np.ndarr
     "Combining two blocks exactly")."""
     m = np.maximum(m_a, m_b)
     return m, np.exp(m_a - m) * l_a + np.exp(m_b - m) * l_b
+
+
+def combine_partials(o_parts: np.ndarray, lse_parts: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """Merge attention results computed over disjoint sets of keys into the
+    result over their union, float64.
+
+    o_parts [P, ..., R, dv]: each part's normalised output O_p; lse_parts
+    [P, ..., R]: its log-sum-exp LSE_p = m_p + ln l_p of the scaled scores.
+    "Lecture 2 - Online Softmax and Numerical Correctness", section "Combining
+    two blocks exactly": the merged max is m = max_p m_p and the merged sum is
+    l = sum_p exp(m_p - m) l_p. Each part enters with the statistics
+    (m_p, l_p) = (LSE_p, 1), which have the same log-sum-exp, so l = sum_p
+    exp(LSE_p - m), LSE = m + ln l, and the merged numerator sum_p exp(m_p - m)
+    l_p O_p divided by l gives O. A part with LSE_p = -inf (no keys) adds
+    nothing; a row whose parts are all -inf gets O = 0 and LSE = -inf.
+    """
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    if o_parts.shape[:-1] != lse_parts.shape:
+        raise ValueError(f"bad shapes o{o_parts.shape} lse{lse_parts.shape}")
+    m = lse_parts.max(axis=0)
+    live = np.isfinite(m)
+    w = np.exp(lse_parts - np.where(live, m, 0.0))        # exp(m_p - m) l_p with l_p = 1
+    l = w.sum(axis=0)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        o = (w[..., None] * o_parts).sum(axis=0) / l[..., None]
+        lse = m + np.log(l)
+    o = np.where(live[..., None], o, 0.0)
+    lse = np.where(live, lse, -np.inf)
+    return o, lse

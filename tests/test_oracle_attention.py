@@ -159,6 +159,63 @@ def test_lse_combine_two_halves():
     assert np.max(np.abs(m + np.log(l) - full)) < 1e-14
 
 
+def test_combine_partials_equals_one_shot():
+    # attention over uneven key ranges, merged, is attention over all keys
+    rng = np.random.default_rng(21)
+    q, k, v = (rng.standard_normal((2, 3, 40, 16)) * 2.0 for _ in range(3))
+    s = 0.3
+    cuts = [0, 7, 26, 29, 40]
+    parts = [A.attention_fwd(q, k[:, :, a:b], v[:, :, a:b], False, s) for a, b in zip(cuts[:-1], cuts[1:])]
+    o, lse = A.combine_partials(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    o_ref, lse_ref = A.attention_fwd(q, k, v, False, s)
+    assert np.max(np.abs(o - o_ref)) < 1e-12 and np.max(np.abs(lse - lse_ref)) < 1e-12
+    # dropping a part's weight (averaging the parts instead) is far off
+    o_bad = np.mean(np.stack([p[0] for p in parts]), axis=0)
+    assert np.max(np.abs(o_bad - o_ref)) > 1e-2
+
+
+def test_combine_partials_causal_chunks():
+    # causal rows of query chunk i: full attention to earlier key chunks, the
+    # chunk-local causal mask on its own chunk, nothing from later chunks
+    rng = np.random.default_rng(5)
+    n, c = 48, 16
+    q, k, v = (rng.standard_normal((1, 2, n, 8)) for _ in range(3))
+    s = 0.5
+    o_ref, lse_ref = A.attention_fwd(q, k, v, True, s)
+    for i in range(n // c):
+        qs = q[:, :, i * c:(i + 1) * c]
+        parts = [A.attention_fwd(qs, k[:, :, j * c:(j + 1) * c], v[:, :, j * c:(j + 1) * c], False, s)
+                 for j in range(i)]
+        parts.append(A.attention_fwd(qs, k[:, :, i * c:(i + 1) * c], v[:, :, i * c:(i + 1) * c], True, s))
+        o, lse = A.combine_partials(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+        assert np.max(np.abs(o - o_ref[:, :, i * c:(i + 1) * c])) < 1e-12
+        assert np.max(np.abs(lse - lse_ref[:, :, i * c:(i + 1) * c])) < 1e-12
+
+
+def test_combine_partials_special_cases():
+    rng = np.random.default_rng(8)
+    o1, l1 = rng.standard_normal((1, 4, 6, 5)), rng.standard_normal((1, 4, 6)) * 4
+    # one part is itself
+    o, lse = A.combine_partials(o1, l1)
+    assert np.array_equal(o, o1[0]) and np.array_equal(lse, l1[0])
+    # a part without keys (LSE = -inf) adds nothing
+    o2 = rng.standard_normal((1, 4, 6, 5))
+    o, lse = A.combine_partials(np.concatenate([o1, o2]), np.concatenate([l1, np.full((1, 4, 6), -np.inf)]))
+    assert np.max(np.abs(o - o1[0])) < 1e-15 and np.array_equal(lse, l1[0])
+    # no keys at all
+    o, lse = A.combine_partials(o2, np.full((1, 4, 6), -np.inf))
+    assert np.all(o == 0) and np.all(lse == -np.inf)
+    # two equal parts: O unchanged, LSE + ln 2
+    o, lse = A.combine_partials(np.concatenate([o1, o1]), np.concatenate([l1, l1]))
+    assert np.max(np.abs(o - o1[0])) < 1e-14 and np.max(np.abs(lse - (l1[0] + math.log(2.0)))) < 1e-14
+    # merging in two steps equals merging at once (associativity of the exact merge)
+    o3, l3 = rng.standard_normal((1, 4, 6, 5)), rng.standard_normal((1, 4, 6)) * 4
+    oa, la = A.combine_partials(np.concatenate([o1, o2]), np.concatenate([l1, l3]))
+    ob, lb = A.combine_partials(np.stack([oa, o3[0]]), np.stack([la, l3[0] + 1.0]))
+    oc, lc = A.combine_partials(np.concatenate([o1, o2, o3]), np.concatenate([l1, l3, l3 + 1.0]))
+    assert np.max(np.abs(ob - oc)) < 1e-13 and np.max(np.abs(lb - lc)) < 1e-13
+
+
 def test_precision_bands():
     # fp32 recurrence ~1e-5 and bf16 inputs with bf16 P ~5e-3..1e-2 against float64
     g = read_golden_kv("exactness_bands.txt")
