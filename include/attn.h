@@ -108,6 +108,33 @@ attn_status_t attn_fwd_2cta(const void* q, const void* k, const void* v, void* o
                             int d, int causal, float scale, void* stream);
 
 /*
+ * attn_combine -- merges the results of attention over disjoint sets of keys
+ * (a sequence split: the same queries against key ranges computed apart, e.g.
+ * the key chunks of a context-parallel ring) into the result over all of
+ * them, with the exact two-block combine of "Lecture 2 - Online Softmax and
+ * Numerical Correctness", section "Combining two blocks exactly", applied to
+ * every part: m = max_p LSE_p, w_p = exp(LSE_p - m), l = sum_p w_p,
+ * O = sum_p w_p O_p / l (fp32 arithmetic, O rounded to bf16 once),
+ * LSE = m + ln l.
+ *
+ *   o_parts    bf16 [parts, B, H, N, d], contiguous: part p's O (as attn_fwd
+ *              writes it), 16-byte aligned
+ *   lse_parts  fp32 [parts, B, H, N], contiguous: part p's LSE; -inf marks a
+ *              part with no key for that row (it adds nothing, and its O row
+ *              may hold anything)
+ *   parts      1 .. 1024
+ *   o, lse     the merged O (bf16 [B, H, N, d], 16-byte aligned) and LSE (fp32
+ *              [B, H, N]); a row whose parts are all -inf gets O = 0 and
+ *              LSE = -inf. They may not overlap the inputs.
+ *   d          64 or 128 (other positive values: ATTN_ERR_UNSUPPORTED)
+ * With parts = 1 the output equals the input bit for bit. Errors:
+ * ATTN_ERR_INVALID_ARG (negative sizes, parts outside 1 .. 1024, null
+ * pointers on a non-empty problem), ATTN_ERR_MISALIGNED, ATTN_ERR_CUDA.
+ */
+attn_status_t attn_combine(const void* o_parts, const float* lse_parts, int parts, void* o, float* lse, int B, int H,
+                           int N, int d, void* stream);
+
+/*
  * attn_fwd_rescale_log -- attn_fwd_ex (software-exp2 share 0) that also
  * records every rescale decision, for checking them against the lagging-max
  * rule of "FlashAttention-4's Softmax Tricks", section "Conditional rescaling,

@@ -45,6 +45,9 @@ _SIGNATURES = {
                     + [ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_void_p], ctypes.c_int),
     # q, k, v, o, lse, B, H, N, d, causal, scale, stream
     "attn_fwd_2cta": ([ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_void_p], ctypes.c_int),
+    # o_parts, lse_parts, parts, o, lse, B, H, N, d, stream
+    "attn_combine": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+                     + [ctypes.c_int] * 4 + [ctypes.c_void_p], ctypes.c_int),
     # q, k, v, o, lse, rescale_log, rescale_log_bytes, B, H, N, d, causal, scale, tau, stream
     "attn_fwd_rescale_log": ([ctypes.c_void_p] * 6 + [ctypes.c_size_t] + [ctypes.c_int] * 5
                              + [ctypes.c_float, ctypes.c_float, ctypes.c_void_p], ctypes.c_int),
@@ -182,6 +185,28 @@ def attn_fwd_2cta(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: boo
         st = lib().attn_fwd_2cta(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(bool(causal)),
                                  float(scale), _stream_handle(stream))
         _check(st, "attn_fwd_2cta")
+    return o, lse
+
+
+def attn_combine(o_parts: torch.Tensor, lse_parts: torch.Tensor, o: torch.Tensor | None = None,
+                 lse: torch.Tensor | None = None, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Merge attention results over disjoint key sets: o_parts bf16 [P,B,H,N,d],
+    lse_parts float32 [P,B,H,N] (CUDA, contiguous) -> (o [B,H,N,d], lse [B,H,N])."""
+    if (not o_parts.is_cuda or o_parts.dtype != torch.bfloat16 or o_parts.dim() != 5
+            or not o_parts.is_contiguous()):
+        raise ValueError("o_parts must be a contiguous CUDA bfloat16 tensor [P,B,H,N,d]")
+    P, B, H, N, d = o_parts.shape
+    if (not lse_parts.is_cuda or lse_parts.dtype != torch.float32 or tuple(lse_parts.shape) != (P, B, H, N)
+            or not lse_parts.is_contiguous()):
+        raise ValueError("lse_parts must be a contiguous CUDA float32 tensor [P,B,H,N]")
+    if o is None:
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=o_parts.device)
+    with torch.cuda.device(o_parts.device):
+        st = lib().attn_combine(_ptr(o_parts), _ptr(lse_parts), P, _ptr(o), _ptr(lse), B, H, N, d,
+                                _stream_handle(stream))
+        _check(st, "attn_combine")
     return o, lse
 
 

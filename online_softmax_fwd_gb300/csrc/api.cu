@@ -26,6 +26,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr long long kMaxN = 1LL << 24;
+constexpr int kMaxCombineParts = 1024;
 // log2(448 / 256), rounded down: the largest tau for which P * 2^8 <= 448
 constexpr float kPConstMaxTau = 0.807f;
 // log2(57344 / 256), rounded down: the same bound for P held in E5M2
@@ -401,6 +402,23 @@ attn_status_t attn_fwd_2cta(const void* q, const void* k, const void* v, void* o
   }
   const cudaError_t e =
       attn::launch_fwd_bf16_d128_2cta(mq, mkh, mv, a, wl, clusters, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_combine(const void* o_parts, const float* lse_parts, int parts, void* o, float* lse, int B,
+                           int H, int N, int d, void* stream) {
+  if (B < 0 || H < 0 || N < 0 || parts < 1 || parts > kMaxCombineParts) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return d > 0 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (!o_parts || !lse_parts || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(o_parts) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(lse_parts) & 3u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return ATTN_ERR_MISALIGNED;
+  const int sms = sm_count();
+  if (sms <= 0) return ATTN_ERR_CUDA;
+  const long long rows = static_cast<long long>(B) * H * N;
+  const cudaError_t e =
+      attn::launch_attn_combine(o_parts, lse_parts, parts, rows, d, o, lse, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -46,6 +46,10 @@ cudaError_t launch_fwd_mxfp8_d128_ukv(int causal, const CUtensorMap& q, const CU
 // the rescale-logging instantiations (fwd_mxfp8_log.cu)
 cudaError_t launch_fwd_mxfp8_d128_log(int causal, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                       const FwdMxArgs& a, const WorkList& wl, int ctas, cudaStream_t s);
+// the merge of partial results over disjoint key sets (combine.cu); o_parts
+// [parts, rows, d] bf16, lse_parts [parts, rows] fp32, d = 64 or 128
+cudaError_t launch_attn_combine(const void* o_parts, const float* lse_parts, int parts, long long rows, int d,
+                                void* o, float* lse, int sms, cudaStream_t stream);
 // the bounded-wait self-test (selftest.cu)
 cudaError_t launch_wait_timeout_selftest(unsigned int* status, long long limit_cycles, cudaStream_t stream);
 

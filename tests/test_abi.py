@@ -248,3 +248,15 @@ def test_mxfp8_rescale_log_rejects_bad_arguments(lib):
     assert f(tau=-1.0) == 1 and f(tau=17.0) == 1
     assert f(d=64) == 2
     assert f(log=0, b=0) == 0
+
+
+def test_combine_rejects_bad_arguments(lib):
+    A = 1 << 20
+    f = lambda parts=3, d=128, b=1, o_parts=A, lse_parts=A * 2, o=A * 3, lse=A * 4: lib.attn_combine(
+        o_parts, lse_parts, parts, o, lse, b, 2, 300, d, None)
+    assert f(parts=0) == 1 and f(parts=1025) == 1 and f(parts=-2) == 1
+    assert f(d=96) == 2 and f(d=0) == 1
+    assert f(o_parts=0) == 1 and f(lse=0) == 1
+    assert f(o_parts=A + 8) == 3 and f(o=A * 3 + 2) == 3 and f(lse_parts=A * 2 + 1) == 3
+    assert f(b=-1) == 1
+    assert f(b=0, o_parts=0, lse=0) == 0   # empty problem: nothing to do, pointers unchecked
