@@ -54,6 +54,7 @@ KERNEL_SOURCES = {
               "online_softmax_fwd_gb300/csrc/fwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/ptx.cuh",
               "online_softmax_fwd_gb300/csrc/exp2_fma.cuh", "online_softmax_fwd_gb300/csrc/schedule.h",
               "online_softmax_fwd_gb300/csrc/schedule.cu"],
+    "combine": ["online_softmax_fwd_gb300/csrc/combine.cu", "online_softmax_fwd_gb300/csrc/ptx.cuh"],
     "bwd": ["online_softmax_fwd_gb300/csrc/bwd_bf16.cuh", "online_softmax_fwd_gb300/csrc/bwd_common.cuh",
             "online_softmax_fwd_gb300/csrc/kernel_setup.h",
             "online_softmax_fwd_gb300/csrc/bwd_aux.cu",
@@ -669,6 +670,79 @@ class BwdMxfp8Step:
                 "d2h_bytes_per_step": sum(h.numel() * 2 for h in outs), "steps": n_steps}
 
 
+class CombineStep:
+    """One merge (attn_combine) of `parts` partial results of a workload's
+    shape, inputs resident in HBM: O parts bf16 [P,B,H,N,d] and LSE parts fp32
+    [P,B,H,N], drawn on the device (N(0,1), the workload's seed)."""
+
+    launches = 1
+
+    def __init__(self, attn, w, dev, parts):
+        self.attn, self.w, self.parts = attn, w, parts
+        g = torch.Generator(device=dev).manual_seed(w.seed)
+        self.o_parts = torch.randn((parts, w.B, w.H, w.N, w.d), generator=g, device=dev).to(torch.bfloat16)
+        self.lse_parts = torch.randn((parts, w.B, w.H, w.N), generator=g, device=dev)
+        self.o = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+
+    def run(self, sh, ev=None):
+        w = self.w
+        if ev:
+            ev[0].record()
+        st = self.attn.lib().attn_combine(self.o_parts.data_ptr(), self.lse_parts.data_ptr(), self.parts,
+                                          self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N, w.d, sh)
+        if ev:
+            ev[1].record()
+        if st != 0:
+            raise self.attn.AttnError(st, "attn_combine")
+
+    def bytes_per_launch(self):
+        """Algorithmic bytes: every part's O row and LSE in, the merged ones out."""
+        rows = self.w.B * self.w.H * self.w.N
+        return (self.parts + 1) * rows * (2 * self.w.d + 4)
+
+    def input_bytes(self):
+        return self.o_parts.numel() * 2 + self.lse_parts.numel() * 4
+
+
+def combine_name(w: I.Workload, parts: int) -> str:
+    return f"combine_p{parts}_b{w.B}h{w.H}n{w.N}d{w.d}"
+
+
+def combine_record(attn, w: I.Workload, parts: int, dev, world: int, steps: int, warmup: int) -> dict:
+    """The merge of `parts` partial results of w's shape, timed like the
+    attention steps; bandwidth against the measured HBM copy rate."""
+    step = CombineStep(attn, w, dev, parts)
+    flush = None
+    l2_note = f"inputs larger than L2 ({step.input_bytes() / 2**20:.0f} MiB > 129 MB)"
+    if step.input_bytes() <= L2_BYTES:
+        scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        flush = scratch.zero_
+        l2_note = "inputs fit in L2: a 258 MB buffer is written between steps; value uses the per-launch events"
+    m = measure(step, dev, world, steps, warmup, flush)
+    launch_mean = float(np.mean(m["launch_ms"]))
+    nbytes = step.bytes_per_launch()
+    hbm = measured_peaks().get("hbm_gbs")
+    src = "measured hbm_gbs (copy)" if hbm else "fallback 6800 GB/s"
+    hbm = hbm or 6800.0
+    achieved = nbytes / (launch_mean * 1e-3) / 1e9
+    name = combine_name(w, parts)
+    rec = {"config": {"workload": name, "parts": parts, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                      "pass": "combine", "l2": l2_note},
+           "steps": steps, "warmup": warmup,
+           "value": nbytes * steps * world / (m["region_ms"] * 1e-3) / 1e9 if flush is None
+           else nbytes * world / (launch_mean * 1e-3) / 1e9,
+           "unit": "GB/s", "ms_per_step": m["region_ms"] / steps if flush is None else launch_mean,
+           "kernel_ms": kernel_ms_of(m["launch_ms"]),
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                        "traffic": profiled_traffic(name), "peak_source": src, "bytes_per_launch": nbytes,
+                        "kernel": "attn_combine_kernel"},
+           "clocks": m["clocks"], "gpu_launches": steps * step.launches}
+    del step
+    torch.cuda.empty_cache()
+    return rec
+
+
 def step_class(w: I.Workload):
     if w.direction == "bwd":
         return BwdMxfp8Step if w.dtype == "mxfp8" else BwdStep
@@ -797,7 +871,9 @@ def workload_suite(attn, args, dev, world: int) -> dict:
     """Every forward workload besides the headline one, each timed on its own:
     the tiny one, the causal d = 128 one (Q, K ~ N(0, 2^2)), the causal d = 64
     one with the MUFU alone and with each software-exp2 share (the best share
-    reported beside it), and the MXFP8 one with the quantiser's share."""
+    reported beside it), the headline shape on CTA pairs, the MXFP8 one with
+    the quantiser's share (on both schedules), and the merge of four partial
+    results of the headline shape (bandwidth against the HBM copy rate)."""
     steps, warmup = args.suite_steps, max(3, args.warmup)
     out = {}
     out[I.TINY.name] = sub_record(attn, I.TINY, dev, world, _Opts(args, exp2_emu16=0), steps, warmup)
@@ -819,6 +895,8 @@ def workload_suite(attn, args, dev, world: int) -> dict:
                                                       _Opts(args, exp2_emu16=0, two_cta=True), steps, warmup)
     out[I.MXFP8_CAUSAL.name] = sub_record(attn, I.MXFP8_CAUSAL, dev, world,
                                           _Opts(args, exp2_emu16=0, p_scaling=0), steps, warmup)
+    # the merge of four partial results of the non-causal d = 128 shape (a sequence split over four ranks)
+    out[combine_name(I.NONCAUSAL_D128, 4)] = combine_record(attn, I.NONCAUSAL_D128, 4, dev, world, steps, warmup)
     # the same on the unroll-KV schedule (attn_fwd_mxfp8_unroll_kv)
     out[I.MXFP8_CAUSAL.name + "_unroll_kv"] = sub_record(attn, I.MXFP8_CAUSAL, dev, world,
                                                          _Opts(args, exp2_emu16=0, p_scaling=0, unroll_kv=True),
@@ -900,6 +978,8 @@ def main() -> None:
                     help="B,H,N,d[,causal[,mxfp8[,bwd]]] instead of a named workload (profiling a smaller case)")
     ap.add_argument("--qk-std", type=float, default=1.0,
                     help="standard deviation of Q and K for --shape (the causal d128 workload uses 2)")
+    ap.add_argument("--combine", type=int, default=0, metavar="P",
+                    help="time only attn_combine merging P partial results of the workload's shape and print its record")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--exp2-emu16", type=int, default=0)
     ap.add_argument("--tau", type=float, default=None,
@@ -935,6 +1015,14 @@ def main() -> None:
                        f[0], f[1], f[2], f[3], causal, dtype=dt, direction=direction, qk_std=args.qk_std)
     world, rank, local = dist_setup(args.gpus)
     try:
+        if args.combine:
+            import online_softmax_fwd_gb300 as attn
+            dev = torch.device("cuda", local)
+            torch.cuda.set_device(dev)
+            rec = combine_record(attn, w, args.combine, dev, world, args.steps, args.warmup)
+            if rank == 0:
+                print(json.dumps(rec), flush=True)
+            return
         if args.impl == "reference":
             bench_reference(args, w, world, rank)
         else:
