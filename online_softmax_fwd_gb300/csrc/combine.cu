@@ -61,9 +61,10 @@ __device__ __forceinline__ void accumulate(float (&acc)[CPL], float w, const Vec
   }
 }
 
-// CPL = columns per lane (d / 32: 2 for d = 64, 4 for d = 128); RPW = rows a
-// warp merges at a time (their loads are in flight together).
-template <int CPL, int RPW>
+// CPL = columns per lane (d / 32: 2 for d = 64, 4 for d = 128). One row per
+// warp at a time: two or four rows per warp (more loads in flight) measured
+// the same, so the loads in flight are not what limits it.
+template <int CPL>
 __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __nv_bfloat16* __restrict__ o_parts,
                                                                        const float* __restrict__ lse_parts,
                                                                        int parts, long long rows,
@@ -72,112 +73,81 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __n
   constexpr int D = 32 * CPL;
   using Vec = typename std::conditional<CPL == 4, uint2, uint32_t>::type;
   const int lane = threadIdx.x & 31;
-  const long long warp_id = static_cast<long long>(blockIdx.x) * (kCombineThreads / 32) + (threadIdx.x >> 5);
   const long long warps = static_cast<long long>(gridDim.x) * (kCombineThreads / 32);
   const long long part_step = rows * 32;  // Vec units (d / 32 columns each) between the parts' rows
-  for (long long row0 = warp_id * RPW; row0 < rows; row0 += warps * RPW) {
-    float acc[RPW][CPL];
-    float m[RPW], l[RPW];
+  for (long long row = static_cast<long long>(blockIdx.x) * (kCombineThreads / 32) + (threadIdx.x >> 5); row < rows;
+       row += warps) {
+    const Vec* src = reinterpret_cast<const Vec*>(o_parts + row * D) + lane;
+    float acc[CPL];
 #pragma unroll
-    for (int r = 0; r < RPW; ++r)
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) acc[r][c] = 0.f;
+    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+    float m, l;
     if (parts <= 32) {
-      // up to 32 parts: the first eight parts' rows of all RPW rows are
-      // requested before the LSEs (one per lane) are read and reduced
-      Vec x[RPW][8];
+      // up to 32 parts: the first eight parts' rows are requested before the
+      // LSEs (one per lane) are read and reduced, so the loads overlap that
+      Vec x[8];
 #pragma unroll
-      for (int r = 0; r < RPW; ++r) {
-        const Vec* src = reinterpret_cast<const Vec*>(o_parts + (row0 + r) * D) + lane;
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (i < parts && row0 + r < rows) x[r][i] = src[i * part_step];
-      }
-      float w[RPW];
-#pragma unroll
-      for (int r = 0; r < RPW; ++r) {
-        const float lp =
-            (lane < parts && row0 + r < rows) ? lse_parts[static_cast<long long>(lane) * rows + row0 + r] : -INFINITY;
-        m[r] = warp_max(lp);
-        // w_p = exp(LSE_p - m): 1 for the largest part, 0 for a part without keys
-        w[r] = m[r] == -INFINITY ? 0.f : ex2_mufu((lp - m[r]) * kLog2e);
-        l[r] = warp_sum(w[r]);
-      }
+      for (int i = 0; i < 8; ++i)
+        if (i < parts) x[i] = src[i * part_step];
+      const float lp = lane < parts ? lse_parts[static_cast<long long>(lane) * rows + row] : -INFINITY;
+      m = warp_max(lp);
+      // w_p = exp(LSE_p - m): 1 for the largest part, 0 for a part without keys
+      const float w = m == -INFINITY ? 0.f : ex2_mufu((lp - m) * kLog2e);
+      l = warp_sum(w);
       for (int c0 = 0; c0 < parts; c0 += 8) {
         if (c0 > 0) {
 #pragma unroll
-          for (int r = 0; r < RPW; ++r) {
-            const Vec* src = reinterpret_cast<const Vec*>(o_parts + (row0 + r) * D) + lane;
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (c0 + i < parts && row0 + r < rows) x[r][i] = src[(c0 + i) * part_step];
-          }
+          for (int i = 0; i < 8; ++i)
+            if (c0 + i < parts) x[i] = src[(c0 + i) * part_step];
         }
 #pragma unroll
-        for (int r = 0; r < RPW; ++r)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (c0 + i < parts) {
-              // a part without keys is skipped, whatever its O holds
-              const float wi = __shfl_sync(0xffffffffu, w[r], c0 + i);
-              if (wi != 0.f) accumulate<CPL>(acc[r], wi, x[r][i]);
-            }
+        for (int i = 0; i < 8; ++i) {
+          if (c0 + i < parts) {
+            // a part without keys is skipped, whatever its O holds
+            const float wi = __shfl_sync(0xffffffffu, w, c0 + i);
+            if (wi != 0.f) accumulate<CPL>(acc, wi, x[i]);
           }
+        }
       }
     } else {
-      // more parts: each row's largest LSE first, 32 parts per step
-#pragma unroll
-      for (int r = 0; r < RPW; ++r) {
-        if (row0 + r >= rows) {
-          m[r] = -INFINITY;
-          l[r] = 0.f;
-          continue;
-        }
-        const long long row = row0 + r;
-        const Vec* src = reinterpret_cast<const Vec*>(o_parts + row * D) + lane;
-        float mp = -INFINITY;
-        for (int p0 = 0; p0 < parts; p0 += 32) {
-          const int p = p0 + lane;
-          if (p < parts) mp = fmaxf(mp, lse_parts[static_cast<long long>(p) * rows + row]);
-        }
-        m[r] = warp_max(mp);
-        float lw = 0.f;
-        for (int p0 = 0; p0 < parts; p0 += 32) {
-          const int p = p0 + lane;
-          const float wp = (p < parts && m[r] != -INFINITY)
-                               ? ex2_mufu((lse_parts[static_cast<long long>(p) * rows + row] - m[r]) * kLog2e)
-                               : 0.f;
-          lw += wp;
-          const int np = parts - p0 < 32 ? parts - p0 : 32;
+      // more parts: the largest LSE first, 32 parts per step
+      float mp = -INFINITY;
+      for (int p0 = 0; p0 < parts; p0 += 32) {
+        const int p = p0 + lane;
+        if (p < parts) mp = fmaxf(mp, lse_parts[static_cast<long long>(p) * rows + row]);
+      }
+      m = warp_max(mp);
+      float lw = 0.f;
+      for (int p0 = 0; p0 < parts; p0 += 32) {
+        const int p = p0 + lane;
+        const float w = (p < parts && m != -INFINITY)
+                            ? ex2_mufu((lse_parts[static_cast<long long>(p) * rows + row] - m) * kLog2e)
+                            : 0.f;
+        lw += w;
+        const int np = parts - p0 < 32 ? parts - p0 : 32;
 #pragma unroll 4
-          for (int i = 0; i < np; ++i) {
-            const float wi = __shfl_sync(0xffffffffu, wp, i);
-            if (wi != 0.f) accumulate<CPL>(acc[r], wi, src[(p0 + i) * part_step]);
-          }
+        for (int i = 0; i < np; ++i) {
+          const float wi = __shfl_sync(0xffffffffu, w, i);
+          if (wi != 0.f) accumulate<CPL>(acc, wi, src[(p0 + i) * part_step]);
         }
-        l[r] = warp_sum(lw);
       }
+      l = warp_sum(lw);
     }
+    Vec* orow = reinterpret_cast<Vec*>(o + row * D) + lane;
+    uint32_t out[CPL / 2];
+    if (m == -INFINITY) {  // no part has a key for this row
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-      const long long row = row0 + r;
-      if (row >= rows) break;
-      Vec* orow = reinterpret_cast<Vec*>(o + row * D) + lane;
-      uint32_t out[CPL / 2];
-      if (m[r] == -INFINITY) {  // no part has a key for this row
+      for (int c = 0; c < CPL / 2; ++c) out[c] = 0u;
+    } else {
+      const float inv_l = 1.0f / l;
 #pragma unroll
-        for (int c = 0; c < CPL / 2; ++c) out[c] = 0u;
-      } else {
-        const float inv_l = 1.0f / l[r];
-#pragma unroll
-        for (int c = 0; c < CPL / 2; ++c) out[c] = pack_bf16x2(acc[r][2 * c] * inv_l, acc[r][2 * c + 1] * inv_l);
-      }
-      if constexpr (CPL == 4)
-        *orow = make_uint2(out[0], out[1]);
-      else
-        *orow = out[0];
-      if (lane == 0) lse[row] = m[r] == -INFINITY ? -INFINITY : m[r] + lg2_mufu(l[r]) * kLn2;
+      for (int c = 0; c < CPL / 2; ++c) out[c] = pack_bf16x2(acc[2 * c] * inv_l, acc[2 * c + 1] * inv_l);
     }
+    if constexpr (CPL == 4)
+      *orow = make_uint2(out[0], out[1]);
+    else
+      *orow = out[0];
+    if (lane == 0) lse[row] = m == -INFINITY ? -INFINITY : m + lg2_mufu(l) * kLn2;
   }
 }
 
@@ -185,17 +155,14 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __n
 
 cudaError_t launch_attn_combine(const void* o_parts, const float* lse_parts, int parts, long long rows, int d,
                                 void* o, float* lse, int sms, cudaStream_t stream) {
-  // one row per warp at a time: two or four rows per warp measured the same
-  // (the loads already in flight are not what limits it)
-  const int rpw = 1;
-  const long long want = (rows + rpw * (kCombineThreads / 32) - 1) / (rpw * (kCombineThreads / 32));
+  const long long want = (rows + kCombineThreads / 32 - 1) / (kCombineThreads / 32);
   const long long cap = static_cast<long long>(sms > 0 ? sms : 1) * 16;
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
   if (d == 128)
-    attn_combine_kernel<4, 1><<<grid, kCombineThreads, 0, stream>>>(
+    attn_combine_kernel<4><<<grid, kCombineThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(o_parts), lse_parts, parts, rows, static_cast<__nv_bfloat16*>(o), lse);
   else
-    attn_combine_kernel<2, 1><<<grid, kCombineThreads, 0, stream>>>(
+    attn_combine_kernel<2><<<grid, kCombineThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(o_parts), lse_parts, parts, rows, static_cast<__nv_bfloat16*>(o), lse);
   return cudaGetLastError();
 }
